@@ -1,0 +1,56 @@
+"""Planted mistakes in the oracle must be caught by its pins.
+
+Each case copies oracle/oracle.cpp, plants one plausible mistake (a dropped term,
+a wrong sign or index, a transposed operand), compiles the copy on the CPU and
+runs the pins against it: at least one pin must fail.
+"""
+import os
+
+import pytest
+
+import oracle
+from oracle_pins import ALL_PINS
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.cpp")
+
+MUTANTS = {
+    "kv_head_modulo": ("int kvh = h / (p.Hq / p.Hkv);", "int kvh = h % p.Hkv;"),
+    "scale_dropped": ("s[j - lo] = p.scale * acc;", "s[j - lo] = acc;"),
+    "split_start_ceil": ("*lo = L * s / S;", "*lo = (L * s + S - 1) / S;"),
+    "split_end_ceil": ("*hi = L * (s + 1) / S;", "*hi = (L * (s + 1) + S - 1) / S;"),
+    "merge_weight_sign": ("double w = std::exp(ls[s] - tot);", "double w = std::exp(tot - ls[s]);"),
+    "lse_max_dropped": ("*lse = m + std::log(z);", "*lse = std::log(z);"),
+    "split_lse_max_dropped": ("double l = m + std::log(z);", "double l = std::log(z);"),
+    "bhsd_heads_batch_swapped": ("(((int64_t)b * p.Hkv + kvh) * p.kv_rows + j)",
+                                 "(((int64_t)kvh * p.B + b) * p.kv_rows + j)"),
+    "varlen_rows_heads_swapped": ("(((int64_t)p.cu[b] + j) * p.Hkv + kvh)",
+                                  "((int64_t)kvh * p.kv_rows + p.cu[b] + j)"),
+    "f16_exponent_bias": ("e - 25);", "e - 24);"),
+    "bf16_exponent_bias": ("e - 134);", "e - 133);"),
+    "softmax_not_normalized": ("double pj = s[j] / z;", "double pj = s[j];"),
+    "max_not_subtracted": ("s[j] = std::exp(s[j] - m);", "s[j] = std::exp(s[j]);"),
+    "q_row_transposed": ("((int64_t)b * p.Hq + h) * p.D", "((int64_t)h * p.B + b) * p.D"),
+    "merge_skips_last_split": ("for (int s = 0; s < S; ++s) {\n            if (ls[s] == kNegInf) continue;",
+                               "for (int s = 0; s + 1 < S; ++s) {\n            if (ls[s] == kNegInf) continue;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    count = src.count(old)
+    assert count >= 1, f"mutation site for {name} not found"
+    mutated = src.replace(old, new)
+    path = tmp_path / "oracle_mutant.cpp"
+    path.write_text(mutated)
+    lib = oracle.load_library(oracle.compile_library(str(path), str(tmp_path / "libmut.so")))
+    orc = oracle.Oracle(lib)
+    failed = []
+    for pin in ALL_PINS:
+        try:
+            pin(orc)
+        except (AssertionError, ValueError, FloatingPointError):
+            failed.append(pin.__name__)
+            break
+    assert failed, f"planted mistake {name} passed every pin"
