@@ -1,0 +1,389 @@
+"""Benchmark: split-KV decode attention on one GB300 (or N replicas under torchrun).
+
+Prints ONE JSON line (rank 0). A step is one decode-attention call over the whole
+workload: the split kernel then the combine kernel, launched through the C ABI
+(decode_attn_splitkv_partial + decode_attn_splitkv_combine are exactly the two
+launches decode_attn_splitkv makes; timing them apart gives the per-kernel
+durations). L2 is flushed between steps by writing a buffer twice its size.
+
+  value      KV-read GB/s = 2 * sum(L_b) * Hkv * D * 2 bytes / mean step time
+  e2e        the same metric through decode_attn_splitkv with the inputs copied
+             host->device (pinned) and the output copied back inside each step
+  roofline   the split kernel: algorithmic bytes per launch / its mean event time,
+             against the measured HBM copy bandwidth
+  cpu_baseline  the float64 oracle on the host cores, on a bounded sample
+
+--impl reference times the float64 CPU oracle alone (there is no other
+implementation of this method to run) on the same workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn µs/call and KV-read HBM GB/s (% of GB300 peak)"
+DEFAULT_WORKLOAD = "mha_bhsd"
+CU_SRC = os.path.join(ROOT, "split_kv_decode_decoding_gb300", "csrc", "decode_attn_splitkv.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--splits", type=int, default=0, help="override the split-count picker")
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-flush", action="store_true", help="do not flush L2 between steps")
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sha() -> str:
+    with open(CU_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, S: int):
+    """DRAM bytes per split-kernel launch from a committed ncu capture, if it is current."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    for e in d.get("entries", []):
+        if e.get("kernel_sha") == kernel_sha() and e.get("workload") == workload and e.get("num_splits") == S:
+            return float(e["dram_bytes_per_launch"])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def problem_tensors(p, device):
+    import numpy as np
+    import torch
+    dt = torch.float16 if p.dtype == "f16" else torch.bfloat16
+
+    def host(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(dt)
+
+    return host(p.q), host(p.k), host(p.v), torch.from_numpy(p.cu.astype(np.int32))
+
+
+def cpu_oracle_sample(p, budget_s: float = 12.0, steps=None):
+    """Time the float64 oracle on (b, h) rows of the workload: returns (GB/s, cores, desc, per-step s)."""
+    import numpy as np
+
+    import oracle
+    orc = oracle.default()
+    cores = os.cpu_count() or 1
+    rows_b = np.repeat(np.arange(p.B), p.Hq).astype(np.int32)
+    rows_h = np.tile(np.arange(p.Hq), p.B).astype(np.int32)
+    nrows = rows_b.size
+    # probe one row per thread to size the sample
+    probe = min(nrows, cores)
+    t0 = time.perf_counter()
+    orc.attention_rows(p, rows_b[:probe], rows_h[:probe], nthreads=cores)
+    t_probe = max(time.perf_counter() - t0, 1e-6)
+    per_row = t_probe / probe * cores          # CPU-seconds per row
+    if steps is None:
+        want = int(budget_s * cores / per_row)
+        n = max(probe, min(nrows, want))
+        sel = np.linspace(0, nrows - 1, n).astype(np.int64)
+        t0 = time.perf_counter()
+        orc.attention_rows(p, rows_b[sel], rows_h[sel], nthreads=cores)
+        dt = time.perf_counter() - t0
+        frac = n / nrows
+        gbs = p.kv_bytes * frac / dt / 1e9
+        desc = (f"{n} of {nrows} (b, h) rows of {p.name} (full key ranges), float64, "
+                f"{cores} threads, {dt:.2f} s wall")
+        return gbs, cores, desc, dt
+    budget_per_step = budget_s / steps
+    n = max(1, min(nrows, int(budget_per_step * cores / per_row)))
+    return n, nrows, cores
+
+
+def run_reference(args, p, ws_, rank):
+    """--impl reference: the float64 oracle alone, each step a bounded sample of rows."""
+    import numpy as np
+
+    import oracle
+    if rank != 0:
+        return None
+    orc = oracle.default()
+    n, nrows, cores = cpu_oracle_sample(p, budget_s=150.0, steps=args.steps + args.warmup)
+    rows_b = np.repeat(np.arange(p.B), p.Hq).astype(np.int32)
+    rows_h = np.tile(np.arange(p.Hq), p.B).astype(np.int32)
+    times = []
+    for i in range(args.warmup + args.steps):
+        sel = (np.arange(n) * (nrows // n) + i) % nrows
+        t0 = time.perf_counter()
+        orc.attention_rows(p, rows_b[sel], rows_h[sel], nthreads=cores)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    frac = n / nrows
+    step = sum(times) / len(times)
+    value = p.kv_bytes * frac / step / 1e9
+    sample = (f"{n} of {nrows} (b, h) rows per step of {p.name}, float64 oracle, {cores} threads")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(step * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(p, None),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def workload_config(p, S):
+    return {"workload": p.name, "batch": p.B, "q_heads": p.Hq, "kv_heads": p.Hkv,
+            "head_dim": p.D, "kv_lens": (p.lens[0] if len(set(p.lens)) == 1 else
+                                         f"{min(p.lens)}..{max(p.lens)} (mean {sum(p.lens) / len(p.lens):.0f})"),
+            "layout": "bhsd" if p.layout == 1 else "varlen", "in_dtype": p.dtype,
+            "num_splits": S, "kv_bytes": p.kv_bytes,
+            "l2": "flushed between steps (write of 2x L2 size)"}
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_env()
+    from synth.workloads import workload
+    p = workload(args.workload)
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo" if args.impl == "reference" else "nccl")
+
+    if args.impl == "reference":
+        line = run_reference(args, p, world, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    import torch
+
+    import split_kv_decode_decoding_gb300 as da
+    da.build()
+    da.load()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+
+    S = args.splits or p.num_splits or da.num_splits(p.B, p.Hq, p.Hkv, p.D, min(p.lens), max(p.lens))
+    hq, hk, hv, hcu = problem_tensors(p, dev)
+    q, k, v, cu = hq.to(dev), hk.to(dev), hv.to(dev), hcu.to(dev)
+    out = torch.empty(p.B, p.Hq, p.D, dtype=q.dtype, device=dev)
+    ws = da.alloc_workspace(p.B, p.Hq, p.D, S, device=dev, stream=stream)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 64 << 20), dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize(dev)
+
+    def step(ev0=None, ev1=None, ev2=None):
+        if not args.no_flush:
+            flush.fill_(1)
+        if ev0 is not None:
+            ev0.record(stream)
+        da.decode_attn_splitkv_partial(q, k, v, cu, ws, num_splits=S, scale=p.scale,
+                                       layout=p.layout, stream=stream)
+        if ev1 is not None:
+            ev1.record(stream)
+        da.decode_attn_splitkv_combine(out, ws, num_splits=S, stream=stream)
+        if ev2 is not None:
+            ev2.record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize(dev)
+        if da.decode_attn_splitkv_get_error(ws, stream=stream) != 0:
+            raise RuntimeError("device error flag set during warm-up")
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+        sampler = ClockSampler(local) if not args.no_clocks else None
+        if sampler:
+            sampler.__enter__()
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            step(*evs[i])
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall
+        if sampler:
+            sampler.__exit__(None, None, None)
+        if world > 1:
+            torch.distributed.barrier()
+    if da.decode_attn_splitkv_get_error(ws, stream=stream) != 0:
+        raise RuntimeError("device error flag set during the timed steps")
+    split_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(args.steps)]
+    comb_ms = [evs[i][1].elapsed_time(evs[i][2]) for i in range(args.steps)]
+    step_ms = [evs[i][0].elapsed_time(evs[i][2]) for i in range(args.steps)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    mean_step_ms = total_ms / args.steps
+    value = world * p.kv_bytes / (mean_step_ms * 1e-3) / 1e9
+
+    # ---- end to end through the public call, host buffers, copies inside each step
+    e2e = None
+    if args.e2e_steps > 0:
+        pq, pk, pv, pcu = hq.pin_memory(), hk.pin_memory(), hv.pin_memory(), hcu.pin_memory()
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+        def e2e_step():
+            q.copy_(pq, non_blocking=True)
+            k.copy_(pk, non_blocking=True)
+            v.copy_(pv, non_blocking=True)
+            cu.copy_(pcu, non_blocking=True)
+            da.decode_attn_splitkv(q, k, v, cu, out, ws, num_splits=S, scale=p.scale,
+                                   layout=p.layout, stream=stream)
+            hout.copy_(out, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                e2e_step()
+            torch.cuda.synchronize(dev)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(args.e2e_steps):
+                e2e_step()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+        h2d = sum(t.numel() * t.element_size() for t in (pq, pk, pv, pcu))
+        e2e = {"value": round(world * p.kv_bytes / (e2e_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+               "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": hout.numel() * hout.element_size(),
+               "api": "decode_attn_splitkv (C ABI), pinned host buffers"}
+
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peaks()
+    split_mean_ms = sum(split_ms) / len(split_ms)
+    ws_bytes = p.B * p.Hq * S * (p.D + 1) * 4
+    q_bytes = p.B * p.Hq * p.D * 2
+    alg_bytes = p.kv_bytes + q_bytes + 4 * (p.B + 1) + ws_bytes
+    achieved = alg_bytes / (split_mean_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(p.name, S)
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_step_ms, 5),
+        "us_per_call": round(mean_step_ms * 1e3, 2),
+        "us_per_call_median": round(statistics.median(step_ms) * 1e3, 2),
+        "pct_of_hbm_peak": round(100.0 * value / world / peak, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": p.dtype, "data": "synthetic (seeded N(0,1), rounded to the input dtype)",
+        "config": workload_config(p, S),
+        "roofline": {"kernel": "split_kernel", "bound": "hbm", "achieved": round(achieved, 2),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "traffic": traffic, "alg_bytes_per_launch": alg_bytes,
+                     "launch_us_mean": round(split_mean_ms * 1e3, 2),
+                     "combine_us_mean": round(sum(comb_ms) / len(comb_ms) * 1e3, 2)},
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "wall_s_timed_region": round(t_wall, 3),
+    }
+    if sampler:
+        line["clocks"] = sampler.summary()
+    if not args.no_cpu_baseline and world == 1:
+        gbs, cores, desc, _ = cpu_oracle_sample(p)
+        line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores,
+                                "kind": "oracle", "sample": desc}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,193 @@
+/*
+ * decode_attn_splitkv.h -- split-KV decode attention (flash-decoding) for
+ * NVIDIA GB300 (sm_103a), as a plain C ABI.
+ *
+ * The operation. One decode step: each of B sequences has one query token
+ * with Hq query heads; its KV cache has Hkv heads (Hq % Hkv == 0, group size
+ * G = Hq / Hkv) and L_b = cu_seqlens_k[b+1] - cu_seqlens_k[b] keys. Query head
+ * h reads KV head h / G (the cur_kv_head rule of the TileLang tutorial page
+ * decode_attention_splitkv.py, split segment). With s_j = scale * q_h . k_j,
+ *
+ *     out[b,h,:] = sum_j softmax(s)_j * v_j                      (j < L_b)
+ *
+ * (MiniInfer flash_decode_splitk.py, flash_decode_reference). The library
+ * computes it the flash-decoding way: each sequence's key range is cut into
+ * num_splits proportional pieces, split s covering
+ *
+ *     [floor(L_b * s / S), floor(L_b * (s+1) / S))
+ *
+ * (TileLang page, split segment, proportional split bounds). One CTA per
+ * (sequence, KV head, split) computes, for every packed query head of that KV
+ * head, the normalised partial output o_s and lse_s = ln sum_{j in s} exp(s_j);
+ * a combine step then merges them exactly:
+ *
+ *     lse = ln sum_s exp(lse_s),   out = sum_s exp(lse_s - lse) * o_s
+ *
+ * (CS349E lecture 11, 04_flash_decoding.py, demo1_exact, first observation;
+ * TileLang page, combine segment). An empty split (only possible when a
+ * caller forces num_splits > L_b) has lse_s = -inf, o_s = 0 and weight 0, as
+ * in the MiniInfer reduce kernel; a sequence with L_b = 0 gets out = 0.
+ *
+ * Conventions for every entry point below.
+ *  - Pointers named "device" must be device memory of the current CUDA
+ *    device; nothing is copied or allocated by the library, and nothing is
+ *    retained after the call returns.
+ *  - `stream` is a cudaStream_t (a CUstream) passed as void*; NULL means the
+ *    legacy default stream. Device work is enqueued on it asynchronously; no
+ *    entry point synchronises unless it says so.
+ *  - Host-side checks run first; a call that returns anything but DA_OK has
+ *    enqueued no device work.
+ *  - Input and output elements are IEEE binary16 (DA_F16) or bfloat16
+ *    (DA_BF16) values; accumulation is float32.
+ */
+#ifndef DECODE_ATTN_SPLITKV_H
+#define DECODE_ATTN_SPLITKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DA_OK = 0,
+    DA_ERR_INVALID_ARG = 1,         /* a size, count or pointer is out of range or NULL */
+    DA_ERR_UNSUPPORTED = 2,         /* head_dim other than 64/128, or no sm_103a device */
+    DA_ERR_ALIGNMENT = 3,           /* a pointer is not aligned as documented */
+    DA_ERR_WORKSPACE_TOO_SMALL = 4, /* workspace_bytes < decode_attn_splitkv_workspace_size() */
+    DA_ERR_CUDA = 5                 /* a CUDA runtime or driver call failed */
+} da_status;
+
+typedef enum { DA_F16 = 0, DA_BF16 = 1 } da_dtype;
+
+typedef enum {
+    /* K, V: [kv_rows, Hkv, D] row-major; sequence b owns rows
+       cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1 (kv_rows = total_kv). */
+    DA_LAYOUT_VARLEN = 0,
+    /* K, V: [B, Hkv, kv_rows, D] row-major; sequence b owns positions
+       0 .. L_b-1 of its own [kv_rows, D] slab per KV head (kv_rows is the
+       per-sequence capacity; L_b still comes from cu_seqlens_k). */
+    DA_LAYOUT_BHSD = 1
+} da_layout;
+
+/* Bits of the device error word (see decode_attn_splitkv_get_error). */
+#define DA_DEVERR_SEQLENS 0x1u /* a sequence's cu_seqlens_k range fell outside K/V; it was treated as empty */
+#define DA_DEVERR_TIMEOUT 0x2u /* a pipeline wait exceeded its time limit; the outputs of that call are invalid */
+
+/* Largest num_splits accepted. */
+#define DA_MAX_SPLITS 1024
+
+/*
+ * Workspace layout (all offsets from the workspace base, which must be
+ * 256-byte aligned):
+ *   [0, 256)            header: uint32 device error word at offset 0, rest reserved
+ *   [256, 256 + A)      lse_part, float32 [B, Hq, num_splits], natural log of the
+ *                       scaled scores, A = round_up(B*Hq*num_splits*4, 256)
+ *   [256 + A, total)    o_part, float32 [B, Hq, num_splits, D], normalised per split
+ * Returns the total size in bytes, or 0 if an argument is out of range.
+ */
+size_t decode_attn_splitkv_workspace_size(int B, int Hq, int D, int num_splits);
+
+/* Byte offsets of lse_part and o_part inside the workspace (layout above). */
+size_t decode_attn_splitkv_lse_offset(void);
+size_t decode_attn_splitkv_opart_offset(int B, int Hq, int num_splits);
+
+/*
+ * Zero the workspace header (the device error word). Call once on a freshly
+ * allocated workspace before its first use. Enqueued on `stream`.
+ * Errors: DA_ERR_INVALID_ARG (NULL, or fewer than 256 bytes),
+ * DA_ERR_ALIGNMENT (not 256-byte aligned), DA_ERR_CUDA.
+ */
+da_status decode_attn_splitkv_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Split-count picker (host only, enqueues nothing). Chooses num_splits for a
+ * batch whose KV lengths lie in [min_kv, max_kv] so that the split step's CTAs
+ * (B * Hkv * ceil(G/8) * num_splits of them) cover the GPU's SMs several times
+ * over, while every split keeps at least a minimum number of keys and no split
+ * is empty (num_splits <= min_kv; the TileLang page's scheduling constraint,
+ * split kernel docstring). sm_count 0 means: query the current device.
+ * Returns a value in [1, DA_MAX_SPLITS]; 1 when min_kv <= 0 or an argument is
+ * out of range.
+ */
+int decode_attn_splitkv_num_splits(int B, int Hq, int Hkv, int D, int min_kv, int max_kv,
+                                   int sm_count);
+
+/* Split s of num_splits over a length-L sequence: [*start, *end) (host helper). */
+void decode_attn_splitkv_split_range(int64_t L, int num_splits, int s, int64_t* start,
+                                     int64_t* end);
+
+/*
+ * The whole decode attention: the split step, then the combine step, both on
+ * `stream`.
+ *   q              device, [B, Hq, D] elements of `dtype`, 16-byte aligned
+ *   k, v           device, layout per `layout` (above), 16-byte aligned; may be
+ *                  NULL only when kv_rows == 0
+ *   cu_seqlens_k   device, int32 [B+1], non-decreasing; 4-byte aligned. Entries
+ *                  outside the K/V extent set DA_DEVERR_SEQLENS on the device
+ *                  and that sequence is treated as empty (never read out of bounds)
+ *   B, Hq, Hkv     >= 1, Hq % Hkv == 0
+ *   D              64 or 128
+ *   kv_rows        >= 0: total_kv (VARLEN) or the per-sequence capacity (BHSD)
+ *   scale          finite; the scores are scale * q . k (1/sqrt(D) is usual)
+ *   num_splits     in [1, DA_MAX_SPLITS]; values above a sequence's length
+ *                  stay exact (the extra splits are empty)
+ *   out            device, [B, Hq, D] elements of `dtype`, 16-byte aligned,
+ *                  rounded to nearest-even from float32
+ *   workspace      device, >= decode_attn_splitkv_workspace_size(B,Hq,D,num_splits)
+ *                  bytes, 256-byte aligned, initialised once (workspace_init);
+ *                  after the call it holds the per-split lse_part and o_part
+ * Errors (host-side, nothing enqueued): DA_ERR_INVALID_ARG, DA_ERR_UNSUPPORTED,
+ * DA_ERR_ALIGNMENT, DA_ERR_WORKSPACE_TOO_SMALL; DA_ERR_CUDA if a launch fails.
+ */
+da_status decode_attn_splitkv(const void* q, const void* k, const void* v,
+                              const int32_t* cu_seqlens_k, int B, int Hq, int Hkv, int D,
+                              int kv_rows, da_dtype dtype, da_layout layout, float scale,
+                              int num_splits, void* out, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/*
+ * The split step alone: fills lse_part and o_part in the workspace (layout
+ * above). Same arguments and errors as decode_attn_splitkv, without `out`.
+ */
+da_status decode_attn_splitkv_partial(const void* q, const void* k, const void* v,
+                                      const int32_t* cu_seqlens_k, int B, int Hq, int Hkv,
+                                      int D, int kv_rows, da_dtype dtype, da_layout layout,
+                                      float scale, int num_splits, void* workspace,
+                                      size_t workspace_bytes, void* stream);
+
+/*
+ * The combine step alone: merges lse_part/o_part from the workspace into
+ * out[B, Hq, D]. The workspace must hold a split step's results for the same
+ * B, Hq, D and num_splits. Errors as above.
+ */
+da_status decode_attn_splitkv_combine(int B, int Hq, int D, int num_splits, da_dtype dtype,
+                                      void* out, const void* workspace, size_t workspace_bytes,
+                                      void* stream);
+
+/*
+ * Read and clear the device error word of `workspace` (DA_DEVERR_* bits).
+ * Synchronises `stream` first. Errors: DA_ERR_INVALID_ARG, DA_ERR_CUDA.
+ */
+da_status decode_attn_splitkv_get_error(void* workspace, uint32_t* device_error_bits,
+                                        void* stream);
+
+/*
+ * Diagnostic: launch one CTA that waits on a pipeline barrier nothing will
+ * complete, through the same bounded wait the split step uses, with a limit
+ * of timeout_us microseconds. It must give up, set DA_DEVERR_TIMEOUT in the
+ * workspace's error word and return; the device stays usable. Used by the
+ * test-suite to exercise the time-out path without hanging a GPU.
+ */
+da_status decode_attn_splitkv_selftest_timeout(void* workspace, size_t workspace_bytes,
+                                               unsigned timeout_us, void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* decode_attn_splitkv_status_string(da_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DECODE_ATTN_SPLITKV_H */

@@ -1,0 +1,819 @@
+// Split-KV decode attention (flash-decoding) for GB300 / sm_103a.
+//
+// Split step (one CTA per (sequence b, KV head, head chunk, split s)):
+//   * The GQA group of the KV head (up to 8 query heads per CTA) is packed
+//     into the N = 8 columns of an m16n8k16 tensor-core product, so every K/V
+//     byte is read from HBM once per group (TileLang decode_attention_splitkv.py,
+//     split segment, cur_kv_head; CS349E lecture 11 04_flash_decoding.py,
+//     demo1_exact second observation).
+//   * Keys are the M rows: S^T[key, head] = K_tile . Q^T, then
+//     O^T[dim, head] += V_tile^T . P^T. The score fragment becomes the P^T
+//     operand with one movmatrix transpose per 8x8 block, so P never touches
+//     shared memory.
+//   * K and V tiles arrive by TMA (cp.async.bulk.tensor, 128-byte swizzle)
+//     into a ring of shared-memory stages guarded by full/empty mbarriers; one
+//     producer warp issues the copies, four consumer warps each own 16 keys of
+//     every 64-key stage.
+//   * Online softmax in the exp2 domain (scale * log2 e folded into the
+//     scores) with running max m, running sum l and accumulator, per warp, in
+//     fp32 registers (TileLang page, split segment online softmax; MiniInfer
+//     flash_decode_splitk.py, _splitk_stage1_kernel). The four warps' states
+//     are merged in shared memory at the end; the split writes the normalised
+//     o_s and lse_s = ln l + m (natural log) to the workspace.
+//   * Split bounds are proportional: [L*s/S, L*(s+1)/S) in 64-bit integers
+//     (TileLang page, split segment). Keys of a stage past the split end are
+//     masked to -inf before the max; TMA reads past the K/V extent are
+//     zero-filled by the hardware, so no load leaves the tensor.
+// Combine step (one CTA per (b, query head)): lse = ln sum exp(lse_s),
+// out = sum exp(lse_s - lse) * o_s, skipping empty splits (TileLang page,
+// combine segment, with the weight indexed by head row; MiniInfer
+// _splitk_reduce_kernel).
+//
+// Every mbarrier wait is bounded in time; on expiry the kernel sets
+// DA_DEVERR_TIMEOUT in the workspace error word and winds down instead of
+// hanging.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "decode_attn_splitkv.h"
+
+namespace {
+
+constexpr int kBoxKeys = 16;        // keys per TMA box = rows of one mma m-tile
+constexpr int kStageKeys = 64;      // keys per pipeline stage
+constexpr int kConsumerWarps = 4;   // each owns 16 keys of a stage
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kHeadsPerCta = 8;     // mma N: packed query heads per CTA
+constexpr int kStages = 3;          // pipeline depth (two CTAs fit per SM at D = 128)
+constexpr size_t kHeaderBytes = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
+
+template <int D>
+struct Shape {
+    static constexpr int kHalves = D / 64;                         // 128-byte column slices
+    static constexpr int kSliceBytes = kStageKeys * 128;           // one slice of a stage tile
+    static constexpr int kTileBytes = kHalves * kSliceBytes;       // K (or V) bytes per stage
+    static constexpr int kStageBytes = 2 * kTileBytes;             // K + V
+    static constexpr int kBoxBytes = kBoxKeys * 128;               // one TMA box
+    static constexpr int kMergeBytes = kConsumerWarps * (D * kHeadsPerCta + 2 * kHeadsPerCta) * 4;
+    static constexpr int kRingBytes = kStages * kStageBytes;
+    static constexpr int kSmemBytes =
+        1024 /* alignment slack */ + (kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes) +
+        2 * kStages * 8 /* barriers */;
+};
+
+struct SplitParams {
+    const uint16_t* q;       // [B, Hq, D]
+    const int32_t* cu;       // [B + 1]
+    float* lse;              // [B, Hq, S]
+    float* opart;            // [B, Hq, S, D]
+    uint32_t* err;           // device error word
+    int B, Hq, Hkv, G, S, kv_rows, layout, chunks, no_kv;
+    float scale_log2;        // scale * log2(e)
+    unsigned long long wait_limit_ns;
+};
+
+// ------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase of `bar` with the given parity to complete, for at most
+// limit_ns nanoseconds. Returns false on expiry.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          unsigned long long limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (true) {
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > limit_ns) return false;
+    }
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+template <int DT>
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+    if constexpr (DT == DA_F16) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
+            " {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    } else {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
+            " {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+}
+
+// Pack two fp32 values into one register of two 16-bit values (lo = a), RN.
+template <int DT>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+    uint32_t r;
+    if constexpr (DT == DA_F16) {
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+    } else {
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+    }
+    return r;
+}
+
+template <int DT>
+__device__ __forceinline__ uint16_t to_bits(float a) {
+    uint16_t r;
+    if constexpr (DT == DA_F16) {
+        asm("cvt.rn.f16.f32 %0, %1;" : "=h"(r) : "f"(a));
+    } else {
+        asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(a));
+    }
+    return r;
+}
+
+// 2^x on the SFU (ex2.approx; 2^-inf = +0).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void flag_error(uint32_t* err, uint32_t bits) { atomicOr(err, bits); }
+
+// Sequence b's key range, validated against the K/V extent. Returns false (and
+// flags DA_DEVERR_SEQLENS) when it cannot be read safely.
+__device__ __forceinline__ bool seq_range(const SplitParams& p, int b, int64_t& base, int64_t& L) {
+    const int64_t c0 = p.cu[b], c1 = p.cu[b + 1];
+    L = c1 - c0;
+    base = p.layout == DA_LAYOUT_VARLEN ? c0 : 0;
+    bool ok = L >= 0;
+    if (p.layout == DA_LAYOUT_VARLEN) ok = ok && c0 >= 0 && c1 <= p.kv_rows;
+    else ok = ok && L <= p.kv_rows;
+    if (p.no_kv) ok = ok && L == 0;
+    if (!ok) L = 0;
+    return ok;
+}
+
+// ------------------------------------------------------------ split step
+template <int D, int DT>
+__global__ void __launch_bounds__(kThreads, 2)
+split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+             const SplitParams p) {
+    using Sh = Shape<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    const int ring_or_merge = Sh::kRingBytes > Sh::kMergeBytes ? Sh::kRingBytes : Sh::kMergeBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ring_or_merge);
+    const uint32_t ring = smem_addr(smem);
+    const uint32_t full0 = smem_addr(bars);
+    const uint32_t empty0 = full0 + kStages * 8;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int s = blockIdx.x;
+    const int chunk = blockIdx.y % p.chunks;
+    const int kvh = blockIdx.y / p.chunks;
+    const int b = blockIdx.z;
+    const int h0 = kvh * p.G + chunk * kHeadsPerCta;
+    const int nh = min(kHeadsPerCta, p.G - chunk * kHeadsPerCta);
+
+    int64_t base, L;
+    const bool seq_ok = seq_range(p, b, base, L);
+    if (!seq_ok && threadIdx.x == 0 && s == 0 && blockIdx.y == 0) flag_error(p.err, DA_DEVERR_SEQLENS);
+    const int64_t lo = L * s / p.S;
+    const int64_t hi = L * (s + 1) / p.S;
+    const int nkeys = static_cast<int>(hi - lo);
+    const int ntiles = (nkeys + kStageKeys - 1) / kStageKeys;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(full0 + 8 * i, 1);
+            mbar_init(empty0 + 8 * i, kConsumerWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kConsumerWarps && lane == 0 && ntiles > 0) {
+        prefetch_tensormap(&tmK);
+        prefetch_tensormap(&tmV);
+    }
+    __syncthreads();
+
+    if (warp == kConsumerWarps) {
+        // ---------------- producer: one lane issues every TMA copy
+        if (lane == 0) {
+            for (int t = 0; t < ntiles; ++t) {
+                const int st = t % kStages;
+                const uint32_t ph = (t / kStages) & 1;
+                if (!mbar_wait(empty0 + 8 * st, ph ^ 1, p.wait_limit_ns)) {
+                    flag_error(p.err, DA_DEVERR_TIMEOUT);
+                    break;
+                }
+                const int keys_t = min(kStageKeys, nkeys - t * kStageKeys);
+                const int nbox = (keys_t + kBoxKeys - 1) / kBoxKeys;
+                const uint32_t fb = full0 + 8 * st;
+                mbar_arrive_expect_tx(fb, nbox * Sh::kHalves * 2 * Sh::kBoxBytes);
+                const uint32_t kdst = ring + st * Sh::kStageBytes;
+                const uint32_t vdst = kdst + Sh::kTileBytes;
+                for (int bx = 0; bx < nbox; ++bx) {
+                    const int key = static_cast<int>(base + lo) + t * kStageKeys + bx * kBoxKeys;
+                    for (int hf = 0; hf < Sh::kHalves; ++hf) {
+                        const uint32_t off = hf * Sh::kSliceBytes + bx * Sh::kBoxBytes;
+                        if (p.layout == DA_LAYOUT_VARLEN) {
+                            tma_load_3d(kdst + off, &tmK, hf * 64, kvh, key, fb);
+                            tma_load_3d(vdst + off, &tmV, hf * 64, kvh, key, fb);
+                        } else {
+                            const int slab = b * p.Hkv + kvh;
+                            tma_load_3d(kdst + off, &tmK, hf * 64, key, slab, fb);
+                            tma_load_3d(vdst + off, &tmV, hf * 64, key, slab, fb);
+                        }
+                    }
+                }
+            }
+        }
+        return;
+    }
+
+    // ---------------- consumers
+    const int g = lane >> 2, t4 = lane & 3;
+    // Q^T fragments (B operand, k16 x n8): head g, dims ks*16 + 2*t4 (+1) and +8 (+9).
+    uint32_t qf[D / 16][2];
+    {
+        const bool hv = g < nh;
+        const uint32_t* qrow =
+            reinterpret_cast<const uint32_t*>(p.q + (static_cast<int64_t>(b) * p.Hq + h0 + (hv ? g : 0)) * D);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            qf[ks][0] = hv ? qrow[ks * 8 + t4] : 0u;
+            qf[ks][1] = hv ? qrow[ks * 8 + 4 + t4] : 0u;
+        }
+    }
+
+    float acc[D / 16][4];
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    float m_run[2] = {-INFINITY, -INFINITY};   // heads 2*t4, 2*t4+1 (log2 domain)
+    float l_run[2] = {0.f, 0.f};               // this thread's share of the running sum
+    bool ok = true;
+    uint32_t bad_bar = 0, bad_ph = 0;
+
+    // ldmatrix lane geometry
+    const int mi = lane >> 3, r8 = lane & 7;
+    const int krow = warp * kBoxKeys + (mi & 1) * 8 + r8;      // K: matrices (rows lo/hi) x (k lo/hi)
+    const int kchunk_add = mi >> 1;
+    const int vrow = warp * kBoxKeys + (mi >> 1) * 8 + r8;     // V^T: matrices (dims lo/hi) x (keys lo/hi)
+    const int vchunk_add = mi & 1;
+
+    for (int t = 0; t < ntiles; ++t) {
+        const int st = t % kStages;
+        const uint32_t ph = (t / kStages) & 1;
+        const uint32_t fb = full0 + 8 * st;
+        if (ok && !mbar_wait(fb, ph, p.wait_limit_ns)) {
+            ok = false;
+            bad_bar = fb;
+            bad_ph = ph;
+            if (lane == 0) flag_error(p.err, DA_DEVERR_TIMEOUT);
+        }
+        const int keys_t = min(kStageKeys, nkeys - t * kStageKeys);
+        bool zeroed = false;
+        if (ok && warp * kBoxKeys < keys_t) {
+            const uint32_t kbase = ring + st * Sh::kStageBytes;
+            const uint32_t vbase = kbase + Sh::kTileBytes;
+            const int valid_rows = keys_t - warp * kBoxKeys;
+            if (valid_rows < kBoxKeys) {
+                // The box's rows past the split end hold other keys (or, in a
+                // padded cache, anything): their P is 0, but 0 * NaN is not, so
+                // clear those V rows before the PV product.
+                const int per_row = Sh::kHalves * 8;   // 16-byte chunks per row
+                for (int c = lane; c < (kBoxKeys - valid_rows) * per_row; c += 32) {
+                    const int r = valid_rows + c / per_row;
+                    const int hf = (c % per_row) >> 3, ch = c & 7;
+                    const uint32_t addr = vbase + hf * Sh::kSliceBytes + (warp * kBoxKeys + r) * 128 + ch * 16;
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+                }
+                zeroed = true;
+                __syncwarp();
+            }
+            // S^T[16 keys, 8 heads] = K_tile . Q^T
+            float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                const int chunk16 = ks * 2 + kchunk_add;          // 16-byte chunk along D
+                const uint32_t addr = kbase + (chunk16 >> 3) * Sh::kSliceBytes + krow * 128 +
+                                      (((chunk16 & 7) ^ (krow & 7)) << 4);
+                uint32_t a[4];
+                ldsm_x4(addr, a);
+                mma_16816<DT>(sc, a, qf[ks][0], qf[ks][1]);
+            }
+            // scores -> exp2 domain, mask keys past the split end
+            const int key_lo = t * kStageKeys + warp * kBoxKeys + g;   // relative to split start
+            const bool va = key_lo < nkeys, vb = key_lo + 8 < nkeys;
+            float x0 = va ? sc[0] * p.scale_log2 : -INFINITY;
+            float x1 = va ? sc[1] * p.scale_log2 : -INFINITY;
+            float x2 = vb ? sc[2] * p.scale_log2 : -INFINITY;
+            float x3 = vb ? sc[3] * p.scale_log2 : -INFINITY;
+            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
+            const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
+            const float al0 = fast_exp2(m_run[0] - mn0), al1 = fast_exp2(m_run[1] - mn1);
+            const float p0 = fast_exp2(x0 - mn0), p1 = fast_exp2(x1 - mn1);
+            const float p2 = fast_exp2(x2 - mn0), p3 = fast_exp2(x3 - mn1);
+            l_run[0] = l_run[0] * al0 + (p0 + p2);
+            l_run[1] = l_run[1] * al1 + (p1 + p3);
+            m_run[0] = mn0;
+            m_run[1] = mn1;
+#pragma unroll
+            for (int i = 0; i < D / 16; ++i) {
+                acc[i][0] *= al0;
+                acc[i][1] *= al1;
+                acc[i][2] *= al0;
+                acc[i][3] *= al1;
+            }
+            // P^T operand (k16 keys x n8 heads) via 8x8 transposes of the score fragment
+            const uint32_t pb0 = movmatrix_trans(pack2<DT>(p0, p1));
+            const uint32_t pb1 = movmatrix_trans(pack2<DT>(p2, p3));
+            // O^T[D, 8] += V_tile^T . P^T
+#pragma unroll
+            for (int i = 0; i < D / 16; ++i) {
+                const int chunk16 = i * 2 + vchunk_add;
+                const uint32_t addr = vbase + (chunk16 >> 3) * Sh::kSliceBytes + vrow * 128 +
+                                      (((chunk16 & 7) ^ (vrow & 7)) << 4);
+                uint32_t a[4];
+                ldsm_x4_trans(addr, a);
+                mma_16816<DT>(acc[i], a, pb0, pb1);
+            }
+        }
+        if (zeroed) {
+            // order the generic-proxy stores above before the next TMA write to this stage
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * st);
+    }
+    if (!ok) {
+        // give a copy that may still be landing one more bounded wait before the CTA exits
+        mbar_wait(bad_bar, bad_ph, p.wait_limit_ns);
+    }
+
+    // per-thread partial sums -> per-warp sums (over the 8 key rows g)
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], off);
+        l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], off);
+    }
+
+    // ---------------- merge the four warps' states (reusing the ring)
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+    float* red_acc = reinterpret_cast<float*>(smem);                        // [warp][D][8]
+    float* red_m = red_acc + kConsumerWarps * D * kHeadsPerCta;             // [warp][8]
+    float* red_l = red_m + kConsumerWarps * kHeadsPerCta;                   // [warp][8]
+    if (g == 0) {
+        red_m[warp * kHeadsPerCta + 2 * t4] = m_run[0];
+        red_m[warp * kHeadsPerCta + 2 * t4 + 1] = m_run[1];
+        red_l[warp * kHeadsPerCta + 2 * t4] = l_run[0];
+        red_l[warp * kHeadsPerCta + 2 * t4 + 1] = l_run[1];
+    }
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i) {
+        float* r0 = red_acc + (warp * D + i * 16 + g) * kHeadsPerCta + 2 * t4;
+        float* r1 = r0 + 8 * kHeadsPerCta;
+        *reinterpret_cast<float2*>(r0) = make_float2(acc[i][0], acc[i][1]);
+        *reinterpret_cast<float2*>(r1) = make_float2(acc[i][2], acc[i][3]);
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+
+    const int tid = threadIdx.x;
+    for (int idx = tid; idx < nh * D; idx += kConsumerWarps * 32) {
+        const int hh = idx / D, d = idx % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, red_m[w * kHeadsPerCta + hh]);
+        float o = 0.f, lsum = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const float wt = fast_exp2(red_m[w * kHeadsPerCta + hh] - M);
+                lsum += wt * red_l[w * kHeadsPerCta + hh];
+                o += wt * red_acc[(w * D + d) * kHeadsPerCta + hh];
+            }
+            o = o / lsum;
+        }
+        const int64_t row = (static_cast<int64_t>(b) * p.Hq + h0 + hh) * p.S + s;
+        p.opart[row * D + d] = o;
+        if (d == 0) p.lse[row] = M == -INFINITY ? -INFINITY : (M + log2f(lsum)) * kLn2;
+    }
+}
+
+// ------------------------------------------------------------ combine step
+template <int D, int DT>
+__global__ void __launch_bounds__(D) combine_kernel(const float* __restrict__ lse,
+                                                    const float* __restrict__ opart,
+                                                    uint16_t* __restrict__ out, int S) {
+    const int64_t row = blockIdx.x;
+    const int d = threadIdx.x;
+    const float* l = lse + row * S;
+    float M = -INFINITY;
+    for (int s = 0; s < S; ++s) M = fmaxf(M, l[s]);
+    float o = 0.f;
+    if (M != -INFINITY) {
+        float z = 0.f;
+        for (int s = 0; s < S; ++s) z += fast_exp2((l[s] - M) * kLog2e);
+        const float inv = 1.f / z;
+        const float* po = opart + row * S * D + d;
+        for (int s = 0; s < S; ++s) {
+            const float w = fast_exp2((l[s] - M) * kLog2e) * inv;
+            o += w * po[static_cast<int64_t>(s) * D];
+        }
+    }
+    out[row * D + d] = to_bits<DT>(o);
+}
+
+// ------------------------------------------------------------ diagnostics
+__global__ void selftest_timeout_kernel(uint32_t* err, unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t a = smem_addr(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(a, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    // Nothing arrives on `bar`: phase 0 never completes.
+    if (threadIdx.x == 0 && !mbar_wait(a, 0, limit_ns)) flag_error(err, DA_DEVERR_TIMEOUT);
+}
+
+// ------------------------------------------------------------ host side
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, []() {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+bool make_kv_map(CUtensorMap* map, const void* base, da_dtype dt, da_layout lay, int B, int Hkv,
+                 int D, int kv_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3], strides[2];
+    cuuint32_t box[3], estr[3] = {1, 1, 1};
+    if (lay == DA_LAYOUT_VARLEN) {
+        dims[0] = D; dims[1] = Hkv; dims[2] = kv_rows;
+        strides[0] = static_cast<cuuint64_t>(D) * 2;
+        strides[1] = static_cast<cuuint64_t>(Hkv) * D * 2;
+        box[0] = 64; box[1] = 1; box[2] = kBoxKeys;
+    } else {
+        dims[0] = D; dims[1] = kv_rows; dims[2] = static_cast<cuuint64_t>(B) * Hkv;
+        strides[0] = static_cast<cuuint64_t>(D) * 2;
+        strides[1] = static_cast<cuuint64_t>(kv_rows) * D * 2;
+        box[0] = 64; box[1] = kBoxKeys; box[2] = 1;
+    }
+    CUresult r = fn(map, dt == DA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                    3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Raise the dynamic shared-memory limit of `kernel` once per device; `done`
+// is the caller's per-kernel bit set of devices already configured.
+template <class K>
+cudaError_t ensure_smem_attr(K kernel, int bytes, std::atomic<uint64_t>& done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
+
+da_status check_common(const void* q, const void* k, const void* v, const int32_t* cu, int B, int Hq,
+                       int Hkv, int D, int kv_rows, int dt, int lay, float scale, int S,
+                       const void* ws, size_t ws_bytes) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || kv_rows < 0) return DA_ERR_INVALID_ARG;
+    if (S < 1 || S > DA_MAX_SPLITS) return DA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return DA_ERR_INVALID_ARG;
+    if (dt != DA_F16 && dt != DA_BF16) return DA_ERR_INVALID_ARG;
+    if (lay != DA_LAYOUT_VARLEN && lay != DA_LAYOUT_BHSD) return DA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return DA_ERR_UNSUPPORTED;
+    if (!q || !cu || !ws) return DA_ERR_INVALID_ARG;
+    if (kv_rows > 0 && (!k || !v)) return DA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(cu, 4) || !aligned(ws, 256)) return DA_ERR_ALIGNMENT;
+    if (kv_rows > 0 && (!aligned(k, 16) || !aligned(v, 16))) return DA_ERR_ALIGNMENT;
+    const size_t need = decode_attn_splitkv_workspace_size(B, Hq, D, S);
+    if (need == 0) return DA_ERR_INVALID_ARG;
+    if (ws_bytes < need) return DA_ERR_WORKSPACE_TOO_SMALL;
+    if (lay == DA_LAYOUT_BHSD && static_cast<int64_t>(B) * Hkv > 0xffffffffll) return DA_ERR_INVALID_ARG;
+    return DA_OK;
+}
+
+template <int D, int DT>
+da_status launch_split(const void* q, const void* k, const void* v, const int32_t* cu, int B, int Hq,
+                       int Hkv, int kv_rows, da_layout lay, float scale, int S, void* ws,
+                       cudaStream_t stream) {
+    alignas(64) CUtensorMap mk, mv;
+    std::memset(&mk, 0, sizeof(mk));
+    std::memset(&mv, 0, sizeof(mv));
+    if (kv_rows > 0) {
+        if (!make_kv_map(&mk, k, static_cast<da_dtype>(DT), lay, B, Hkv, D, kv_rows) ||
+            !make_kv_map(&mv, v, static_cast<da_dtype>(DT), lay, B, Hkv, D, kv_rows))
+            return DA_ERR_CUDA;
+    }
+    SplitParams p;
+    p.q = static_cast<const uint16_t*>(q);
+    p.cu = cu;
+    p.err = static_cast<uint32_t*>(ws);
+    p.lse = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + decode_attn_splitkv_lse_offset());
+    p.opart = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + decode_attn_splitkv_opart_offset(B, Hq, S));
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.G = Hq / Hkv;
+    p.S = S;
+    p.kv_rows = kv_rows;
+    p.layout = lay;
+    p.chunks = (p.G + kHeadsPerCta - 1) / kHeadsPerCta;
+    p.no_kv = kv_rows == 0;
+    p.scale_log2 = scale * kLog2e;
+    p.wait_limit_ns = kWaitLimitNs;
+
+    const int smem = Shape<D>::kSmemBytes;
+    auto kern = split_kernel<D, DT>;
+    static std::atomic<uint64_t> attr_done{0};
+    if (ensure_smem_attr(kern, smem, attr_done) != cudaSuccess) return DA_ERR_CUDA;
+    if (static_cast<int64_t>(Hkv) * p.chunks > 65535 || B > 65535) return DA_ERR_INVALID_ARG;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(S, Hkv * p.chunks, B);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = nullptr;
+    cfg.numAttrs = 0;
+    return cudaLaunchKernelEx(&cfg, kern, mk, mv, p) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
+}
+
+template <int D, int DT>
+da_status launch_combine(int B, int Hq, int S, void* out, const void* ws, cudaStream_t stream) {
+    const float* lse = reinterpret_cast<const float*>(static_cast<const uint8_t*>(ws) +
+                                                      decode_attn_splitkv_lse_offset());
+    const float* opart = reinterpret_cast<const float*>(static_cast<const uint8_t*>(ws) +
+                                                        decode_attn_splitkv_opart_offset(B, Hq, S));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(static_cast<int64_t>(B) * Hq));
+    cfg.blockDim = dim3(D);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    return cudaLaunchKernelEx(&cfg, combine_kernel<D, DT>, lse, opart, static_cast<uint16_t*>(out), S) ==
+                   cudaSuccess
+               ? DA_OK
+               : DA_ERR_CUDA;
+}
+
+da_status dispatch_split(const void* q, const void* k, const void* v, const int32_t* cu, int B, int Hq,
+                         int Hkv, int D, int kv_rows, da_dtype dt, da_layout lay, float scale, int S,
+                         void* ws, cudaStream_t st) {
+    if (D == 128)
+        return dt == DA_F16 ? launch_split<128, DA_F16>(q, k, v, cu, B, Hq, Hkv, kv_rows, lay, scale, S, ws, st)
+                            : launch_split<128, DA_BF16>(q, k, v, cu, B, Hq, Hkv, kv_rows, lay, scale, S, ws, st);
+    return dt == DA_F16 ? launch_split<64, DA_F16>(q, k, v, cu, B, Hq, Hkv, kv_rows, lay, scale, S, ws, st)
+                        : launch_split<64, DA_BF16>(q, k, v, cu, B, Hq, Hkv, kv_rows, lay, scale, S, ws, st);
+}
+
+da_status dispatch_combine(int B, int Hq, int D, int S, da_dtype dt, void* out, const void* ws,
+                           cudaStream_t st) {
+    if (D == 128)
+        return dt == DA_F16 ? launch_combine<128, DA_F16>(B, Hq, S, out, ws, st)
+                            : launch_combine<128, DA_BF16>(B, Hq, S, out, ws, st);
+    return dt == DA_F16 ? launch_combine<64, DA_F16>(B, Hq, S, out, ws, st)
+                        : launch_combine<64, DA_BF16>(B, Hq, S, out, ws, st);
+}
+
+}  // namespace
+
+// ================================================================ C ABI
+extern "C" {
+
+size_t decode_attn_splitkv_lse_offset(void) { return kHeaderBytes; }
+
+size_t decode_attn_splitkv_opart_offset(int B, int Hq, int num_splits) {
+    return kHeaderBytes + round_up(static_cast<size_t>(B) * Hq * num_splits * 4, 256);
+}
+
+size_t decode_attn_splitkv_workspace_size(int B, int Hq, int D, int num_splits) {
+    if (B < 1 || Hq < 1 || D < 1 || num_splits < 1 || num_splits > DA_MAX_SPLITS) return 0;
+    return decode_attn_splitkv_opart_offset(B, Hq, num_splits) +
+           static_cast<size_t>(B) * Hq * num_splits * D * 4;
+}
+
+da_status decode_attn_splitkv_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+    if (!workspace || workspace_bytes < kHeaderBytes) return DA_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256)) return DA_ERR_ALIGNMENT;
+    return cudaMemsetAsync(workspace, 0, kHeaderBytes, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? DA_OK
+               : DA_ERR_CUDA;
+}
+
+void decode_attn_splitkv_split_range(int64_t L, int num_splits, int s, int64_t* start, int64_t* end) {
+    if (!start || !end) return;
+    if (num_splits < 1 || L < 0) {
+        *start = *end = 0;
+        return;
+    }
+    *start = L * s / num_splits;
+    *end = L * (s + 1) / num_splits;
+}
+
+int decode_attn_splitkv_num_splits(int B, int Hq, int Hkv, int D, int min_kv, int max_kv, int sm_count) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || (D != 64 && D != 128)) return 1;
+    if (min_kv <= 0 || max_kv < min_kv) return 1;
+    if (sm_count <= 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            sm_count <= 0)
+            sm_count = 148;
+    }
+    const int64_t chunks = (Hq / Hkv + kHeadsPerCta - 1) / kHeadsPerCta;
+    const int64_t units = static_cast<int64_t>(B) * Hkv * chunks;
+    const int64_t slots = static_cast<int64_t>(sm_count) * 2;   // two resident split CTAs per SM
+    // Aim for about four CTAs per resident slot so that unequal splits balance out.
+    int64_t S = (4 * slots + units - 1) / units;
+    // Keep every split at least kMinKeys long (one or more full stages) ...
+    constexpr int64_t kMinKeys = 128;
+    S = std::min<int64_t>(S, std::max<int64_t>(1, min_kv / kMinKeys));
+    // ... never empty, and within the ABI limit.
+    S = std::min<int64_t>(S, min_kv);
+    S = std::max<int64_t>(1, std::min<int64_t>(S, DA_MAX_SPLITS));
+    return static_cast<int>(S);
+}
+
+da_status decode_attn_splitkv_partial(const void* q, const void* k, const void* v,
+                                      const int32_t* cu_seqlens_k, int B, int Hq, int Hkv, int D,
+                                      int kv_rows, da_dtype dtype, da_layout layout, float scale,
+                                      int num_splits, void* workspace, size_t workspace_bytes,
+                                      void* stream) {
+    da_status st = check_common(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale,
+                                num_splits, workspace, workspace_bytes);
+    if (st != DA_OK) return st;
+    return dispatch_split(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale,
+                          num_splits, workspace, static_cast<cudaStream_t>(stream));
+}
+
+da_status decode_attn_splitkv_combine(int B, int Hq, int D, int num_splits, da_dtype dtype, void* out,
+                                      const void* workspace, size_t workspace_bytes, void* stream) {
+    if (B < 1 || Hq < 1 || num_splits < 1 || num_splits > DA_MAX_SPLITS) return DA_ERR_INVALID_ARG;
+    if (dtype != DA_F16 && dtype != DA_BF16) return DA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return DA_ERR_UNSUPPORTED;
+    if (!out || !workspace) return DA_ERR_INVALID_ARG;
+    if (!aligned(out, 16) || !aligned(workspace, 256)) return DA_ERR_ALIGNMENT;
+    if (workspace_bytes < decode_attn_splitkv_workspace_size(B, Hq, D, num_splits))
+        return DA_ERR_WORKSPACE_TOO_SMALL;
+    if (static_cast<int64_t>(B) * Hq > 0x7fffffffll) return DA_ERR_INVALID_ARG;
+    return dispatch_combine(B, Hq, D, num_splits, dtype, out, workspace, static_cast<cudaStream_t>(stream));
+}
+
+da_status decode_attn_splitkv(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_k,
+                              int B, int Hq, int Hkv, int D, int kv_rows, da_dtype dtype,
+                              da_layout layout, float scale, int num_splits, void* out,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+    da_status st = check_common(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale,
+                                num_splits, workspace, workspace_bytes);
+    if (st != DA_OK) return st;
+    if (!out) return DA_ERR_INVALID_ARG;
+    if (!aligned(out, 16)) return DA_ERR_ALIGNMENT;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    st = dispatch_split(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale, num_splits,
+                        workspace, s);
+    if (st != DA_OK) return st;
+    return dispatch_combine(B, Hq, D, num_splits, dtype, out, workspace, s);
+}
+
+da_status decode_attn_splitkv_get_error(void* workspace, uint32_t* device_error_bits, void* stream) {
+    if (!workspace || !device_error_bits) return DA_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256)) return DA_ERR_ALIGNMENT;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t bits = 0;
+    if (cudaMemcpyAsync(&bits, workspace, sizeof(bits), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return DA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return DA_ERR_CUDA;
+    *device_error_bits = bits;
+    if (cudaMemsetAsync(workspace, 0, sizeof(uint32_t), s) != cudaSuccess) return DA_ERR_CUDA;
+    return DA_OK;
+}
+
+da_status decode_attn_splitkv_selftest_timeout(void* workspace, size_t workspace_bytes,
+                                               unsigned timeout_us, void* stream) {
+    if (!workspace || workspace_bytes < kHeaderBytes || timeout_us == 0 || timeout_us > 10000000u)
+        return DA_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256)) return DA_ERR_ALIGNMENT;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(32);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    return cudaLaunchKernelEx(&cfg, selftest_timeout_kernel, static_cast<uint32_t*>(workspace),
+                              static_cast<unsigned long long>(timeout_us) * 1000ull) == cudaSuccess
+               ? DA_OK
+               : DA_ERR_CUDA;
+}
+
+const char* decode_attn_splitkv_status_string(da_status status) {
+    switch (status) {
+        case DA_OK: return "DA_OK";
+        case DA_ERR_INVALID_ARG: return "DA_ERR_INVALID_ARG: an argument is out of range or NULL";
+        case DA_ERR_UNSUPPORTED: return "DA_ERR_UNSUPPORTED: head_dim must be 64 or 128";
+        case DA_ERR_ALIGNMENT: return "DA_ERR_ALIGNMENT: a pointer is not aligned as documented";
+        case DA_ERR_WORKSPACE_TOO_SMALL: return "DA_ERR_WORKSPACE_TOO_SMALL";
+        case DA_ERR_CUDA: return "DA_ERR_CUDA: a CUDA runtime or driver call failed";
+    }
+    return "unknown da_status";
+}
+
+}  // extern "C"

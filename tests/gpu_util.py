@@ -1,0 +1,64 @@
+"""Helpers for the GPU parity tests: move a synthetic problem to the device, run the
+CUDA path through the C ABI, and derive tolerances from the arithmetic."""
+import numpy as np
+import torch
+
+import split_kv_decode_decoding_gb300 as da
+from synth.workloads import LAYOUT_VARLEN
+
+# Parity bounds fixed for this method: final output max |delta| (fp16/bf16 outputs)
+# and per-split log-sum-exp max |delta| (fp32).
+OUT_TOL = 4e-3
+LSE_TOL = 1e-4
+
+
+def opart_tol(p) -> float:
+    """Bound for the fp32 per-split outputs.
+
+    The kernel rounds the softmax weights P to the input dtype before the PV
+    tensor-core product (unit roundoff u = 2^-11 for fp16, 2^-8 for bf16, so a
+    relative error of at most u/2... u per weight), which moves o_s by at most
+    u * max|v|; fp32 accumulation and the exp2 approximation add far less.
+    """
+    u = 2.0 ** -11 if p.dtype == "f16" else 2.0 ** -8
+    vmax = float(np.abs(_decode(p.v, p.dtype)[np.isfinite(_decode(p.v, p.dtype))]).max()) if p.v.size else 1.0
+    return u * vmax + 1e-5
+
+
+def _decode(bits, dtype):
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.view(torch.float16 if dtype == "f16" else torch.bfloat16).to(torch.float64).numpy()
+
+
+def torch_dtype(p):
+    return torch.float16 if p.dtype == "f16" else torch.bfloat16
+
+
+def to_device(p, device="cuda"):
+    dt = torch_dtype(p)
+
+    def dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(dt).to(device)
+
+    return dev(p.q), dev(p.k), dev(p.v), torch.from_numpy(p.cu.astype(np.int32)).to(device)
+
+
+def run(p, S, device="cuda", stream=None, tensors=None):
+    """Run the full call; returns (out, lse_part, o_part, error_bits) as float64 numpy."""
+    q, k, v, cu = tensors if tensors is not None else to_device(p, device)
+    ws = da.alloc_workspace(p.B, p.Hq, p.D, S, device=device, stream=stream)
+    out = torch.empty(p.B, p.Hq, p.D, dtype=torch_dtype(p), device=device)
+    da.decode_attn_splitkv(q, k, v, cu, out, ws, num_splits=S, scale=p.scale, layout=p.layout,
+                           stream=stream)
+    err = da.decode_attn_splitkv_get_error(ws, stream=stream)
+    lse, opart = da.workspace_views(ws, p.B, p.Hq, p.D, S)
+    return (out.to(torch.float64).cpu().numpy(), lse.to(torch.float64).cpu().numpy(),
+            opart.to(torch.float64).cpu().numpy(), err)
+
+
+def max_abs(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    both_inf = np.isneginf(a) & np.isneginf(b)
+    d = np.where(both_inf, 0.0, np.abs(a - b))
+    return float(np.nan_to_num(d, nan=np.inf).max()) if d.size else 0.0

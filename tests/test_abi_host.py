@@ -1,0 +1,159 @@
+"""The C-ABI library on the host: symbols, layout arithmetic, picker, argument checks.
+
+Nothing here reaches a CUDA call: every case is rejected (or answered) by the
+host-side code before any device work would be enqueued.
+"""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+import oracle
+import split_kv_decode_decoding_gb300 as da
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "decode_attn_splitkv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    da.build()
+    return da.load()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(decode_attn_splitkv\w*)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = header_functions()
+    assert len(names) == 12
+    assert sorted(names) == sorted(da.EXPORTED)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        s = da.status_string(code)
+        assert s and s != "unknown da_status"
+    assert da.status_string(99) == "unknown da_status"
+
+
+def test_workspace_layout(lib):
+    B, Hq, D, S = 3, 28, 128, 7
+    lo = lib.decode_attn_splitkv_lse_offset()
+    oo = lib.decode_attn_splitkv_opart_offset(B, Hq, S)
+    assert lo == 256 and oo % 256 == 0 and oo >= lo + 4 * B * Hq * S
+    assert da.workspace_size(B, Hq, D, S) == oo + 4 * B * Hq * S * D
+    assert da.workspace_size(0, Hq, D, S) == 0
+    assert da.workspace_size(B, Hq, D, 0) == 0
+    assert da.workspace_size(B, Hq, D, da.DA_MAX_SPLITS + 1) == 0
+
+
+def test_split_range_matches_oracle_bit_exact(lib):
+    orc = oracle.default()
+    for L in list(range(0, 300, 7)) + [4096, 8191, 131072, 2_000_000_000]:
+        for S in (1, 2, 3, 4, 7, 16, 37, 152, 1000, 1024):
+            for s in {0, 1, S // 2, S - 1}:
+                if s < S:
+                    assert da.split_range(L, S, s) == orc.split_range(L, S, s), (L, S, s)
+
+
+@pytest.mark.parametrize("shape", [
+    (2, 4, 1, 64, 37, 200), (8, 32, 32, 128, 4096, 4096), (64, 28, 4, 128, 512, 8192),
+    (256, 16, 2, 128, 256, 256), (1, 16, 2, 128, 65536, 65536), (1, 16, 2, 128, 131072, 131072),
+    (1, 32, 8, 128, 1024, 1024), (16, 32, 8, 128, 131072, 131072), (4, 64, 1, 128, 3, 9000),
+])
+def test_picker_properties(lib, shape):
+    B, Hq, Hkv, D, mn, mx = shape
+    for sm in (148, 152):
+        S = da.num_splits(B, Hq, Hkv, D, mn, mx, sm)
+        assert 1 <= S <= min(mn, da.DA_MAX_SPLITS)
+        assert S == da.num_splits(B, Hq, Hkv, D, mn, mx, sm)
+        units = B * Hkv * math.ceil(Hq // Hkv / 8)
+        # never more splits than needed for about four CTAs per resident slot
+        assert units * (S - 1) < 4 * 2 * sm
+
+
+def test_picker_degenerate(lib):
+    assert da.num_splits(2, 4, 1, 64, 0, 10, 152) == 1      # an empty sequence present
+    assert da.num_splits(2, 4, 3, 64, 10, 10, 152) == 1     # Hq % Hkv != 0
+    assert da.num_splits(2, 4, 1, 96, 10, 10, 152) == 1     # unsupported D
+    assert da.num_splits(2, 4, 1, 64, 20, 10, 152) == 1     # min > max
+    assert da.num_splits(1, 8, 1, 128, 1, 1, 152) == 1      # one key: one split
+
+
+# --- argument checks (fake, aligned device addresses: never dereferenced) -------------
+FAKE = 0x7f0000000000
+
+
+def call_full(lib, **kw):
+    a = dict(q=FAKE, k=FAKE + 0x100000, v=FAKE + 0x200000, cu=FAKE + 0x300000, B=2, Hq=4, Hkv=1,
+             D=64, kv_rows=237, dt=0, lay=0, scale=0.125, S=4, out=FAKE + 0x400000,
+             ws=FAKE + 0x500000, ws_bytes=1 << 20, stream=None)
+    a.update(kw)
+    v = ctypes.c_void_p
+    return lib.decode_attn_splitkv(v(a["q"]), v(a["k"]), v(a["v"]), v(a["cu"]), a["B"], a["Hq"],
+                                   a["Hkv"], a["D"], a["kv_rows"], a["dt"], a["lay"], a["scale"],
+                                   a["S"], v(a["out"]), v(a["ws"]), a["ws_bytes"], v(a["stream"]))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=0), da.DA_ERR_INVALID_ARG),
+    (dict(Hq=0), da.DA_ERR_INVALID_ARG),
+    (dict(Hq=6, Hkv=4), da.DA_ERR_INVALID_ARG),
+    (dict(kv_rows=-1), da.DA_ERR_INVALID_ARG),
+    (dict(S=0), da.DA_ERR_INVALID_ARG),
+    (dict(S=da.DA_MAX_SPLITS + 1), da.DA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), da.DA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), da.DA_ERR_INVALID_ARG),
+    (dict(dt=2), da.DA_ERR_INVALID_ARG),
+    (dict(lay=2), da.DA_ERR_INVALID_ARG),
+    (dict(D=96), da.DA_ERR_UNSUPPORTED),
+    (dict(D=256), da.DA_ERR_UNSUPPORTED),
+    (dict(q=0), da.DA_ERR_INVALID_ARG),
+    (dict(cu=0), da.DA_ERR_INVALID_ARG),
+    (dict(ws=0), da.DA_ERR_INVALID_ARG),
+    (dict(k=0), da.DA_ERR_INVALID_ARG),
+    (dict(out=0), da.DA_ERR_INVALID_ARG),
+    (dict(q=FAKE + 8), da.DA_ERR_ALIGNMENT),
+    (dict(k=FAKE + 0x100004), da.DA_ERR_ALIGNMENT),
+    (dict(cu=FAKE + 0x300002), da.DA_ERR_ALIGNMENT),
+    (dict(ws=FAKE + 0x500080), da.DA_ERR_ALIGNMENT),
+    (dict(out=FAKE + 0x400008), da.DA_ERR_ALIGNMENT),
+    (dict(ws_bytes=1000), da.DA_ERR_WORKSPACE_TOO_SMALL),
+])
+def test_host_checks(lib, kw, code):
+    assert call_full(lib, **kw) == code
+
+
+def test_other_entry_points_reject_bad_args(lib):
+    v = ctypes.c_void_p
+    bits = ctypes.c_uint32()
+    assert lib.decode_attn_splitkv_get_error(None, ctypes.byref(bits), None) == da.DA_ERR_INVALID_ARG
+    assert lib.decode_attn_splitkv_get_error(v(FAKE + 64), ctypes.byref(bits), None) == da.DA_ERR_ALIGNMENT
+    assert lib.decode_attn_splitkv_workspace_init(None, 1 << 20, None) == da.DA_ERR_INVALID_ARG
+    assert lib.decode_attn_splitkv_workspace_init(v(FAKE), 100, None) == da.DA_ERR_INVALID_ARG
+    assert lib.decode_attn_splitkv_selftest_timeout(v(FAKE), 1 << 20, 0, None) == da.DA_ERR_INVALID_ARG
+    assert lib.decode_attn_splitkv_combine(2, 4, 64, 4, 0, None, v(FAKE), 1 << 20, None) == da.DA_ERR_INVALID_ARG
+    assert lib.decode_attn_splitkv_combine(2, 4, 96, 4, 0, v(FAKE), v(FAKE), 1 << 20, None) == da.DA_ERR_UNSUPPORTED
+    assert lib.decode_attn_splitkv_combine(2, 4, 64, 4, 0, v(FAKE), v(FAKE), 100, None) == da.DA_ERR_WORKSPACE_TOO_SMALL
+    assert lib.decode_attn_splitkv_partial(v(FAKE), v(FAKE), v(FAKE), v(FAKE), 2, 4, 1, 64, 237, 0, 0,
+                                           0.125, 4, v(FAKE), 10, None) == da.DA_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_binding_refuses_without_library(tmp_path):
+    import importlib
+    mod = importlib.import_module("split_kv_decode_decoding_gb300")
+    saved = mod._lib
+    try:
+        mod._lib = None
+        with pytest.raises(RuntimeError):
+            mod.load(str(tmp_path / "missing.so"))
+    finally:
+        mod._lib = saved

@@ -1,0 +1,189 @@
+"""CUDA path vs the float64 oracle, element by element, through the C ABI."""
+import math
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import split_kv_decode_decoding_gb300 as da
+from gpu_util import LSE_TOL, OUT_TOL, max_abs, opart_tol, run, to_device, torch_dtype
+from synth.workloads import LAYOUT_BHSD, LAYOUT_VARLEN, all_workload_names, custom, workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    da.build()
+    da.load()
+
+
+def check_full(p, S):
+    out, lse, opart, err = run(p, S)
+    assert err == 0
+    ref, _ = oracle.default().attention(p)
+    ref_op, ref_lse = oracle.default().split_partials(p, S)
+    e_out = max_abs(out, ref)
+    e_lse = max_abs(lse, ref_lse)
+    e_op = max_abs(opart, ref_op)
+    assert np.array_equal(np.isneginf(lse), np.isneginf(ref_lse)), "empty-split pattern differs"
+    assert e_out <= OUT_TOL, f"out max|d| {e_out}"
+    assert e_lse <= LSE_TOL, f"lse_part max|d| {e_lse}"
+    assert e_op <= opart_tol(p), f"o_part max|d| {e_op} > {opart_tol(p)}"
+    return e_out, e_lse, e_op
+
+
+def test_tiny_workload():
+    p = workload("tiny")
+    check_full(p, p.num_splits)
+
+
+CASES = [
+    # name, B, Hq, Hkv, D, lens, dtype, layout, S, kv_rows
+    ("short_tiles", 3, 8, 1, 128, [1, 16, 17], "f16", LAYOUT_VARLEN, 1, 0),
+    ("stage_edges", 3, 8, 1, 128, [63, 64, 65], "f16", LAYOUT_VARLEN, 2, 0),
+    ("qwen_heads", 2, 28, 4, 128, [1000, 777], "f16", LAYOUT_VARLEN, 7, 0),
+    ("mha_bhsd", 2, 32, 32, 128, [300, 300], "f16", LAYOUT_BHSD, 3, 300),
+    ("bhsd_padded", 2, 32, 32, 128, [129, 250], "f16", LAYOUT_BHSD, 4, 256),
+    ("codellama_heads", 3, 16, 2, 128, [512, 100, 1023], "f16", LAYOUT_VARLEN, 16, 0),
+    ("llama_heads_bf16", 2, 32, 8, 128, [1024, 555], "bf16", LAYOUT_VARLEN, 5, 0),
+    ("group12_d64_bf16", 2, 12, 1, 64, [200, 333], "bf16", LAYOUT_VARLEN, 3, 0),
+    ("group16", 2, 16, 1, 128, [80, 90], "f16", LAYOUT_VARLEN, 2, 0),
+    ("empty_sequences", 4, 4, 4, 64, [0, 5, 0, 70], "f16", LAYOUT_VARLEN, 3, 0),
+    ("more_splits_than_keys", 2, 8, 2, 64, [3, 10], "f16", LAYOUT_VARLEN, 6, 0),
+    ("long_single_split", 1, 7, 1, 128, [4096], "f16", LAYOUT_VARLEN, 1, 0),
+    ("d64_bhsd_bf16", 3, 8, 2, 64, [77, 1, 64], "bf16", LAYOUT_BHSD, 2, 80),
+    ("many_splits", 2, 4, 1, 128, [2000, 1500], "f16", LAYOUT_VARLEN, 100, 0),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_parity_cases(case):
+    name, B, Hq, Hkv, D, lens, dtype, layout, S, kv_rows = case
+    p = custom(name, B, Hq, Hkv, D, lens, dtype, layout, S, seed=zlib.crc32(name.encode()) % 1000, kv_rows=kv_rows)
+    if layout == LAYOUT_BHSD:
+        # positions past each sequence's length hold NaN: they must never reach the result
+        for b, L in enumerate(lens):
+            p.k[b, :, L:, :] = 0x7E00
+            p.v[b, :, L:, :] = 0x7E00
+    check_full(p, S)
+
+
+def test_varlen_rows_past_the_last_sequence_are_ignored():
+    p = custom("tailnan", 2, 8, 2, 128, [70, 45], "f16", LAYOUT_VARLEN, 3, seed=5, data=False)
+    from synth.workloads import materialize
+    materialize(p)
+    cap = p.total_kv + 40
+    k = np.full((cap, p.Hkv, p.D), 0x7E00, dtype=np.uint16)
+    v = np.full((cap, p.Hkv, p.D), 0x7E00, dtype=np.uint16)
+    k[: p.total_kv] = p.k
+    v[: p.total_kv] = p.v
+    p.k, p.v, p.kv_rows = k, v, cap
+    check_full(p, 3)
+
+
+@pytest.mark.parametrize("S", [1, 2, 3, 4, 5, 7, 9, 16, 37])
+def test_split_bounds_bit_exact_q_zero(S):
+    """q = 0: lse_s = ln(split length) exactly pins every split boundary on the device."""
+    lens = [37, 200, 1, 16, 65, 129, 1000]
+    p = custom("qz", len(lens), 4, 1, 64, lens, "f16", LAYOUT_VARLEN, S, seed=3, q_std=0.0)
+    out, lse, opart, err = run(p, S)
+    assert err == 0
+    orc = oracle.default()
+    for b, L in enumerate(lens):
+        for s in range(S):
+            lo, hi = orc.split_range(L, S, s)
+            n = hi - lo
+            for h in range(4):
+                if n == 0:
+                    assert lse[b, h, s] == -math.inf
+                else:
+                    assert abs(lse[b, h, s] - math.log(n)) <= 1e-5, (b, s, n, lse[b, h, s])
+    ref_op, _ = orc.split_partials(p, S)
+    assert max_abs(opart, ref_op) <= opart_tol(p)
+
+
+@pytest.mark.parametrize("name", [n for n in all_workload_names() if n != "tiny"])
+def test_named_workloads_sampled(name):
+    """Full-size workloads in the launch configuration the benchmark uses, sampled rows."""
+    p = workload(name)
+    S = p.num_splits or da.num_splits(p.B, p.Hq, p.Hkv, p.D, min(p.lens), max(p.lens))
+    out, lse, opart, err = run(p, S)
+    assert err == 0
+    assert np.isfinite(out).all() and np.isfinite(lse).all() and np.isfinite(opart).all()
+    rng = np.random.default_rng(0)
+    n = 24
+    rb = np.concatenate([[0, p.B - 1], rng.integers(0, p.B, n)]).astype(np.int32)
+    rh = np.concatenate([[0, p.Hq - 1], rng.integers(0, p.Hq, n)]).astype(np.int32)
+    ref, ref_lse = oracle.default().attention_rows(p, rb, rh)
+    e = max_abs(out[rb, rh], ref)
+    assert e <= OUT_TOL, f"{name}: out max|d| {e}"
+    # every split's log-sum-exp merges back to the row's total (property at any size)
+    m = lse[rb, rh].max(axis=1, keepdims=True)
+    tot = m[:, 0] + np.log(np.exp(lse[rb, rh] - m).sum(axis=1))
+    assert np.abs(tot - ref_lse).max() <= LSE_TOL
+
+
+def test_bad_seqlens_flagged_and_contained():
+    p = custom("badcu", 3, 8, 2, 128, [50, 60, 70], "f16", LAYOUT_VARLEN, 2, seed=8)
+    q, k, v, cu = to_device(p)
+    cu_bad = cu.clone()
+    cu_bad[3] = p.total_kv + 1000        # past the end of K/V
+    out, lse, opart, err = run(p, 2, tensors=(q, k, v, cu_bad))
+    assert err & da.DA_DEVERR_SEQLENS
+    ref, _ = oracle.default().attention(p)
+    assert max_abs(out[:2], ref[:2]) <= OUT_TOL
+    assert not out[2].any() and np.isneginf(lse[2]).all()
+
+
+def test_timeout_path_sets_flag_and_device_survives():
+    ws = da.alloc_workspace(1, 1, 64, 1)
+    da.decode_attn_splitkv_selftest_timeout(ws, 20_000)
+    assert da.decode_attn_splitkv_get_error(ws) == da.DA_DEVERR_TIMEOUT
+    assert da.decode_attn_splitkv_get_error(ws) == 0
+    check_full(workload("tiny"), 4)
+
+
+def test_partial_plus_combine_equals_full_and_is_deterministic():
+    p = custom("det", 2, 28, 4, 128, [900, 1300], "f16", LAYOUT_VARLEN, 6, seed=12)
+    q, k, v, cu = to_device(p)
+    S = 6
+    ws = da.alloc_workspace(p.B, p.Hq, p.D, S)
+    a = torch.empty(p.B, p.Hq, p.D, dtype=torch.float16, device="cuda")
+    b = torch.empty_like(a)
+    da.decode_attn_splitkv(q, k, v, cu, a, ws, num_splits=S, scale=p.scale)
+    da.decode_attn_splitkv_partial(q, k, v, cu, ws, num_splits=S, scale=p.scale)
+    da.decode_attn_splitkv_combine(b, ws, num_splits=S)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    c = torch.empty_like(a)
+    da.decode_attn_splitkv(q, k, v, cu, c, ws, num_splits=S, scale=p.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(a, c)
+
+
+def test_cuda_graph_capture_and_side_stream():
+    p = custom("graph", 4, 32, 8, 128, [700, 20, 1500, 333], "bf16", LAYOUT_VARLEN, 8, seed=13)
+    q, k, v, cu = to_device(p)
+    S = 8
+    side = torch.cuda.Stream()
+    ws = da.alloc_workspace(p.B, p.Hq, p.D, S, stream=side)
+    out = torch.empty(p.B, p.Hq, p.D, dtype=torch.bfloat16, device="cuda")
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        da.decode_attn_splitkv(q, k, v, cu, out, ws, num_splits=S, scale=p.scale, stream=side)
+    side.synchronize()
+    eager = out.clone()
+    g = torch.cuda.CUDAGraph()
+    out.zero_()
+    with torch.cuda.graph(g):
+        da.decode_attn_splitkv(q, k, v, cu, out, ws, num_splits=S, scale=p.scale)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
+    ref, _ = oracle.default().attention(p)
+    assert max_abs(out.to(torch.float64).cpu().numpy(), ref) <= OUT_TOL
