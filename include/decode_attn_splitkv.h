@@ -56,7 +56,9 @@ typedef enum {
     DA_ERR_UNSUPPORTED = 2,         /* head_dim other than 64/128, or no sm_103a device */
     DA_ERR_ALIGNMENT = 3,           /* a pointer is not aligned as documented */
     DA_ERR_WORKSPACE_TOO_SMALL = 4, /* workspace_bytes < decode_attn_splitkv_workspace_size() */
-    DA_ERR_CUDA = 5                 /* a CUDA runtime or driver call failed */
+    DA_ERR_CUDA = 5,                /* a CUDA runtime or driver call failed */
+    DA_ERR_SCRATCH_LIMIT = 6        /* decode_attn_splitkv_noalloc: the problem needs more scratch
+                                       than DA_NOALLOC_SCRATCH_BYTES */
 } da_status;
 
 typedef enum { DA_F16 = 0, DA_BF16 = 1 } da_dtype;
@@ -182,6 +184,46 @@ da_status decode_attn_splitkv_get_error(void* workspace, uint32_t* device_error_
  */
 da_status decode_attn_splitkv_selftest_timeout(void* workspace, size_t workspace_bytes,
                                                unsigned timeout_us, void* stream);
+
+/* Size of the library's built-in scratch array used by decode_attn_splitkv_noalloc. */
+#define DA_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+
+/*
+ * decode_attn_splitkv without a caller-supplied workspace, for callers that
+ * cannot allocate device memory: code that runs behind a plugin or operator
+ * interface which hands it only its input and output buffers and owns every
+ * allocation itself, and code on a latency-critical path where cudaMalloc is
+ * off limits because it can synchronise the whole device. The pages have no
+ * counterpart of this entry point; it is an addition of this library.
+ *
+ * Instead of a workspace it uses one scratch array compiled into the library
+ * (a file-scope __device__ array of DA_NOALLOC_SCRATCH_BYTES = 8 MiB). Every
+ * GPU that loads the library holds that array until the process exits. The
+ * call itself allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ * library routine.
+ *   - Arguments, layout and results are those of decode_attn_splitkv, minus
+ *     the workspace. The per-split results land in the scratch array, where
+ *     the caller cannot read them.
+ *   - Problems whose workspace_size(B, Hq, D, num_splits) exceeds
+ *     DA_NOALLOC_SCRATCH_BYTES are refused with DA_ERR_SCRATCH_LIMIT and
+ *     nothing is enqueued. (For example B=64, Hq=28, D=128 fits up to 9 splits.)
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current and caches it; make
+ *     that first call before any stream capture on the device.
+ *   - All calls share the one array, which keeps the previous call's
+ *     contents; each call clears the part that must start at zero (the error
+ *     word) and overwrites the rest before reading it. Calls that can overlap
+ *     on the GPU (different streams without ordering between them, or
+ *     several host threads) race on the array and corrupt each other's
+ *     results: serialise them.
+ *   - Device-side error bits (DA_DEVERR_*) of these calls are not reported;
+ *     use decode_attn_splitkv with a workspace to diagnose them.
+ * Errors: those of decode_attn_splitkv, plus DA_ERR_SCRATCH_LIMIT.
+ */
+da_status decode_attn_splitkv_noalloc(const void* q, const void* k, const void* v,
+                                      const int32_t* cu_seqlens_k, int B, int Hq, int Hkv,
+                                      int D, int kv_rows, da_dtype dtype, da_layout layout,
+                                      float scale, int num_splits, void* out, void* stream);
 
 /* Static, human-readable name of a status code. */
 const char* decode_attn_splitkv_status_string(da_status status);

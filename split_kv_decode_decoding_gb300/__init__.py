@@ -15,11 +15,12 @@ import os
 from .build import LIB, build
 
 DA_OK, DA_ERR_INVALID_ARG, DA_ERR_UNSUPPORTED, DA_ERR_ALIGNMENT = 0, 1, 2, 3
-DA_ERR_WORKSPACE_TOO_SMALL, DA_ERR_CUDA = 4, 5
+DA_ERR_WORKSPACE_TOO_SMALL, DA_ERR_CUDA, DA_ERR_SCRATCH_LIMIT = 4, 5, 6
 DA_F16, DA_BF16 = 0, 1
 DA_LAYOUT_VARLEN, DA_LAYOUT_BHSD = 0, 1
 DA_DEVERR_SEQLENS, DA_DEVERR_TIMEOUT = 0x1, 0x2
 DA_MAX_SPLITS = 1024
+DA_NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 
 EXPORTED = [
     "decode_attn_splitkv_workspace_size", "decode_attn_splitkv_lse_offset",
@@ -27,6 +28,7 @@ EXPORTED = [
     "decode_attn_splitkv_num_splits", "decode_attn_splitkv_split_range", "decode_attn_splitkv",
     "decode_attn_splitkv_partial", "decode_attn_splitkv_combine", "decode_attn_splitkv_get_error",
     "decode_attn_splitkv_selftest_timeout", "decode_attn_splitkv_status_string",
+    "decode_attn_splitkv_noalloc",
 ]
 
 _lib = None
@@ -71,6 +73,8 @@ def load(path: str = LIB):
     lib.decode_attn_splitkv_get_error.restype = I
     lib.decode_attn_splitkv_selftest_timeout.argtypes = [P, SZ, ctypes.c_uint, P]
     lib.decode_attn_splitkv_selftest_timeout.restype = I
+    lib.decode_attn_splitkv_noalloc.argtypes = [P, P, P, P, I, I, I, I, I, I, I, F, I, P, P]
+    lib.decode_attn_splitkv_noalloc.restype = I
     lib.decode_attn_splitkv_status_string.argtypes = [I]
     lib.decode_attn_splitkv_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -198,3 +202,23 @@ def decode_attn_splitkv_selftest_timeout(workspace, timeout_us: int, stream=None
     _check(load().decode_attn_splitkv_selftest_timeout(_ptr(workspace), workspace.numel(),
                                                        timeout_us, _stream(stream)),
            "decode_attn_splitkv_selftest_timeout")
+
+
+def decode_attn_splitkv_noalloc(q, k, v, cu_seqlens_k, out, *, num_splits: int,
+                                scale: float | None = None, layout: int = DA_LAYOUT_VARLEN,
+                                stream=None):
+    """decode_attn_splitkv with the library's built-in scratch array instead of a workspace.
+
+    For callers that may not allocate device memory (a plugin interface that
+    owns all allocation, or a path where cudaMalloc's device-wide
+    synchronisation is not acceptable). Problems needing more than
+    DA_NOALLOC_SCRATCH_BYTES of scratch raise DecodeAttnError
+    (DA_ERR_SCRATCH_LIMIT). Calls share the array: do not let them overlap.
+    """
+    B, Hq, Hkv, D, kv_rows = _shape_args(q, k, cu_seqlens_k, layout)
+    sc = 1.0 / math.sqrt(D) if scale is None else scale
+    st = load().decode_attn_splitkv_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_k), B, Hq, Hkv, D, kv_rows, _dtype_code(q),
+        layout, sc, num_splits, _ptr(out), _stream(stream))
+    _check(st, "decode_attn_splitkv_noalloc")
+    return out

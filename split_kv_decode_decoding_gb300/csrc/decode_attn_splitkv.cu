@@ -812,8 +812,64 @@ const char* decode_attn_splitkv_status_string(da_status status) {
         case DA_ERR_ALIGNMENT: return "DA_ERR_ALIGNMENT: a pointer is not aligned as documented";
         case DA_ERR_WORKSPACE_TOO_SMALL: return "DA_ERR_WORKSPACE_TOO_SMALL";
         case DA_ERR_CUDA: return "DA_ERR_CUDA: a CUDA runtime or driver call failed";
+        case DA_ERR_SCRATCH_LIMIT:
+            return "DA_ERR_SCRATCH_LIMIT: the problem needs more scratch than the library's "
+                   "8 MiB built-in array (use decode_attn_splitkv with a workspace)";
     }
     return "unknown da_status";
 }
 
 }  // extern "C"
+
+// ================================================================ no-allocation variant
+// For callers that may not allocate device memory: the workspace is a scratch
+// array compiled into this library instead of a caller buffer.
+namespace {
+
+__device__ __align__(256) uint8_t g_noalloc_scratch[DA_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[128] = {};   // device address of g_noalloc_scratch, per device ordinal
+
+// In host code g_noalloc_scratch names a host-side shadow, not device memory:
+// the device address comes from cudaGetSymbolAddress, looked up once per
+// device with that device current.
+da_status noalloc_scratch(void** addr) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return DA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_addr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return DA_ERR_CUDA;
+        g_noalloc_addr[dev] = p;
+    }
+    *addr = g_noalloc_addr[dev];
+    return DA_OK;
+}
+
+}  // namespace
+
+extern "C" da_status decode_attn_splitkv_noalloc(const void* q, const void* k, const void* v,
+                                                 const int32_t* cu_seqlens_k, int B, int Hq, int Hkv,
+                                                 int D, int kv_rows, da_dtype dtype, da_layout layout,
+                                                 float scale, int num_splits, void* out, void* stream) {
+    const size_t need = decode_attn_splitkv_workspace_size(B, Hq, D, num_splits);
+    if (need > DA_NOALLOC_SCRATCH_BYTES) return DA_ERR_SCRATCH_LIMIT;
+    void* ws = nullptr;
+    if (need > 0) {
+        // only sizes that pass the workspace arithmetic reach the device lookup
+        da_status st = noalloc_scratch(&ws);
+        if (st != DA_OK) return st;
+    }
+    da_status st = check_common(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale,
+                                num_splits, ws, DA_NOALLOC_SCRATCH_BYTES);
+    if (st != DA_OK) return st;
+    if (!out) return DA_ERR_INVALID_ARG;
+    if (!aligned(out, 16)) return DA_ERR_ALIGNMENT;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(ws, 0, kHeaderBytes, s) != cudaSuccess) return DA_ERR_CUDA;
+    st = dispatch_split(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale, num_splits,
+                        ws, s);
+    if (st != DA_OK) return st;
+    return dispatch_combine(B, Hq, D, num_splits, dtype, out, ws, s);
+}

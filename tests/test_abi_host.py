@@ -31,14 +31,14 @@ def header_functions():
 
 def test_exports_every_declared_symbol(lib):
     names = header_functions()
-    assert len(names) == 12
+    assert len(names) == 13
     assert sorted(names) == sorted(da.EXPORTED)
     for n in names:
         assert hasattr(lib, n), n
 
 
 def test_status_strings(lib):
-    for code in range(6):
+    for code in range(7):
         s = da.status_string(code)
         assert s and s != "unknown da_status"
     assert da.status_string(99) == "unknown da_status"

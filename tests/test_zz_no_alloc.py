@@ -1,0 +1,71 @@
+"""The no-allocation entry point against the workspace entry point.
+
+decode_attn_splitkv_noalloc exists for callers that cannot allocate device
+memory -- code behind a plugin interface that only hands it input and output
+buffers, or a latency-critical path where cudaMalloc's device-wide
+synchronisation is not allowed. It runs the same kernels on a scratch array
+compiled into the library. This file is collected last on purpose, and works
+both alone in a fresh process and after the rest of the suite.
+"""
+import numpy as np
+import pytest
+import torch
+
+import split_kv_decode_decoding_gb300 as da
+from gpu_util import OUT_TOL, to_device, torch_dtype
+from synth.workloads import LAYOUT_BHSD, LAYOUT_VARLEN, custom
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    da.build()
+    da.load()
+
+
+def with_workspace(p, S, tensors):
+    q, k, v, cu = tensors
+    ws = da.alloc_workspace(p.B, p.Hq, p.D, S)
+    out = torch.empty(p.B, p.Hq, p.D, dtype=torch_dtype(p), device="cuda")
+    da.decode_attn_splitkv(q, k, v, cu, out, ws, num_splits=S, scale=p.scale, layout=p.layout)
+    assert da.decode_attn_splitkv_get_error(ws) == 0
+    return out
+
+
+def test_noalloc_matches_workspace_call_on_two_calls_in_a_row():
+    a = custom("na_a", 4, 28, 4, 128, [700, 1500, 64, 3000], "f16", LAYOUT_VARLEN, 6, seed=71)
+    b = custom("na_b", 3, 32, 8, 128, [2048, 333, 1024], "bf16", LAYOUT_BHSD, 9, seed=72,
+               kv_rows=2048)
+    ta, tb = to_device(a), to_device(b)
+    ref_a = with_workspace(a, 6, ta)
+    ref_b = with_workspace(b, 9, tb)
+    out_a = torch.full_like(ref_a, float("nan"))
+    out_b = torch.full_like(ref_b, float("nan"))
+    # two calls back to back on the same stream; the second reuses the scratch the first left
+    da.decode_attn_splitkv_noalloc(*ta, out_a, num_splits=6, scale=a.scale, layout=a.layout)
+    da.decode_attn_splitkv_noalloc(*tb, out_b, num_splits=9, scale=b.scale, layout=b.layout)
+    torch.cuda.synchronize()
+    for got, ref in ((out_a, ref_a), (out_b, ref_b)):
+        d = (got.double() - ref.double()).abs().max().item()
+        assert d <= OUT_TOL, d
+    # and once more with the first problem, after the second problem's contents
+    again = torch.full_like(ref_a, float("nan"))
+    da.decode_attn_splitkv_noalloc(*ta, again, num_splits=6, scale=a.scale, layout=a.layout)
+    torch.cuda.synchronize()
+    assert (again.double() - ref_a.double()).abs().max().item() <= OUT_TOL
+
+
+def test_noalloc_refuses_problems_beyond_its_scratch():
+    p = custom("na_big", 64, 28, 4, 128, [16] * 64, "f16", LAYOUT_VARLEN, 16, seed=73)
+    need = da.workspace_size(p.B, p.Hq, p.D, 16)
+    assert need > da.DA_NOALLOC_SCRATCH_BYTES
+    q, k, v, cu = to_device(p)
+    out = torch.zeros(p.B, p.Hq, p.D, dtype=torch.float16, device="cuda")
+    with pytest.raises(da.DecodeAttnError) as e:
+        da.decode_attn_splitkv_noalloc(q, k, v, cu, out, num_splits=16, scale=p.scale)
+    assert e.value.status == da.DA_ERR_SCRATCH_LIMIT
+    torch.cuda.synchronize()
+    assert not out.any()
