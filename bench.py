@@ -4,7 +4,7 @@ Prints ONE JSON line (rank 0). A step is one decode-attention call over the whol
 workload: the split kernel then the combine kernel, launched through the C ABI
 (decode_attn_splitkv_partial + decode_attn_splitkv_combine are exactly the two
 launches decode_attn_splitkv makes; timing them apart gives the per-kernel
-durations). L2 is flushed between steps by writing a buffer twice its size.
+durations). L2 is flushed between steps by writing a buffer twice its size, then reading another.
 
   value      KV-read GB/s = 2 * sum(L_b) * Hkv * D * 2 bytes / mean step time
   e2e        the same metric through decode_attn_splitkv with the inputs copied
@@ -173,14 +173,16 @@ def cpu_oracle_sample(p, budget_s: float = 12.0, steps=None):
     if steps is None:
         want = int(budget_s * cores / per_row)
         n = max(probe, min(nrows, want))
+        reps = max(1, min(20, want // nrows)) if n == nrows else 1
         sel = np.linspace(0, nrows - 1, n).astype(np.int64)
         t0 = time.perf_counter()
-        orc.attention_rows(p, rows_b[sel], rows_h[sel], nthreads=cores)
+        for _ in range(reps):
+            orc.attention_rows(p, rows_b[sel], rows_h[sel], nthreads=cores)
         dt = time.perf_counter() - t0
-        frac = n / nrows
+        frac = n * reps / nrows
         gbs = p.kv_bytes * frac / dt / 1e9
-        desc = (f"{n} of {nrows} (b, h) rows of {p.name} (full key ranges), float64, "
-                f"{cores} threads, {dt:.2f} s wall")
+        desc = (f"{n} of {nrows} (b, h) rows of {p.name} (full key ranges) x {reps} passes, "
+                f"float64, {cores} threads, {dt:.2f} s wall")
         return gbs, cores, desc, dt
     budget_per_step = budget_s / steps
     n = max(1, min(nrows, int(budget_per_step * cores / per_row)))
@@ -229,7 +231,7 @@ def workload_config(p, S):
                                          f"{min(p.lens)}..{max(p.lens)} (mean {sum(p.lens) / len(p.lens):.0f})"),
             "layout": "bhsd" if p.layout == 1 else "varlen", "in_dtype": p.dtype,
             "num_splits": S, "kv_bytes": p.kv_bytes,
-            "l2": "flushed between steps (write of 2x L2 size)"}
+            "l2": "flushed between steps (write then read of 2x L2 size)"}
 
 
 def main():
@@ -263,12 +265,16 @@ def main():
     out = torch.empty(p.B, p.Hq, p.D, dtype=q.dtype, device=dev)
     ws = da.alloc_workspace(p.B, p.Hq, p.D, S, device=dev, stream=stream)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(2 * l2, 64 << 20), dtype=torch.uint8, device=dev)
+    # L2 flush: write one buffer twice the L2 size, then read another one, so the
+    # timed kernel starts with none of its inputs cached and no dirty lines to write back
+    flush_w = torch.empty(max(2 * l2, 64 << 20), dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(max(2 * l2, 64 << 20) // 4, dtype=torch.float32, device=dev)
     torch.cuda.synchronize(dev)
 
     def step(ev0=None, ev1=None, ev2=None):
         if not args.no_flush:
-            flush.fill_(1)
+            flush_w.fill_(1)
+            flush_r.sum()
         if ev0 is not None:
             ev0.record(stream)
         da.decode_attn_splitkv_partial(q, k, v, cu, ws, num_splits=S, scale=p.scale,
