@@ -1,10 +1,10 @@
 """Benchmark: split-KV decode attention on one GB300 (or N replicas under torchrun).
 
-Prints ONE JSON line (rank 0). A step is one decode-attention call over the whole
-workload: the split kernel then the combine kernel, launched through the C ABI
-(decode_attn_splitkv_partial + decode_attn_splitkv_combine are exactly the two
-launches decode_attn_splitkv makes; timing them apart gives the per-kernel
-durations). L2 is flushed between steps by writing a buffer twice its size, then reading another.
+Prints ONE JSON line (rank 0). A step is one decode_attn_splitkv call over the
+whole workload (the split kernel then the combine kernel, chained by programmatic
+dependent launch), timed with CUDA events on its stream. After the K steps,
+K/2 more steps call decode_attn_splitkv_partial and decode_attn_splitkv_combine
+(the same two launches) with events around the split kernel alone, for its roofline. L2 is flushed between steps by writing a buffer twice its size, then reading another.
 
   value      KV-read GB/s = 2 * sum(L_b) * Hkv * D * 2 bytes / mean step time
   e2e        the same metric through decode_attn_splitkv with the inputs copied
@@ -59,6 +59,18 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """The maximum of a per-rank float over all ranks (x itself without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    dev = device if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 def measured_peaks():
@@ -271,19 +283,29 @@ def main():
     flush_r = torch.ones(max(2 * l2, 64 << 20) // 4, dtype=torch.float32, device=dev)
     torch.cuda.synchronize(dev)
 
-    def step(ev0=None, ev1=None, ev2=None):
+    def flush():
         if not args.no_flush:
             flush_w.fill_(1)
             flush_r.sum()
+
+    def step(ev0=None, ev1=None):
+        # one public call: split kernel + combine kernel (chained by programmatic launch)
+        flush()
         if ev0 is not None:
             ev0.record(stream)
-        da.decode_attn_splitkv_partial(q, k, v, cu, ws, num_splits=S, scale=p.scale,
-                                       layout=p.layout, stream=stream)
+        da.decode_attn_splitkv(q, k, v, cu, out, ws, num_splits=S, scale=p.scale,
+                               layout=p.layout, stream=stream)
         if ev1 is not None:
             ev1.record(stream)
+
+    def split_step(ev0, ev1):
+        # the split kernel alone, for its roofline; the combine follows untimed
+        flush()
+        ev0.record(stream)
+        da.decode_attn_splitkv_partial(q, k, v, cu, ws, num_splits=S, scale=p.scale,
+                                       layout=p.layout, stream=stream)
+        ev1.record(stream)
         da.decode_attn_splitkv_combine(out, ws, num_splits=S, stream=stream)
-        if ev2 is not None:
-            ev2.record(stream)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -291,7 +313,9 @@ def main():
         torch.cuda.synchronize(dev)
         if da.decode_attn_splitkv_get_error(ws, stream=stream) != 0:
             raise RuntimeError("device error flag set during warm-up")
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        k_split = max(1, args.steps // 2)
+        evk = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(k_split)]
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize(dev)
@@ -301,6 +325,8 @@ def main():
         t_wall = time.perf_counter()
         for i in range(args.steps):
             step(*evs[i])
+        for i in range(k_split):
+            split_step(*evk[i])
         torch.cuda.synchronize(dev)
         t_wall = time.perf_counter() - t_wall
         if sampler:
@@ -309,14 +335,9 @@ def main():
             torch.distributed.barrier()
     if da.decode_attn_splitkv_get_error(ws, stream=stream) != 0:
         raise RuntimeError("device error flag set during the timed steps")
-    split_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(args.steps)]
-    comb_ms = [evs[i][1].elapsed_time(evs[i][2]) for i in range(args.steps)]
-    step_ms = [evs[i][0].elapsed_time(evs[i][2]) for i in range(args.steps)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    step_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(args.steps)]
+    split_ms = [evk[i][0].elapsed_time(evk[i][1]) for i in range(k_split)]
+    total_ms = max_over_ranks(sum(step_ms), dev)
     mean_step_ms = total_ms / args.steps
     value = world * p.kv_bytes / (mean_step_ms * 1e-3) / 1e9
 
@@ -377,9 +398,10 @@ def main():
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "traffic": traffic, "alg_bytes_per_launch": alg_bytes,
                      "launch_us_mean": round(split_mean_ms * 1e3, 2),
-                     "combine_us_mean": round(sum(comb_ms) / len(comb_ms) * 1e3, 2)},
+                     "launches_timed": k_split,
+                     "combine_us_mean_derived": round((mean_step_ms - split_mean_ms) * 1e3, 2)},
         "e2e": e2e,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": 2 * args.steps + 2 * k_split,
         "wall_s_timed_region": round(t_wall, 3),
     }
     if sampler:

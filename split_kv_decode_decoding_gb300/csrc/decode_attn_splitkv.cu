@@ -1,33 +1,43 @@
 // Split-KV decode attention (flash-decoding) for GB300 / sm_103a.
 //
-// Split step (one CTA per (sequence b, KV head, head chunk, split s)):
-//   * The GQA group of the KV head (up to 8 query heads per CTA) is packed
-//     into the N = 8 columns of an m16n8k16 tensor-core product, so every K/V
-//     byte is read from HBM once per group (TileLang decode_attention_splitkv.py,
-//     split segment, cur_kv_head; CS349E lecture 11 04_flash_decoding.py,
-//     demo1_exact second observation).
-//   * Keys are the M rows: S^T[key, head] = K_tile . Q^T, then
-//     O^T[dim, head] += V_tile^T . P^T. The score fragment becomes the P^T
-//     operand with one movmatrix transpose per 8x8 block, so P never touches
-//     shared memory.
-//   * K and V tiles arrive by TMA (cp.async.bulk.tensor, 128-byte swizzle)
-//     into a ring of shared-memory stages guarded by full/empty mbarriers; one
-//     producer warp issues the copies, four consumer warps each own 16 keys of
-//     every 64-key stage.
+// Split step: a persistent kernel, two CTAs per SM (more at head_dim 64), that
+// takes work items (sequence b, KV head, head chunk, split s) from a queue in
+// the workspace. For each item it computes, for the up-to-8 query heads of the
+// KV head's group that the chunk holds, the normalised partial output o_s and
+// lse_s = ln sum_{j in split} exp(s_j), and writes them to the workspace.
+//   * The GQA group (up to 8 query heads) is packed into the N = 8 columns of
+//     m16n8k16 tensor-core products, so every K/V byte is read from HBM once
+//     per group (TileLang decode_attention_splitkv.py, split segment,
+//     cur_kv_head; CS349E lecture 11 04_flash_decoding.py, demo1_exact second
+//     observation). Keys are the M rows: S^T[key, head] = K_tile . Q^T, then
+//     O^T[dim, head] += V_tile^T . P^T; the score fragment turns into the P^T
+//     operand with one movmatrix transpose per 8x8 block, so P stays in
+//     registers.
+//   * One producer warp runs ahead of four consumer warps: it takes the next
+//     item from the queue, publishes its descriptor and bulk-copies its Q rows
+//     into shared memory, and streams the item's K and V tiles with TMA
+//     (cp.async.bulk.tensor, 128-byte swizzle; 64-key boxes for full stages,
+//     16-key boxes for the ragged end of a split) into a three-stage ring
+//     guarded by full/empty mbarriers. The ring keeps filling
+//     across item boundaries, so one item's epilogue overlaps the next item's
+//     loads. Each consumer warp owns 16 keys of every 64-key stage.
 //   * Online softmax in the exp2 domain (scale * log2 e folded into the
-//     scores) with running max m, running sum l and accumulator, per warp, in
-//     fp32 registers (TileLang page, split segment online softmax; MiniInfer
-//     flash_decode_splitk.py, _splitk_stage1_kernel). The four warps' states
-//     are merged in shared memory at the end; the split writes the normalised
-//     o_s and lse_s = ln l + m (natural log) to the workspace.
+//     scores), with running max, running sum and accumulator per consumer warp
+//     in fp32 registers (TileLang page, split segment online softmax; MiniInfer
+//     flash_decode_splitk.py, _splitk_stage1_kernel). At the end of an item
+//     the producer hands the consumers one ring stage instead of a tile, and
+//     the four warps merge their states through it in a fixed order (the
+//     result does not depend on timing).
 //   * Split bounds are proportional: [L*s/S, L*(s+1)/S) in 64-bit integers
 //     (TileLang page, split segment). Keys of a stage past the split end are
-//     masked to -inf before the max; TMA reads past the K/V extent are
-//     zero-filled by the hardware, so no load leaves the tensor.
-// Combine step (one CTA per (b, query head)): lse = ln sum exp(lse_s),
-// out = sum exp(lse_s - lse) * o_s, skipping empty splits (TileLang page,
-// combine segment, with the weight indexed by head row; MiniInfer
-// _splitk_reduce_kernel).
+//     masked to -inf before the max, and their V rows are cleared in shared
+//     memory (0 * NaN is NaN); TMA reads past the K/V extent are zero-filled
+//     by the hardware, so no load leaves the tensor.
+// Combine step: one warp per (b, query head, slice of head_dim), reading the
+// splits' lse and o from L2: lse = ln sum exp(lse_s), out = sum exp(lse_s -
+// lse) * o_s, empty splits weighing 0 (TileLang page, combine segment, with
+// the weight indexed by head row; MiniInfer _splitk_reduce_kernel).
+// The two kernels are chained with programmatic dependent launch.
 //
 // Every mbarrier wait is bounded in time; on expiry the kernel sets
 // DA_DEVERR_TIMEOUT in the workspace error word and winds down instead of
@@ -52,12 +62,24 @@ constexpr int kBoxKeys = 16;        // keys per TMA box = rows of one mma m-tile
 constexpr int kStageKeys = 64;      // keys per pipeline stage
 constexpr int kConsumerWarps = 4;   // each owns 16 keys of a stage
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kHeadsPerCta = 8;     // mma N: packed query heads per CTA
-constexpr int kStages = 3;          // pipeline depth (two CTAs fit per SM at D = 128)
+constexpr int kHeadsPerCta = 8;     // mma N: packed query heads per item
+constexpr int kStages = 3;          // pipeline depth (two CTAs per SM at head_dim 128)
+constexpr int kMinBlocksPerSm = 2;
+constexpr int kItemSlots = 2;       // item descriptors the producer may run ahead
 constexpr size_t kHeaderBytes = 256;
+constexpr size_t kWorkCounterOff = 64;   // header: uint32 work-queue head
+constexpr size_t kDoneCounterOff = 128;  // header: uint32 count of CTAs finished
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
+
+struct ItemSlot {          // one work item, as the producer decoded it
+    int32_t b, kvh, h0, nh;
+    int32_t s, nkeys, ntiles, valid;   // valid = 0 marks the end of the queue
+    int64_t first_key;                 // varlen: K/V row of the split start; bhsd: position
+    int64_t pad;
+};
+static_assert(sizeof(ItemSlot) == 48, "ItemSlot layout");
 
 template <int D>
 struct Shape {
@@ -66,11 +88,22 @@ struct Shape {
     static constexpr int kTileBytes = kHalves * kSliceBytes;       // K (or V) bytes per stage
     static constexpr int kStageBytes = 2 * kTileBytes;             // K + V
     static constexpr int kBoxBytes = kBoxKeys * 128;               // one TMA box
-    static constexpr int kMergeBytes = kConsumerWarps * (D * kHeadsPerCta + 2 * kHeadsPerCta) * 4;
     static constexpr int kRingBytes = kStages * kStageBytes;
-    static constexpr int kSmemBytes =
-        1024 /* alignment slack */ + (kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes) +
-        2 * kStages * 8 /* barriers */;
+    // Item merge, laid out in the ring stage the producer hands over at the end of
+    // each item: per-warp accumulators [warp][head][D + 4] (the pad keeps both the
+    // fragment stores and the row reads free of bank conflicts), then [warp][8]
+    // maxima and [warp][8] sums.
+    static constexpr int kMergeRow = D + 4;
+    static constexpr int kMergeBytes = (kConsumerWarps * kHeadsPerCta * kMergeRow + 2 * kConsumerWarps * kHeadsPerCta) * 4;
+    static_assert(kMergeBytes <= kStageBytes, "item merge must fit in one ring stage");
+    static constexpr int kQBytes = kHeadsPerCta * D * 2;           // Q rows of one item
+    static constexpr int kQOff = kRingBytes;
+    static constexpr int kSlotOff = kQOff + kItemSlots * kQBytes;
+    static constexpr int kBarOff = kSlotOff + kItemSlots * (int)sizeof(ItemSlot);
+    static constexpr int kNumBars = 2 * kStages + 2 * kItemSlots + 1;
+    static constexpr int kEnd = kBarOff + kNumBars * 8;
+    static constexpr int kSmemBytes = 1024 /* alignment slack */ + kEnd;
+    static_assert(kQOff % 16 == 0 && kSlotOff % 16 == 0 && kBarOff % 8 == 0, "smem alignment");
 };
 
 struct SplitParams {
@@ -79,7 +112,9 @@ struct SplitParams {
     float* lse;              // [B, Hq, S]
     float* opart;            // [B, Hq, S, D]
     uint32_t* err;           // device error word
-    int B, Hq, Hkv, G, S, kv_rows, layout, chunks, no_kv;
+    uint32_t* work;          // work-queue head
+    uint32_t* done;          // CTAs finished
+    int B, Hq, Hkv, G, S, kv_rows, layout, chunks, no_kv, n_items;
     float scale_log2;        // scale * log2(e)
     unsigned long long wait_limit_ns;
 };
@@ -124,6 +159,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
     }
 }
 
+// mbar_wait by every lane of a warp, with one verdict for the whole warp, so
+// that the warp-synchronous instructions after it are never split by a
+// time-out that only some lanes saw.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
+                                               unsigned long long limit_ns) {
+    const bool ok = mbar_wait(bar, parity, limit_ns);
+    return __all_sync(0xffffffffu, ok);
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -142,8 +186,24 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// Contiguous global -> shared copy (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dependents_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
@@ -194,17 +254,6 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     return r;
 }
 
-template <int DT>
-__device__ __forceinline__ uint16_t to_bits(float a) {
-    uint16_t r;
-    if constexpr (DT == DA_F16) {
-        asm("cvt.rn.f16.f32 %0, %1;" : "=h"(r) : "f"(a));
-    } else {
-        asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(a));
-    }
-    return r;
-}
-
 // 2^x on the SFU (ex2.approx; 2^-inf = +0).
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
@@ -212,95 +261,189 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+__device__ __forceinline__ int ld_cg_s32(const int32_t* p) {
+    int v;
+    asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float ld_cg_f32(const float* p) {
+    float v;
+    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float4 ld_cg_f32x4(const float* p) {
+    float4 v;
+    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ void flag_error(uint32_t* err, uint32_t bits) { atomicOr(err, bits); }
 
-// Sequence b's key range, validated against the K/V extent. Returns false (and
-// flags DA_DEVERR_SEQLENS) when it cannot be read safely.
-__device__ __forceinline__ bool seq_range(const SplitParams& p, int b, int64_t& base, int64_t& L) {
-    const int64_t c0 = p.cu[b], c1 = p.cu[b + 1];
-    L = c1 - c0;
-    base = p.layout == DA_LAYOUT_VARLEN ? c0 : 0;
+// Decode work item `idx` into its descriptor (reads cu_seqlens_k). Flags a
+// sequence whose range cannot be read safely and treats it as empty.
+__device__ __forceinline__ ItemSlot decode_item(const SplitParams& p, int idx) {
+    ItemSlot it;
+    int r = idx;
+    it.s = r % p.S;
+    r /= p.S;
+    const int chunk = r % p.chunks;
+    r /= p.chunks;
+    it.kvh = r % p.Hkv;
+    it.b = r / p.Hkv;
+    it.h0 = it.kvh * p.G + chunk * kHeadsPerCta;
+    it.nh = min(kHeadsPerCta, p.G - chunk * kHeadsPerCta);
+    const int64_t c0 = ld_cg_s32(p.cu + it.b), c1 = ld_cg_s32(p.cu + it.b + 1);
+    int64_t L = c1 - c0;
+    const int64_t base = p.layout == DA_LAYOUT_VARLEN ? c0 : 0;
     bool ok = L >= 0;
     if (p.layout == DA_LAYOUT_VARLEN) ok = ok && c0 >= 0 && c1 <= p.kv_rows;
     else ok = ok && L <= p.kv_rows;
     if (p.no_kv) ok = ok && L == 0;
-    if (!ok) L = 0;
-    return ok;
+    if (!ok) {
+        L = 0;
+        if (it.s == 0 && chunk == 0 && it.kvh == 0) flag_error(p.err, DA_DEVERR_SEQLENS);
+    }
+    const int64_t lo = L * it.s / p.S, hi = L * (it.s + 1) / p.S;
+    it.nkeys = static_cast<int>(hi - lo);
+    it.ntiles = (it.nkeys + kStageKeys - 1) / kStageKeys;
+    it.first_key = base + lo;
+    it.valid = 1;
+    it.pad = 0;
+    return it;
 }
 
 // ------------------------------------------------------------ split step
 template <int D, int DT>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, kMinBlocksPerSm)
 split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+             const __grid_constant__ CUtensorMap tmK16, const __grid_constant__ CUtensorMap tmV16,
              const SplitParams p) {
     using Sh = Shape<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
-    const int ring_or_merge = Sh::kRingBytes > Sh::kMergeBytes ? Sh::kRingBytes : Sh::kMergeBytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ring_or_merge);
+    ItemSlot* slots = reinterpret_cast<ItemSlot*>(smem + Sh::kSlotOff);
     const uint32_t ring = smem_addr(smem);
-    const uint32_t full0 = smem_addr(bars);
-    const uint32_t empty0 = full0 + kStages * 8;
+    const uint32_t qbuf = ring + Sh::kQOff;
+    const uint32_t full0 = ring + Sh::kBarOff;          // [kStages]
+    const uint32_t empty0 = full0 + 8 * kStages;        // [kStages]
+    const uint32_t ifull0 = empty0 + 8 * kStages;       // [kItemSlots]
+    const uint32_t iempty0 = ifull0 + 8 * kItemSlots;   // [kItemSlots]
+    const uint32_t mfull = iempty0 + 8 * kItemSlots;    // an item's per-warp partials written
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int s = blockIdx.x;
-    const int chunk = blockIdx.y % p.chunks;
-    const int kvh = blockIdx.y / p.chunks;
-    const int b = blockIdx.z;
-    const int h0 = kvh * p.G + chunk * kHeadsPerCta;
-    const int nh = min(kHeadsPerCta, p.G - chunk * kHeadsPerCta);
-
-    int64_t base, L;
-    const bool seq_ok = seq_range(p, b, base, L);
-    if (!seq_ok && threadIdx.x == 0 && s == 0 && blockIdx.y == 0) flag_error(p.err, DA_DEVERR_SEQLENS);
-    const int64_t lo = L * s / p.S;
-    const int64_t hi = L * (s + 1) / p.S;
-    const int nkeys = static_cast<int>(hi - lo);
-    const int ntiles = (nkeys + kStageKeys - 1) / kStageKeys;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(full0 + 8 * i, 1);
             mbar_init(empty0 + 8 * i, kConsumerWarps);
         }
+        for (int i = 0; i < kItemSlots; ++i) {
+            mbar_init(ifull0 + 8 * i, 1);
+            mbar_init(iempty0 + 8 * i, kConsumerWarps);
+        }
+        mbar_init(mfull, kConsumerWarps);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == kConsumerWarps && lane == 0 && ntiles > 0) {
+    if (warp == kConsumerWarps && lane == 0 && p.no_kv == 0) {
         prefetch_tensormap(&tmK);
         prefetch_tensormap(&tmV);
+        prefetch_tensormap(&tmK16);
+        prefetch_tensormap(&tmV16);
     }
     __syncthreads();
+    // Everything above overlaps the previous kernel in the stream; from here on
+    // this grid touches global memory, so wait for that kernel to finish.
+    grid_dependency_wait();
+    if (threadIdx.x == 0) grid_dependents_launch();
 
     if (warp == kConsumerWarps) {
-        // ---------------- producer: one lane issues every TMA copy
+        // ---------------- producer: one lane takes items and issues every copy
         if (lane == 0) {
-            for (int t = 0; t < ntiles; ++t) {
-                const int st = t % kStages;
-                const uint32_t ph = (t / kStages) & 1;
+            int st = 0;          // ring position of the next tile
+            uint32_t ph = 0;     // its phase parity
+            for (uint32_t it = 0;; ++it) {
+                const int slot = it % kItemSlots;
+                const uint32_t iph = (it / kItemSlots) & 1;
+                if (!mbar_wait(iempty0 + 8 * slot, iph ^ 1, p.wait_limit_ns)) {
+                    flag_error(p.err, DA_DEVERR_TIMEOUT);
+                    break;
+                }
+                const int idx = static_cast<int>(atomicAdd(p.work, 1u));
+                if (idx >= p.n_items) {
+                    slots[slot].valid = 0;
+                    mbar_arrive(ifull0 + 8 * slot);
+                    break;
+                }
+                const ItemSlot item = decode_item(p, idx);
+                slots[slot] = item;
+                const uint32_t ib = ifull0 + 8 * slot;
+                mbar_arrive_expect_tx(ib, item.nh * D * 2);
+                bulk_load(qbuf + slot * Sh::kQBytes, p.q + (static_cast<int64_t>(item.b) * p.Hq + item.h0) * D,
+                          item.nh * D * 2, ib);
+                bool ok = true;
+                for (int t = 0; t < item.ntiles; ++t) {
+                    if (!mbar_wait(empty0 + 8 * st, ph ^ 1, p.wait_limit_ns)) {
+                        flag_error(p.err, DA_DEVERR_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    const int keys_t = min(kStageKeys, item.nkeys - t * kStageKeys);
+                    const uint32_t fb = full0 + 8 * st;
+                    const uint32_t kdst = ring + st * Sh::kStageBytes;
+                    const uint32_t vdst = kdst + Sh::kTileBytes;
+                    const int key0 = static_cast<int>(item.first_key) + t * kStageKeys;
+                    const int slab = item.b * p.Hkv + item.kvh;
+                    if (keys_t == kStageKeys) {
+                        // a full stage: one 64-key box per 128-byte column slice
+                        mbar_arrive_expect_tx(fb, Sh::kHalves * 2 * Sh::kSliceBytes);
+                        for (int hf = 0; hf < Sh::kHalves; ++hf) {
+                            const uint32_t off = hf * Sh::kSliceBytes;
+                            if (p.layout == DA_LAYOUT_VARLEN) {
+                                tma_load_3d(kdst + off, &tmK, hf * 64, item.kvh, key0, fb);
+                                tma_load_3d(vdst + off, &tmV, hf * 64, item.kvh, key0, fb);
+                            } else {
+                                tma_load_3d(kdst + off, &tmK, hf * 64, key0, slab, fb);
+                                tma_load_3d(vdst + off, &tmV, hf * 64, key0, slab, fb);
+                            }
+                        }
+                    } else {
+                        // the ragged last stage of a split: 16-key boxes up to its end
+                        const int nbox = (keys_t + kBoxKeys - 1) / kBoxKeys;
+                        mbar_arrive_expect_tx(fb, nbox * Sh::kHalves * 2 * Sh::kBoxBytes);
+                        for (int bx = 0; bx < nbox; ++bx) {
+                            const int key = key0 + bx * kBoxKeys;
+                            for (int hf = 0; hf < Sh::kHalves; ++hf) {
+                                const uint32_t off = hf * Sh::kSliceBytes + bx * Sh::kBoxBytes;
+                                if (p.layout == DA_LAYOUT_VARLEN) {
+                                    tma_load_3d(kdst + off, &tmK16, hf * 64, item.kvh, key, fb);
+                                    tma_load_3d(vdst + off, &tmV16, hf * 64, item.kvh, key, fb);
+                                } else {
+                                    tma_load_3d(kdst + off, &tmK16, hf * 64, key, slab, fb);
+                                    tma_load_3d(vdst + off, &tmV16, hf * 64, key, slab, fb);
+                                }
+                            }
+                        }
+                    }
+                    if (++st == kStages) {
+                        st = 0;
+                        ph ^= 1;
+                    }
+                }
+                if (!ok) break;
+                // Hand the next stage to the consumers, empty, for this item's merge.
                 if (!mbar_wait(empty0 + 8 * st, ph ^ 1, p.wait_limit_ns)) {
                     flag_error(p.err, DA_DEVERR_TIMEOUT);
                     break;
                 }
-                const int keys_t = min(kStageKeys, nkeys - t * kStageKeys);
-                const int nbox = (keys_t + kBoxKeys - 1) / kBoxKeys;
-                const uint32_t fb = full0 + 8 * st;
-                mbar_arrive_expect_tx(fb, nbox * Sh::kHalves * 2 * Sh::kBoxBytes);
-                const uint32_t kdst = ring + st * Sh::kStageBytes;
-                const uint32_t vdst = kdst + Sh::kTileBytes;
-                for (int bx = 0; bx < nbox; ++bx) {
-                    const int key = static_cast<int>(base + lo) + t * kStageKeys + bx * kBoxKeys;
-                    for (int hf = 0; hf < Sh::kHalves; ++hf) {
-                        const uint32_t off = hf * Sh::kSliceBytes + bx * Sh::kBoxBytes;
-                        if (p.layout == DA_LAYOUT_VARLEN) {
-                            tma_load_3d(kdst + off, &tmK, hf * 64, kvh, key, fb);
-                            tma_load_3d(vdst + off, &tmV, hf * 64, kvh, key, fb);
-                        } else {
-                            const int slab = b * p.Hkv + kvh;
-                            tma_load_3d(kdst + off, &tmK, hf * 64, key, slab, fb);
-                            tma_load_3d(vdst + off, &tmV, hf * 64, key, slab, fb);
-                        }
-                    }
+                mbar_arrive(full0 + 8 * st);
+                if (++st == kStages) {
+                    st = 0;
+                    ph ^= 1;
                 }
             }
         }
@@ -309,200 +452,294 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
 
     // ---------------- consumers
     const int g = lane >> 2, t4 = lane & 3;
-    // Q^T fragments (B operand, k16 x n8): head g, dims ks*16 + 2*t4 (+1) and +8 (+9).
-    uint32_t qf[D / 16][2];
-    {
-        const bool hv = g < nh;
-        const uint32_t* qrow =
-            reinterpret_cast<const uint32_t*>(p.q + (static_cast<int64_t>(b) * p.Hq + h0 + (hv ? g : 0)) * D);
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-            qf[ks][0] = hv ? qrow[ks * 8 + t4] : 0u;
-            qf[ks][1] = hv ? qrow[ks * 8 + 4 + t4] : 0u;
-        }
-    }
-
-    float acc[D / 16][4];
-#pragma unroll
-    for (int i = 0; i < D / 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-    float m_run[2] = {-INFINITY, -INFINITY};   // heads 2*t4, 2*t4+1 (log2 domain)
-    float l_run[2] = {0.f, 0.f};               // this thread's share of the running sum
-    bool ok = true;
-    uint32_t bad_bar = 0, bad_ph = 0;
-
-    // ldmatrix lane geometry
     const int mi = lane >> 3, r8 = lane & 7;
     const int krow = warp * kBoxKeys + (mi & 1) * 8 + r8;      // K: matrices (rows lo/hi) x (k lo/hi)
     const int kchunk_add = mi >> 1;
     const int vrow = warp * kBoxKeys + (mi >> 1) * 8 + r8;     // V^T: matrices (dims lo/hi) x (keys lo/hi)
     const int vchunk_add = mi & 1;
+    bool ok = true;
+    uint32_t bad_bar = 0, bad_ph = 0;
+    int st = 0;          // ring position of the next tile
+    uint32_t ph = 0;     // its phase parity
 
-    for (int t = 0; t < ntiles; ++t) {
-        const int st = t % kStages;
-        const uint32_t ph = (t / kStages) & 1;
-        const uint32_t fb = full0 + 8 * st;
-        if (ok && !mbar_wait(fb, ph, p.wait_limit_ns)) {
-            ok = false;
-            bad_bar = fb;
-            bad_ph = ph;
+    uint32_t it = 0;
+    for (;; ++it) {
+        const int slot = it % kItemSlots;
+        const uint32_t iph = (it / kItemSlots) & 1;
+        if (!mbar_wait_warp(ifull0 + 8 * slot, iph, p.wait_limit_ns)) {
             if (lane == 0) flag_error(p.err, DA_DEVERR_TIMEOUT);
+            ok = false;
+            break;
         }
-        const int keys_t = min(kStageKeys, nkeys - t * kStageKeys);
-        bool zeroed = false;
-        if (ok && warp * kBoxKeys < keys_t) {
-            const uint32_t kbase = ring + st * Sh::kStageBytes;
-            const uint32_t vbase = kbase + Sh::kTileBytes;
-            const int valid_rows = keys_t - warp * kBoxKeys;
-            if (valid_rows < kBoxKeys) {
-                // The box's rows past the split end hold other keys (or, in a
-                // padded cache, anything): their P is 0, but 0 * NaN is not, so
-                // clear those V rows before the PV product.
-                const int per_row = Sh::kHalves * 8;   // 16-byte chunks per row
-                for (int c = lane; c < (kBoxKeys - valid_rows) * per_row; c += 32) {
-                    const int r = valid_rows + c / per_row;
-                    const int hf = (c % per_row) >> 3, ch = c & 7;
-                    const uint32_t addr = vbase + hf * Sh::kSliceBytes + (warp * kBoxKeys + r) * 128 + ch * 16;
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
-                }
-                zeroed = true;
-                __syncwarp();
-            }
-            // S^T[16 keys, 8 heads] = K_tile . Q^T
-            float sc[4] = {0.f, 0.f, 0.f, 0.f};
+        const ItemSlot item = slots[slot];
+        // Q^T fragments (B operand, k16 x n8): head g, dims ks*16 + 2*t4 (+1) and +8 (+9).
+        uint32_t qf[D / 16][2];
+        {
+            const bool hv = g < item.nh;
+            const uint32_t qrow = qbuf + slot * Sh::kQBytes + (hv ? g : 0) * D * 2;
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
-                const int chunk16 = ks * 2 + kchunk_add;          // 16-byte chunk along D
-                const uint32_t addr = kbase + (chunk16 >> 3) * Sh::kSliceBytes + krow * 128 +
-                                      (((chunk16 & 7) ^ (krow & 7)) << 4);
-                uint32_t a[4];
-                ldsm_x4(addr, a);
-                mma_16816<DT>(sc, a, qf[ks][0], qf[ks][1]);
+                uint32_t a0, a1;
+                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(a0) : "r"(qrow + (ks * 16 + 2 * t4) * 2));
+                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(a1) : "r"(qrow + (ks * 16 + 8 + 2 * t4) * 2));
+                qf[ks][0] = hv ? a0 : 0u;
+                qf[ks][1] = hv ? a1 : 0u;
             }
-            // scores -> exp2 domain, mask keys past the split end
-            const int key_lo = t * kStageKeys + warp * kBoxKeys + g;   // relative to split start
-            const bool va = key_lo < nkeys, vb = key_lo + 8 < nkeys;
-            float x0 = va ? sc[0] * p.scale_log2 : -INFINITY;
-            float x1 = va ? sc[1] * p.scale_log2 : -INFINITY;
-            float x2 = vb ? sc[2] * p.scale_log2 : -INFINITY;
-            float x3 = vb ? sc[3] * p.scale_log2 : -INFINITY;
-            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
-#pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-            }
-            const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
-            const float al0 = fast_exp2(m_run[0] - mn0), al1 = fast_exp2(m_run[1] - mn1);
-            const float p0 = fast_exp2(x0 - mn0), p1 = fast_exp2(x1 - mn1);
-            const float p2 = fast_exp2(x2 - mn0), p3 = fast_exp2(x3 - mn1);
-            l_run[0] = l_run[0] * al0 + (p0 + p2);
-            l_run[1] = l_run[1] * al1 + (p1 + p3);
-            m_run[0] = mn0;
-            m_run[1] = mn1;
-#pragma unroll
-            for (int i = 0; i < D / 16; ++i) {
-                acc[i][0] *= al0;
-                acc[i][1] *= al1;
-                acc[i][2] *= al0;
-                acc[i][3] *= al1;
-            }
-            // P^T operand (k16 keys x n8 heads) via 8x8 transposes of the score fragment
-            const uint32_t pb0 = movmatrix_trans(pack2<DT>(p0, p1));
-            const uint32_t pb1 = movmatrix_trans(pack2<DT>(p2, p3));
-            // O^T[D, 8] += V_tile^T . P^T
-#pragma unroll
-            for (int i = 0; i < D / 16; ++i) {
-                const int chunk16 = i * 2 + vchunk_add;
-                const uint32_t addr = vbase + (chunk16 >> 3) * Sh::kSliceBytes + vrow * 128 +
-                                      (((chunk16 & 7) ^ (vrow & 7)) << 4);
-                uint32_t a[4];
-                ldsm_x4_trans(addr, a);
-                mma_16816<DT>(acc[i], a, pb0, pb1);
-            }
-        }
-        if (zeroed) {
-            // order the generic-proxy stores above before the next TMA write to this stage
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
         __syncwarp();
+        if (lane == 0) mbar_arrive(iempty0 + 8 * slot);
+        if (!item.valid) break;
+
+        float acc[D / 16][4];
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+        float m_run[2] = {-INFINITY, -INFINITY};   // heads 2*t4, 2*t4+1 (log2 domain)
+        float l_run[2] = {0.f, 0.f};               // this thread's share of the running sum
+
+        for (int t = 0; t < item.ntiles; ++t) {
+            const uint32_t fb = full0 + 8 * st;
+            if (ok && !mbar_wait_warp(fb, ph, p.wait_limit_ns)) {
+                ok = false;
+                bad_bar = fb;
+                bad_ph = ph;
+                if (lane == 0) flag_error(p.err, DA_DEVERR_TIMEOUT);
+            }
+            const int keys_t = min(kStageKeys, item.nkeys - t * kStageKeys);
+            bool zeroed = false;
+            if (ok && warp * kBoxKeys < keys_t) {
+                const uint32_t kbase = ring + st * Sh::kStageBytes;
+                const uint32_t vbase = kbase + Sh::kTileBytes;
+                const int valid_rows = keys_t - warp * kBoxKeys;
+                if (valid_rows < kBoxKeys) {
+                    // The box's rows past the split end hold other keys (or, in a
+                    // padded cache, anything): their P is 0, but 0 * NaN is not, so
+                    // clear those V rows before the PV product.
+                    const int per_row = Sh::kHalves * 8;   // 16-byte chunks per row
+                    for (int c = lane; c < (kBoxKeys - valid_rows) * per_row; c += 32) {
+                        const int r = valid_rows + c / per_row;
+                        const int hf = (c % per_row) >> 3, ch = c & 7;
+                        const uint32_t addr = vbase + hf * Sh::kSliceBytes + (warp * kBoxKeys + r) * 128 + ch * 16;
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+                    }
+                    zeroed = true;
+                    __syncwarp();
+                }
+                // S^T[16 keys, 8 heads] = K_tile . Q^T, two independent accumulator chains
+                float sc[4] = {0.f, 0.f, 0.f, 0.f};
+                float sd[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const int chunk16 = ks * 2 + kchunk_add;          // 16-byte chunk along D
+                    const uint32_t addr = kbase + (chunk16 >> 3) * Sh::kSliceBytes + krow * 128 +
+                                          (((chunk16 & 7) ^ (krow & 7)) << 4);
+                    uint32_t a[4];
+                    ldsm_x4(addr, a);
+                    if (ks & 1) mma_16816<DT>(sd, a, qf[ks][0], qf[ks][1]);
+                    else mma_16816<DT>(sc, a, qf[ks][0], qf[ks][1]);
+                }
+                // scores -> exp2 domain, mask keys past the split end
+                const int key_lo = t * kStageKeys + warp * kBoxKeys + g;   // relative to split start
+                const bool va = key_lo < item.nkeys, vb = key_lo + 8 < item.nkeys;
+                const float x0 = va ? (sc[0] + sd[0]) * p.scale_log2 : -INFINITY;
+                const float x1 = va ? (sc[1] + sd[1]) * p.scale_log2 : -INFINITY;
+                const float x2 = vb ? (sc[2] + sd[2]) * p.scale_log2 : -INFINITY;
+                const float x3 = vb ? (sc[3] + sd[3]) * p.scale_log2 : -INFINITY;
+                float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                }
+                const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
+                const float p0 = fast_exp2(x0 - mn0), p1 = fast_exp2(x1 - mn1);
+                const float p2 = fast_exp2(x2 - mn0), p3 = fast_exp2(x3 - mn1);
+                if (mn0 != m_run[0] || mn1 != m_run[1]) {
+                    const float al0 = fast_exp2(m_run[0] - mn0), al1 = fast_exp2(m_run[1] - mn1);
+                    l_run[0] *= al0;
+                    l_run[1] *= al1;
+#pragma unroll
+                    for (int i = 0; i < D / 16; ++i) {
+                        acc[i][0] *= al0;
+                        acc[i][1] *= al1;
+                        acc[i][2] *= al0;
+                        acc[i][3] *= al1;
+                    }
+                    m_run[0] = mn0;
+                    m_run[1] = mn1;
+                }
+                l_run[0] += p0 + p2;
+                l_run[1] += p1 + p3;
+                // P^T operand (k16 keys x n8 heads) via 8x8 transposes of the score fragment
+                const uint32_t pb0 = movmatrix_trans(pack2<DT>(p0, p1));
+                const uint32_t pb1 = movmatrix_trans(pack2<DT>(p2, p3));
+                // O^T[D, 8] += V_tile^T . P^T
+#pragma unroll
+                for (int i = 0; i < D / 16; ++i) {
+                    const int chunk16 = i * 2 + vchunk_add;
+                    const uint32_t addr = vbase + (chunk16 >> 3) * Sh::kSliceBytes + vrow * 128 +
+                                          (((chunk16 & 7) ^ (vrow & 7)) << 4);
+                    uint32_t a[4];
+                    ldsm_x4_trans(addr, a);
+                    mma_16816<DT>(acc[i], a, pb0, pb1);
+                }
+            }
+            if (zeroed) {
+                // order the generic-proxy stores above before the next TMA write to this stage
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * st);
+            if (++st == kStages) {
+                st = 0;
+                ph ^= 1;
+            }
+        }
+
+        // per-thread partial sums -> per-warp sums (over the 8 key rows g)
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], off);
+            l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], off);
+        }
+
+        // ---------------- merge the four warps' states for this item, in the
+        // ring stage the producer handed over (it loads nothing into it)
+        if (ok && !mbar_wait_warp(full0 + 8 * st, ph, p.wait_limit_ns)) {
+            ok = false;
+            if (lane == 0) flag_error(p.err, DA_DEVERR_TIMEOUT);
+        }
+        float* red_acc = reinterpret_cast<float*>(smem + st * Sh::kStageBytes);   // [warp][8][D+4]
+        float* red_m = red_acc + kConsumerWarps * kHeadsPerCta * Sh::kMergeRow;    // [warp][8]
+        float* red_l = red_m + kConsumerWarps * kHeadsPerCta;                       // [warp][8]
+        if (g == 0) {
+            red_m[warp * kHeadsPerCta + 2 * t4] = m_run[0];
+            red_m[warp * kHeadsPerCta + 2 * t4 + 1] = m_run[1];
+            red_l[warp * kHeadsPerCta + 2 * t4] = l_run[0];
+            red_l[warp * kHeadsPerCta + 2 * t4 + 1] = l_run[1];
+        }
+        {
+            float* h0row = red_acc + (warp * kHeadsPerCta + 2 * t4) * Sh::kMergeRow;
+            float* h1row = h0row + Sh::kMergeRow;
+#pragma unroll
+            for (int i = 0; i < D / 16; ++i) {
+                h0row[i * 16 + g] = acc[i][0];
+                h1row[i * 16 + g] = acc[i][1];
+                h0row[i * 16 + g + 8] = acc[i][2];
+                h1row[i * 16 + g + 8] = acc[i][3];
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(mfull);
+        if (ok && !mbar_wait_warp(mfull, it & 1, p.wait_limit_ns)) {
+            ok = false;
+            if (lane == 0) flag_error(p.err, DA_DEVERR_TIMEOUT);
+        }
+        for (int idx = threadIdx.x; idx < item.nh * D; idx += kConsumerWarps * 32) {
+            const int hh = idx / D, d = idx % D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, red_m[w * kHeadsPerCta + hh]);
+            float o = 0.f, lsum = 0.f;
+            if (M != -INFINITY) {
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) {
+                    const float wt = fast_exp2(red_m[w * kHeadsPerCta + hh] - M);
+                    lsum += wt * red_l[w * kHeadsPerCta + hh];
+                    o += wt * red_acc[(w * kHeadsPerCta + hh) * Sh::kMergeRow + d];
+                }
+                o = o / lsum;
+            }
+            const int64_t row = (static_cast<int64_t>(item.b) * p.Hq + item.h0 + hh) * p.S + item.s;
+            p.opart[row * D + d] = o;
+            if (d == 0) p.lse[row] = M == -INFINITY ? -INFINITY : (M + log2f(lsum)) * kLn2;
+        }
+        // release the stage: order these generic-proxy stores before the TMA writes that refill it
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * st);
+        if (++st == kStages) {
+            st = 0;
+            ph ^= 1;
+        }
+        if (!ok) break;
     }
     if (!ok) {
-        // give a copy that may still be landing one more bounded wait before the CTA exits
-        mbar_wait(bad_bar, bad_ph, p.wait_limit_ns);
+        // a copy may still be landing: give it one more bounded wait before the CTA exits
+        if (bad_bar != 0) mbar_wait(bad_bar, bad_ph, p.wait_limit_ns);
+        return;
     }
-
-    // per-thread partial sums -> per-warp sums (over the 8 key rows g)
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-        l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], off);
-        l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], off);
-    }
-
-    // ---------------- merge the four warps' states (reusing the ring)
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-    float* red_acc = reinterpret_cast<float*>(smem);                        // [warp][D][8]
-    float* red_m = red_acc + kConsumerWarps * D * kHeadsPerCta;             // [warp][8]
-    float* red_l = red_m + kConsumerWarps * kHeadsPerCta;                   // [warp][8]
-    if (g == 0) {
-        red_m[warp * kHeadsPerCta + 2 * t4] = m_run[0];
-        red_m[warp * kHeadsPerCta + 2 * t4 + 1] = m_run[1];
-        red_l[warp * kHeadsPerCta + 2 * t4] = l_run[0];
-        red_l[warp * kHeadsPerCta + 2 * t4 + 1] = l_run[1];
-    }
-#pragma unroll
-    for (int i = 0; i < D / 16; ++i) {
-        float* r0 = red_acc + (warp * D + i * 16 + g) * kHeadsPerCta + 2 * t4;
-        float* r1 = r0 + 8 * kHeadsPerCta;
-        *reinterpret_cast<float2*>(r0) = make_float2(acc[i][0], acc[i][1]);
-        *reinterpret_cast<float2*>(r1) = make_float2(acc[i][2], acc[i][3]);
-    }
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-
-    const int tid = threadIdx.x;
-    for (int idx = tid; idx < nh * D; idx += kConsumerWarps * 32) {
-        const int hh = idx / D, d = idx % D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, red_m[w * kHeadsPerCta + hh]);
-        float o = 0.f, lsum = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const float wt = fast_exp2(red_m[w * kHeadsPerCta + hh] - M);
-                lsum += wt * red_l[w * kHeadsPerCta + hh];
-                o += wt * red_acc[(w * D + d) * kHeadsPerCta + hh];
-            }
-            o = o / lsum;
+    // The last CTA to finish re-arms the work queue for the next call.
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const uint32_t prev = atomicAdd(p.done, 1u);
+        if (prev == gridDim.x - 1) {
+            __threadfence();
+            atomicExch(p.work, 0u);
+            atomicExch(p.done, 0u);
         }
-        const int64_t row = (static_cast<int64_t>(b) * p.Hq + h0 + hh) * p.S + s;
-        p.opart[row * D + d] = o;
-        if (d == 0) p.lse[row] = M == -INFINITY ? -INFINITY : (M + log2f(lsum)) * kLn2;
     }
 }
 
 // ------------------------------------------------------------ combine step
+// One warp per (row = (b, query head), slice of DC = D / dchunks dims). Each
+// lane owns four dims of one split at a time; 32 / (DC / 4) splits are read per
+// iteration and folded together with shuffles at the end.
 template <int D, int DT>
-__global__ void __launch_bounds__(D) combine_kernel(const float* __restrict__ lse,
-                                                    const float* __restrict__ opart,
-                                                    uint16_t* __restrict__ out, int S) {
-    const int64_t row = blockIdx.x;
-    const int d = threadIdx.x;
-    const float* l = lse + row * S;
+__global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ lse,
+                                                      const float* __restrict__ opart,
+                                                      uint16_t* __restrict__ out, int rows, int S,
+                                                      int dchunks) {
+    grid_dependency_wait();
+    if (threadIdx.x == 0) grid_dependents_launch();
+    const int warp_id = blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (warp_id >= rows * dchunks) return;
+    const int row = warp_id / dchunks, dc = warp_id % dchunks;
+    const int DC = D / dchunks;
+    const int lps = DC / 4;               // lanes per split row
+    const int spi = 32 / lps;             // splits per iteration
+    const int sub = lane / lps, dv = lane % lps;
+    const float* l = lse + static_cast<int64_t>(row) * S;
+
     float M = -INFINITY;
-    for (int s = 0; s < S; ++s) M = fmaxf(M, l[s]);
-    float o = 0.f;
-    if (M != -INFINITY) {
-        float z = 0.f;
-        for (int s = 0; s < S; ++s) z += fast_exp2((l[s] - M) * kLog2e);
-        const float inv = 1.f / z;
-        const float* po = opart + row * S * D + d;
-        for (int s = 0; s < S; ++s) {
-            const float w = fast_exp2((l[s] - M) * kLog2e) * inv;
-            o += w * po[static_cast<int64_t>(s) * D];
-        }
+    for (int s = lane; s < S; s += 32) M = fmaxf(M, ld_cg_f32(l + s));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const int d0 = dc * DC + dv * 4;
+    uint16_t* o = out + static_cast<int64_t>(row) * D + d0;
+    if (M == -INFINITY) {
+        if (sub == 0) *reinterpret_cast<uint2*>(o) = make_uint2(0u, 0u);
+        return;
     }
-    out[row * D + d] = to_bits<DT>(o);
+    const float Ml = M * kLog2e;
+    float z = 0.f;
+    for (int s = lane; s < S; s += 32) z += fast_exp2(fmaf(ld_cg_f32(l + s), kLog2e, -Ml));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float* po = opart + static_cast<int64_t>(row) * S * D + d0;
+#pragma unroll 4
+    for (int s = sub; s < S; s += spi) {
+        const float w = fast_exp2(fmaf(ld_cg_f32(l + s), kLog2e, -Ml));
+        const float4 v = ld_cg_f32x4(po + static_cast<int64_t>(s) * D);
+        acc.x = fmaf(w, v.x, acc.x);
+        acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z);
+        acc.w = fmaf(w, v.w, acc.w);
+    }
+    for (int off = lps; off < 32; off <<= 1) {
+        acc.x += __shfl_xor_sync(0xffffffffu, acc.x, off);
+        acc.y += __shfl_xor_sync(0xffffffffu, acc.y, off);
+        acc.z += __shfl_xor_sync(0xffffffffu, acc.z, off);
+        acc.w += __shfl_xor_sync(0xffffffffu, acc.w, off);
+    }
+    if (sub == 0) {
+        const float inv = 1.f / z;
+        const uint32_t lo = pack2<DT>(acc.x * inv, acc.y * inv);
+        const uint32_t hi = pack2<DT>(acc.z * inv, acc.w * inv);
+        *reinterpret_cast<uint2*>(o) = make_uint2(lo, hi);
+    }
 }
 
 // ------------------------------------------------------------ diagnostics
@@ -538,7 +775,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 bool make_kv_map(CUtensorMap* map, const void* base, da_dtype dt, da_layout lay, int B, int Hkv,
-                 int D, int kv_rows) {
+                 int D, int kv_rows, int box_rows) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3], strides[2];
@@ -547,12 +784,12 @@ bool make_kv_map(CUtensorMap* map, const void* base, da_dtype dt, da_layout lay,
         dims[0] = D; dims[1] = Hkv; dims[2] = kv_rows;
         strides[0] = static_cast<cuuint64_t>(D) * 2;
         strides[1] = static_cast<cuuint64_t>(Hkv) * D * 2;
-        box[0] = 64; box[1] = 1; box[2] = kBoxKeys;
+        box[0] = 64; box[1] = 1; box[2] = box_rows;
     } else {
         dims[0] = D; dims[1] = kv_rows; dims[2] = static_cast<cuuint64_t>(B) * Hkv;
         strides[0] = static_cast<cuuint64_t>(D) * 2;
         strides[1] = static_cast<cuuint64_t>(kv_rows) * D * 2;
-        box[0] = 64; box[1] = kBoxKeys; box[2] = 1;
+        box[0] = 64; box[1] = box_rows; box[2] = 1;
     }
     CUresult r = fn(map, dt == DA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                     3, const_cast<void*>(base), dims, strides, box, estr,
@@ -561,18 +798,34 @@ bool make_kv_map(CUtensorMap* map, const void* base, da_dtype dt, da_layout lay,
     return r == CUDA_SUCCESS;
 }
 
-// Raise the dynamic shared-memory limit of `kernel` once per device; `done`
-// is the caller's per-kernel bit set of devices already configured.
+// Per-kernel, per-device launch facts: the dynamic shared-memory limit is
+// raised once per device and the persistent grid size is cached.
+struct DeviceCache {
+    std::atomic<uint64_t> attr_done{0};
+    std::atomic<int> grid[64] = {};
+};
+
 template <class K>
-cudaError_t ensure_smem_attr(K kernel, int bytes, std::atomic<uint64_t>& done) {
+cudaError_t persistent_grid(K kernel, int smem, DeviceCache& cache, int* grid) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const uint64_t bit = 1ull << (dev & 63);
-    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
-    return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    const uint64_t bit = 1ull << dev;
+    if (!(cache.attr_done.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        int sms = 0, per_sm = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem);
+        if (e != cudaSuccess) return e;
+        if (per_sm < 1) return cudaErrorInvalidConfiguration;
+        cache.grid[dev].store(sms * per_sm, std::memory_order_relaxed);
+        cache.attr_done.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    *grid = cache.grid[dev].load(std::memory_order_relaxed);
+    return cudaSuccess;
 }
 
 da_status check_common(const void* q, const void* k, const void* v, const int32_t* cu, int B, int Hq,
@@ -591,28 +844,45 @@ da_status check_common(const void* q, const void* k, const void* v, const int32_
     const size_t need = decode_attn_splitkv_workspace_size(B, Hq, D, S);
     if (need == 0) return DA_ERR_INVALID_ARG;
     if (ws_bytes < need) return DA_ERR_WORKSPACE_TOO_SMALL;
-    if (lay == DA_LAYOUT_BHSD && static_cast<int64_t>(B) * Hkv > 0xffffffffll) return DA_ERR_INVALID_ARG;
+    const int64_t chunks = (Hq / Hkv + kHeadsPerCta - 1) / kHeadsPerCta;
+    if (static_cast<int64_t>(B) * Hkv * chunks * S > 0x7fffffffll) return DA_ERR_INVALID_ARG;
     return DA_OK;
+}
+
+cudaLaunchAttribute pdl_attr() {
+    cudaLaunchAttribute a;
+    a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    a.val.programmaticStreamSerializationAllowed = 1;
+    return a;
 }
 
 template <int D, int DT>
 da_status launch_split(const void* q, const void* k, const void* v, const int32_t* cu, int B, int Hq,
                        int Hkv, int kv_rows, da_layout lay, float scale, int S, void* ws,
                        cudaStream_t stream) {
-    alignas(64) CUtensorMap mk, mv;
+    // 64-key boxes for full stages, 16-key boxes for the ragged end of a split
+    alignas(64) CUtensorMap mk, mv, mk16, mv16;
     std::memset(&mk, 0, sizeof(mk));
     std::memset(&mv, 0, sizeof(mv));
+    std::memset(&mk16, 0, sizeof(mk16));
+    std::memset(&mv16, 0, sizeof(mv16));
     if (kv_rows > 0) {
-        if (!make_kv_map(&mk, k, static_cast<da_dtype>(DT), lay, B, Hkv, D, kv_rows) ||
-            !make_kv_map(&mv, v, static_cast<da_dtype>(DT), lay, B, Hkv, D, kv_rows))
+        const da_dtype dt = static_cast<da_dtype>(DT);
+        if (!make_kv_map(&mk, k, dt, lay, B, Hkv, D, kv_rows, kStageKeys) ||
+            !make_kv_map(&mv, v, dt, lay, B, Hkv, D, kv_rows, kStageKeys) ||
+            !make_kv_map(&mk16, k, dt, lay, B, Hkv, D, kv_rows, kBoxKeys) ||
+            !make_kv_map(&mv16, v, dt, lay, B, Hkv, D, kv_rows, kBoxKeys))
             return DA_ERR_CUDA;
     }
     SplitParams p;
+    uint8_t* wsb = static_cast<uint8_t*>(ws);
     p.q = static_cast<const uint16_t*>(q);
     p.cu = cu;
-    p.err = static_cast<uint32_t*>(ws);
-    p.lse = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + decode_attn_splitkv_lse_offset());
-    p.opart = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + decode_attn_splitkv_opart_offset(B, Hq, S));
+    p.err = reinterpret_cast<uint32_t*>(wsb);
+    p.work = reinterpret_cast<uint32_t*>(wsb + kWorkCounterOff);
+    p.done = reinterpret_cast<uint32_t*>(wsb + kDoneCounterOff);
+    p.lse = reinterpret_cast<float*>(wsb + decode_attn_splitkv_lse_offset());
+    p.opart = reinterpret_cast<float*>(wsb + decode_attn_splitkv_opart_offset(B, Hq, S));
     p.B = B;
     p.Hq = Hq;
     p.Hkv = Hkv;
@@ -622,22 +892,32 @@ da_status launch_split(const void* q, const void* k, const void* v, const int32_
     p.layout = lay;
     p.chunks = (p.G + kHeadsPerCta - 1) / kHeadsPerCta;
     p.no_kv = kv_rows == 0;
+    p.n_items = B * Hkv * p.chunks * S;
     p.scale_log2 = scale * kLog2e;
     p.wait_limit_ns = kWaitLimitNs;
 
     const int smem = Shape<D>::kSmemBytes;
     auto kern = split_kernel<D, DT>;
-    static std::atomic<uint64_t> attr_done{0};
-    if (ensure_smem_attr(kern, smem, attr_done) != cudaSuccess) return DA_ERR_CUDA;
-    if (static_cast<int64_t>(Hkv) * p.chunks > 65535 || B > 65535) return DA_ERR_INVALID_ARG;
+    static DeviceCache cache;
+    int grid = 0;
+    if (persistent_grid(kern, smem, cache, &grid) != cudaSuccess) return DA_ERR_CUDA;
+    grid = std::min(grid, p.n_items);
+    cudaLaunchAttribute attrs[1] = {pdl_attr()};
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(S, Hkv * p.chunks, B);
+    cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cfg.attrs = nullptr;
-    cfg.numAttrs = 0;
-    return cudaLaunchKernelEx(&cfg, kern, mk, mv, p) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
+    cfg.attrs = attrs;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, mk, mv, mk16, mv16, p) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
+}
+
+// dims per combine warp: enough warps to cover the GPU, at least 8 dims each
+int combine_dchunks(int rows, int D, int S) {
+    int dchunks = 1;
+    while (D / dchunks > 8 && static_cast<int64_t>(rows) * dchunks < 2048 && S > 4 * dchunks) dchunks *= 2;
+    return dchunks;
 }
 
 template <int D, int DT>
@@ -646,13 +926,19 @@ da_status launch_combine(int B, int Hq, int S, void* out, const void* ws, cudaSt
                                                       decode_attn_splitkv_lse_offset());
     const float* opart = reinterpret_cast<const float*>(static_cast<const uint8_t*>(ws) +
                                                         decode_attn_splitkv_opart_offset(B, Hq, S));
+    const int rows = B * Hq;
+    const int dchunks = combine_dchunks(rows, D, S);
+    const int64_t warps = static_cast<int64_t>(rows) * dchunks;
+    cudaLaunchAttribute attrs[1] = {pdl_attr()};
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(static_cast<int64_t>(B) * Hq));
-    cfg.blockDim = dim3(D);
+    cfg.gridDim = dim3(static_cast<unsigned>((warps + 3) / 4));
+    cfg.blockDim = dim3(128);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
-    return cudaLaunchKernelEx(&cfg, combine_kernel<D, DT>, lse, opart, static_cast<uint16_t*>(out), S) ==
-                   cudaSuccess
+    cfg.attrs = attrs;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, combine_kernel<D, DT>, lse, opart, static_cast<uint16_t*>(out), rows, S,
+                              dchunks) == cudaSuccess
                ? DA_OK
                : DA_ERR_CUDA;
 }
@@ -723,8 +1009,8 @@ int decode_attn_splitkv_num_splits(int B, int Hq, int Hkv, int D, int min_kv, in
     }
     const int64_t chunks = (Hq / Hkv + kHeadsPerCta - 1) / kHeadsPerCta;
     const int64_t units = static_cast<int64_t>(B) * Hkv * chunks;
-    const int64_t slots = static_cast<int64_t>(sm_count) * 2;   // two resident split CTAs per SM
-    // Aim for about four CTAs per resident slot so that unequal splits balance out.
+    const int64_t slots = static_cast<int64_t>(sm_count) * 2;   // work items in flight per wave
+    // Aim for about four items per slot so that unequal splits balance out.
     int64_t S = (4 * slots + units - 1) / units;
     // Keep every split at least kMinKeys long (one or more full stages) ...
     constexpr int64_t kMinKeys = 128;
@@ -756,7 +1042,7 @@ da_status decode_attn_splitkv_combine(int B, int Hq, int D, int num_splits, da_d
     if (!aligned(out, 16) || !aligned(workspace, 256)) return DA_ERR_ALIGNMENT;
     if (workspace_bytes < decode_attn_splitkv_workspace_size(B, Hq, D, num_splits))
         return DA_ERR_WORKSPACE_TOO_SMALL;
-    if (static_cast<int64_t>(B) * Hq > 0x7fffffffll) return DA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(B) * Hq * D > 0x7fffffffll) return DA_ERR_INVALID_ARG;
     return dispatch_combine(B, Hq, D, num_splits, dtype, out, workspace, static_cast<cudaStream_t>(stream));
 }
 
@@ -769,6 +1055,7 @@ da_status decode_attn_splitkv(const void* q, const void* k, const void* v, const
     if (st != DA_OK) return st;
     if (!out) return DA_ERR_INVALID_ARG;
     if (!aligned(out, 16)) return DA_ERR_ALIGNMENT;
+    if (static_cast<int64_t>(B) * Hq * D > 0x7fffffffll) return DA_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     st = dispatch_split(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale, num_splits,
                         workspace, s);

@@ -1,0 +1,67 @@
+"""Host-side pieces of bench.py: rank aggregation (2 gloo ranks on CPU), clock parsing."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        q.put((rank, bench.max_over_ranks(10.0 + 5.0 * rank)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    got = dict(q.get(timeout=10) for _ in range(2))
+    assert got == {0: 15.0, 1: 15.0}
+
+
+def test_max_over_ranks_without_process_group():
+    assert bench.max_over_ranks(3.5) == 3.5
+
+
+def test_clock_summary_parsing():
+    c = bench.ClockSampler(0)
+    c.lines = [
+        "0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "0, 1980, 2070, 1350.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "0, 2070, 2070, 1000.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+    ]
+    s = c.summary()
+    assert s["sm_mhz"] == 2070 and s["sm_max_mhz"] == 2070 and s["reasons"] == ["sw_power_cap"]
+    c.lines = []
+    assert c.summary()["reasons"] == ["no samples"]
+
+
+def test_recorded_traffic_needs_current_kernel(tmp_path, monkeypatch):
+    f = tmp_path / "t.json"
+    f.write_text('{"entries": [{"kernel_sha": "%s", "workload": "w", "num_splits": 3, '
+                 '"dram_bytes_per_launch": 123.0}]}' % bench.kernel_sha())
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    assert bench.recorded_traffic("w", 3) == 123.0
+    assert bench.recorded_traffic("w", 4) is None
+    f.write_text('{"entries": [{"kernel_sha": "old", "workload": "w", "num_splits": 3, '
+                 '"dram_bytes_per_launch": 1.0}]}')
+    assert bench.recorded_traffic("w", 3) is None
