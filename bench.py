@@ -401,7 +401,7 @@ def main():
                      "launches_timed": k_split,
                      "combine_us_mean_derived": round((mean_step_ms - split_mean_ms) * 1e3, 2)},
         "e2e": e2e,
-        "gpu_launches": 2 * args.steps + 2 * k_split,
+        "gpu_launches": (1 if S == 1 else 2) * args.steps + 2 * k_split,
         "wall_s_timed_region": round(t_wall, 3),
     }
     if sampler:

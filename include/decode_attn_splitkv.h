@@ -105,13 +105,14 @@ da_status decode_attn_splitkv_workspace_init(void* workspace, size_t workspace_b
 
 /*
  * Split-count picker (host only, enqueues nothing). Chooses num_splits for a
- * batch whose KV lengths lie in [min_kv, max_kv] so that the split step's CTAs
- * (B * Hkv * ceil(G/8) * num_splits of them) cover the GPU's SMs several times
- * over, while every split keeps at least a minimum number of keys and no split
- * is empty (num_splits <= min_kv; the TileLang page's scheduling constraint,
- * split kernel docstring). sm_count 0 means: query the current device.
- * Returns a value in [1, DA_MAX_SPLITS]; 1 when min_kv <= 0 or an argument is
- * out of range.
+ * batch whose KV lengths lie in [min_kv, max_kv]. The split step has
+ * B * Hkv * ceil(G/8) * num_splits work items. For even lengths it aims at
+ * about one item per SM with splits of 256 to 1024 keys; for ragged lengths
+ * (max_kv >= 2 * min_kv) at about eight items per SM, so the work queue can
+ * balance unequal splits. No split is ever empty (num_splits <= min_kv; the
+ * TileLang page's scheduling constraint, split kernel docstring). sm_count 0
+ * means: query the current device. Returns a value in [1, DA_MAX_SPLITS]; 1
+ * when min_kv <= 0 or an argument is out of range.
  */
 int decode_attn_splitkv_num_splits(int B, int Hq, int Hkv, int D, int min_kv, int max_kv,
                                    int sm_count);

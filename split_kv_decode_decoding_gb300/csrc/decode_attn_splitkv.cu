@@ -37,7 +37,8 @@
 // splits' lse and o from L2: lse = ln sum exp(lse_s), out = sum exp(lse_s -
 // lse) * o_s, empty splits weighing 0 (TileLang page, combine segment, with
 // the weight indexed by head row; MiniInfer _splitk_reduce_kernel).
-// The two kernels are chained with programmatic dependent launch.
+// The two kernels are chained with programmatic dependent launch. With a single
+// split the split kernel writes the output itself and no combine is launched.
 //
 // Every mbarrier wait is bounded in time; on expiry the kernel sets
 // DA_DEVERR_TIMEOUT in the workspace error word and winds down instead of
@@ -114,6 +115,7 @@ struct SplitParams {
     uint32_t* err;           // device error word
     uint32_t* work;          // work-queue head
     uint32_t* done;          // CTAs finished
+    uint16_t* out;           // [B, Hq, D] when S == 1 (o_0 is the output), else nullptr
     int B, Hq, Hkv, G, S, kv_rows, layout, chunks, no_kv, n_items;
     float scale_log2;        // scale * log2(e)
     unsigned long long wait_limit_ns;
@@ -254,6 +256,17 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     return r;
 }
 
+template <int DT>
+__device__ __forceinline__ uint16_t to_bits(float a) {
+    uint16_t r;
+    if constexpr (DT == DA_F16) {
+        asm("cvt.rn.f16.f32 %0, %1;" : "=h"(r) : "f"(a));
+    } else {
+        asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(a));
+    }
+    return r;
+}
+
 // 2^x on the SFU (ex2.approx; 2^-inf = +0).
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
@@ -264,20 +277,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
 __device__ __forceinline__ int ld_cg_s32(const int32_t* p) {
     int v;
     asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p));
-    return v;
-}
-
-__device__ __forceinline__ float ld_cg_f32(const float* p) {
-    float v;
-    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
-    return v;
-}
-
-__device__ __forceinline__ float4 ld_cg_f32x4(const float* p) {
-    float4 v;
-    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "l"(p));
     return v;
 }
 
@@ -373,7 +372,9 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
                     flag_error(p.err, DA_DEVERR_TIMEOUT);
                     break;
                 }
-                const int idx = static_cast<int>(atomicAdd(p.work, 1u));
+                // the first item of each CTA is its own index; later ones come from the queue
+                const int idx = it == 0 ? static_cast<int>(blockIdx.x)
+                                        : static_cast<int>(gridDim.x + atomicAdd(p.work, 1u));
                 if (idx >= p.n_items) {
                     slots[slot].valid = 0;
                     mbar_arrive(ifull0 + 8 * slot);
@@ -652,6 +653,8 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
             const int64_t row = (static_cast<int64_t>(item.b) * p.Hq + item.h0 + hh) * p.S + item.s;
             p.opart[row * D + d] = o;
             if (d == 0) p.lse[row] = M == -INFINITY ? -INFINITY : (M + log2f(lsum)) * kLn2;
+            // one split: its weight exp(lse_0 - lse) is 1, so o_0 is the answer
+            if (p.out != nullptr) p.out[(static_cast<int64_t>(item.b) * p.Hq + item.h0 + hh) * D + d] = to_bits<DT>(o);
         }
         // release the stage: order these generic-proxy stores before the TMA writes that refill it
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -681,9 +684,32 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
 }
 
 // ------------------------------------------------------------ combine step
+// Fold one split (its lse and four dims of its o) into a lane's running
+// (max, sum, weighted accumulator); the max moves up as larger lse arrive, so a
+// single pass over the splits suffices. Empty splits (lse = -inf) weigh 0.
+__device__ __forceinline__ void combine_fold(float lv, float4 ov, float& m, float& z, float4& acc) {
+    if (lv == -INFINITY) return;
+    if (lv > m) {
+        const float sc = fast_exp2((m - lv) * kLog2e);   // 0 when m is still -inf
+        acc.x *= sc;
+        acc.y *= sc;
+        acc.z *= sc;
+        acc.w *= sc;
+        z *= sc;
+        m = lv;
+    }
+    const float w = fast_exp2((lv - m) * kLog2e);
+    acc.x = fmaf(w, ov.x, acc.x);
+    acc.y = fmaf(w, ov.y, acc.y);
+    acc.z = fmaf(w, ov.z, acc.z);
+    acc.w = fmaf(w, ov.w, acc.w);
+    z += w;
+}
+
 // One warp per (row = (b, query head), slice of DC = D / dchunks dims). Each
 // lane owns four dims of one split at a time; 32 / (DC / 4) splits are read per
-// iteration and folded together with shuffles at the end.
+// iteration, four iterations' loads are issued together, and the lanes' partial
+// states are merged with shuffles at the end (a fixed order: deterministic).
 template <int D, int DT>
 __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ lse,
                                                       const float* __restrict__ opart,
@@ -699,46 +725,58 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
     const int lps = DC / 4;               // lanes per split row
     const int spi = 32 / lps;             // splits per iteration
     const int sub = lane / lps, dv = lane % lps;
-    const float* l = lse + static_cast<int64_t>(row) * S;
-
-    float M = -INFINITY;
-    for (int s = lane; s < S; s += 32) M = fmaxf(M, ld_cg_f32(l + s));
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     const int d0 = dc * DC + dv * 4;
-    uint16_t* o = out + static_cast<int64_t>(row) * D + d0;
-    if (M == -INFINITY) {
-        if (sub == 0) *reinterpret_cast<uint2*>(o) = make_uint2(0u, 0u);
-        return;
-    }
-    const float Ml = M * kLog2e;
-    float z = 0.f;
-    for (int s = lane; s < S; s += 32) z += fast_exp2(fmaf(ld_cg_f32(l + s), kLog2e, -Ml));
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float* l = lse + static_cast<int64_t>(row) * S;
     const float* po = opart + static_cast<int64_t>(row) * S * D + d0;
-#pragma unroll 4
-    for (int s = sub; s < S; s += spi) {
-        const float w = fast_exp2(fmaf(ld_cg_f32(l + s), kLog2e, -Ml));
-        const float4 v = ld_cg_f32x4(po + static_cast<int64_t>(s) * D);
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z);
-        acc.w = fmaf(w, v.w, acc.w);
+
+    float m = -INFINITY, z = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int s = sub;
+    for (; s + 3 * spi < S; s += 4 * spi) {
+        float lv[4];
+        float4 ov[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            lv[u] = __ldcg(l + s + u * spi);
+            ov[u] = __ldcg(reinterpret_cast<const float4*>(po + static_cast<int64_t>(s + u * spi) * D));
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) combine_fold(lv[u], ov[u], m, z, acc);
     }
+    for (; s < S; s += spi)
+        combine_fold(__ldcg(l + s), __ldcg(reinterpret_cast<const float4*>(po + static_cast<int64_t>(s) * D)), m,
+                     z, acc);
+    // merge the lanes that hold the same dims
     for (int off = lps; off < 32; off <<= 1) {
-        acc.x += __shfl_xor_sync(0xffffffffu, acc.x, off);
-        acc.y += __shfl_xor_sync(0xffffffffu, acc.y, off);
-        acc.z += __shfl_xor_sync(0xffffffffu, acc.z, off);
-        acc.w += __shfl_xor_sync(0xffffffffu, acc.w, off);
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+        const float z2 = __shfl_xor_sync(0xffffffffu, z, off);
+        float4 a2;
+        a2.x = __shfl_xor_sync(0xffffffffu, acc.x, off);
+        a2.y = __shfl_xor_sync(0xffffffffu, acc.y, off);
+        a2.z = __shfl_xor_sync(0xffffffffu, acc.z, off);
+        a2.w = __shfl_xor_sync(0xffffffffu, acc.w, off);
+        const float M = fmaxf(m, m2);
+        if (M != -INFINITY) {
+            const float a = m == -INFINITY ? 0.f : fast_exp2((m - M) * kLog2e);
+            const float b = m2 == -INFINITY ? 0.f : fast_exp2((m2 - M) * kLog2e);
+            acc.x = a * acc.x + b * a2.x;
+            acc.y = a * acc.y + b * a2.y;
+            acc.z = a * acc.z + b * a2.z;
+            acc.w = a * acc.w + b * a2.w;
+            z = a * z + b * z2;
+            m = M;
+        }
     }
     if (sub == 0) {
-        const float inv = 1.f / z;
-        const uint32_t lo = pack2<DT>(acc.x * inv, acc.y * inv);
-        const uint32_t hi = pack2<DT>(acc.z * inv, acc.w * inv);
-        *reinterpret_cast<uint2*>(o) = make_uint2(lo, hi);
+        uint16_t* o = out + static_cast<int64_t>(row) * D + d0;
+        if (m == -INFINITY) {
+            *reinterpret_cast<uint2*>(o) = make_uint2(0u, 0u);
+        } else {
+            const float inv = 1.f / z;
+            const uint32_t lo = pack2<DT>(acc.x * inv, acc.y * inv);
+            const uint32_t hi = pack2<DT>(acc.z * inv, acc.w * inv);
+            *reinterpret_cast<uint2*>(o) = make_uint2(lo, hi);
+        }
     }
 }
 
@@ -858,7 +896,7 @@ cudaLaunchAttribute pdl_attr() {
 
 template <int D, int DT>
 da_status launch_split(const void* q, const void* k, const void* v, const int32_t* cu, int B, int Hq,
-                       int Hkv, int kv_rows, da_layout lay, float scale, int S, void* ws,
+                       int Hkv, int kv_rows, da_layout lay, float scale, int S, void* ws, void* out,
                        cudaStream_t stream) {
     // 64-key boxes for full stages, 16-key boxes for the ragged end of a split
     alignas(64) CUtensorMap mk, mv, mk16, mv16;
@@ -881,6 +919,7 @@ da_status launch_split(const void* q, const void* k, const void* v, const int32_
     p.err = reinterpret_cast<uint32_t*>(wsb);
     p.work = reinterpret_cast<uint32_t*>(wsb + kWorkCounterOff);
     p.done = reinterpret_cast<uint32_t*>(wsb + kDoneCounterOff);
+    p.out = S == 1 ? static_cast<uint16_t*>(out) : nullptr;
     p.lse = reinterpret_cast<float*>(wsb + decode_attn_splitkv_lse_offset());
     p.opart = reinterpret_cast<float*>(wsb + decode_attn_splitkv_opart_offset(B, Hq, S));
     p.B = B;
@@ -943,14 +982,15 @@ da_status launch_combine(int B, int Hq, int S, void* out, const void* ws, cudaSt
                : DA_ERR_CUDA;
 }
 
+// `out` may be nullptr (split step only); with one split the split kernel writes it.
 da_status dispatch_split(const void* q, const void* k, const void* v, const int32_t* cu, int B, int Hq,
                          int Hkv, int D, int kv_rows, da_dtype dt, da_layout lay, float scale, int S,
-                         void* ws, cudaStream_t st) {
+                         void* ws, void* out, cudaStream_t st) {
     if (D == 128)
-        return dt == DA_F16 ? launch_split<128, DA_F16>(q, k, v, cu, B, Hq, Hkv, kv_rows, lay, scale, S, ws, st)
-                            : launch_split<128, DA_BF16>(q, k, v, cu, B, Hq, Hkv, kv_rows, lay, scale, S, ws, st);
-    return dt == DA_F16 ? launch_split<64, DA_F16>(q, k, v, cu, B, Hq, Hkv, kv_rows, lay, scale, S, ws, st)
-                        : launch_split<64, DA_BF16>(q, k, v, cu, B, Hq, Hkv, kv_rows, lay, scale, S, ws, st);
+        return dt == DA_F16 ? launch_split<128, DA_F16>(q, k, v, cu, B, Hq, Hkv, kv_rows, lay, scale, S, ws, out, st)
+                            : launch_split<128, DA_BF16>(q, k, v, cu, B, Hq, Hkv, kv_rows, lay, scale, S, ws, out, st);
+    return dt == DA_F16 ? launch_split<64, DA_F16>(q, k, v, cu, B, Hq, Hkv, kv_rows, lay, scale, S, ws, out, st)
+                        : launch_split<64, DA_BF16>(q, k, v, cu, B, Hq, Hkv, kv_rows, lay, scale, S, ws, out, st);
 }
 
 da_status dispatch_combine(int B, int Hq, int D, int S, da_dtype dt, void* out, const void* ws,
@@ -960,6 +1000,15 @@ da_status dispatch_combine(int B, int Hq, int D, int S, da_dtype dt, void* out, 
                             : launch_combine<128, DA_BF16>(B, Hq, S, out, ws, st);
     return dt == DA_F16 ? launch_combine<64, DA_F16>(B, Hq, S, out, ws, st)
                         : launch_combine<64, DA_BF16>(B, Hq, S, out, ws, st);
+}
+
+// Split step, then the combine step unless a single split already wrote `out`.
+da_status run_decode(const void* q, const void* k, const void* v, const int32_t* cu, int B, int Hq, int Hkv,
+                     int D, int kv_rows, da_dtype dt, da_layout lay, float scale, int S, void* out, void* ws,
+                     cudaStream_t st) {
+    da_status r = dispatch_split(q, k, v, cu, B, Hq, Hkv, D, kv_rows, dt, lay, scale, S, ws, out, st);
+    if (r != DA_OK || S == 1) return r;
+    return dispatch_combine(B, Hq, D, S, dt, out, ws, st);
 }
 
 }  // namespace
@@ -1008,14 +1057,22 @@ int decode_attn_splitkv_num_splits(int B, int Hq, int Hkv, int D, int min_kv, in
             sm_count = 148;
     }
     const int64_t chunks = (Hq / Hkv + kHeadsPerCta - 1) / kHeadsPerCta;
-    const int64_t units = static_cast<int64_t>(B) * Hkv * chunks;
-    const int64_t slots = static_cast<int64_t>(sm_count) * 2;   // work items in flight per wave
-    // Aim for about four items per slot so that unequal splits balance out.
-    int64_t S = (4 * slots + units - 1) / units;
-    // Keep every split at least kMinKeys long (one or more full stages) ...
-    constexpr int64_t kMinKeys = 128;
-    S = std::min<int64_t>(S, std::max<int64_t>(1, min_kv / kMinKeys));
-    // ... never empty, and within the ABI limit.
+    const int64_t units = static_cast<int64_t>(B) * Hkv * chunks;   // (sequence, KV head, chunk)
+    int64_t target, min_len;
+    if (2 * static_cast<int64_t>(min_kv) <= max_kv) {
+        // Ragged lengths: about four items per resident CTA (two per SM), so the
+        // work queue can even out splits of unequal length; splits may be short.
+        target = 8 * static_cast<int64_t>(sm_count);
+        min_len = 64;
+    } else {
+        // Even lengths: about one item per SM, each split long enough (256 to
+        // 1024 keys) that its start-up and merge stay small next to its stream.
+        target = sm_count;
+        min_len = std::min<int64_t>(1024, std::max<int64_t>(256, static_cast<int64_t>(min_kv) * units / sm_count));
+    }
+    int64_t S = (target + units - 1) / units;
+    S = std::min<int64_t>(S, std::max<int64_t>(1, min_kv / min_len));
+    // never an empty split (the TileLang page's num_splits <= min_kv rule)
     S = std::min<int64_t>(S, min_kv);
     S = std::max<int64_t>(1, std::min<int64_t>(S, DA_MAX_SPLITS));
     return static_cast<int>(S);
@@ -1030,7 +1087,7 @@ da_status decode_attn_splitkv_partial(const void* q, const void* k, const void* 
                                 num_splits, workspace, workspace_bytes);
     if (st != DA_OK) return st;
     return dispatch_split(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale,
-                          num_splits, workspace, static_cast<cudaStream_t>(stream));
+                          num_splits, workspace, nullptr, static_cast<cudaStream_t>(stream));
 }
 
 da_status decode_attn_splitkv_combine(int B, int Hq, int D, int num_splits, da_dtype dtype, void* out,
@@ -1056,11 +1113,8 @@ da_status decode_attn_splitkv(const void* q, const void* k, const void* v, const
     if (!out) return DA_ERR_INVALID_ARG;
     if (!aligned(out, 16)) return DA_ERR_ALIGNMENT;
     if (static_cast<int64_t>(B) * Hq * D > 0x7fffffffll) return DA_ERR_INVALID_ARG;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    st = dispatch_split(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale, num_splits,
-                        workspace, s);
-    if (st != DA_OK) return st;
-    return dispatch_combine(B, Hq, D, num_splits, dtype, out, workspace, s);
+    return run_decode(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale, num_splits, out,
+                      workspace, static_cast<cudaStream_t>(stream));
 }
 
 da_status decode_attn_splitkv_get_error(void* workspace, uint32_t* device_error_bits, void* stream) {
@@ -1155,8 +1209,6 @@ extern "C" da_status decode_attn_splitkv_noalloc(const void* q, const void* k, c
     if (!aligned(out, 16)) return DA_ERR_ALIGNMENT;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(ws, 0, kHeaderBytes, s) != cudaSuccess) return DA_ERR_CUDA;
-    st = dispatch_split(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale, num_splits,
-                        ws, s);
-    if (st != DA_OK) return st;
-    return dispatch_combine(B, Hq, D, num_splits, dtype, out, ws, s);
+    return run_decode(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale, num_splits, out, ws,
+                      s);
 }
