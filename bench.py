@@ -47,6 +47,9 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--splits", type=int, default=0, help="override the split-count picker")
+    ap.add_argument("--varsplit", action="store_true",
+                    help="per-sequence split counts (decode_attn_splitkv_varsplit) with its planner")
+    ap.add_argument("--split-len", type=int, default=0, help="override the planner's split_len")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
@@ -271,7 +274,14 @@ def main():
     dev = torch.device("cuda", local)
     stream = torch.cuda.Stream(device=dev)
 
-    S = args.splits or p.num_splits or da.num_splits(p.B, p.Hq, p.Hkv, p.D, min(p.lens), max(p.lens))
+    split_len = 0
+    if args.varsplit:
+        split_len, S = da.varsplit_plan(p.B, p.Hq, p.Hkv, p.D, p.total_kv, max(p.lens))
+        if args.split_len:
+            split_len = args.split_len
+            S = min(da.DA_MAX_SPLITS, -(-max(p.lens) // split_len))
+    else:
+        S = args.splits or p.num_splits or da.num_splits(p.B, p.Hq, p.Hkv, p.D, min(p.lens), max(p.lens))
     hq, hk, hv, hcu = problem_tensors(p, dev)
     q, k, v, cu = hq.to(dev), hk.to(dev), hv.to(dev), hcu.to(dev)
     out = torch.empty(p.B, p.Hq, p.D, dtype=q.dtype, device=dev)
@@ -293,13 +303,19 @@ def main():
         flush()
         if ev0 is not None:
             ev0.record(stream)
-        da.decode_attn_splitkv(q, k, v, cu, out, ws, num_splits=S, scale=p.scale,
-                               layout=p.layout, stream=stream)
+        if split_len:
+            da.decode_attn_splitkv_varsplit(q, k, v, cu, out, ws, split_len=split_len, max_splits=S,
+                                            scale=p.scale, layout=p.layout, stream=stream)
+        else:
+            da.decode_attn_splitkv(q, k, v, cu, out, ws, num_splits=S, scale=p.scale,
+                                   layout=p.layout, stream=stream)
         if ev1 is not None:
             ev1.record(stream)
 
     def split_step(ev0, ev1):
         # the split kernel alone, for its roofline; the combine follows untimed
+        if split_len:
+            return step(ev0, ev1)   # per-sequence mode has no split-only entry point: time the call
         flush()
         ev0.record(stream)
         da.decode_attn_splitkv_partial(q, k, v, cu, ws, num_splits=S, scale=p.scale,
@@ -352,8 +368,13 @@ def main():
             k.copy_(pk, non_blocking=True)
             v.copy_(pv, non_blocking=True)
             cu.copy_(pcu, non_blocking=True)
-            da.decode_attn_splitkv(q, k, v, cu, out, ws, num_splits=S, scale=p.scale,
-                                   layout=p.layout, stream=stream)
+            if split_len:
+                da.decode_attn_splitkv_varsplit(q, k, v, cu, out, ws, split_len=split_len,
+                                                max_splits=S, scale=p.scale, layout=p.layout,
+                                                stream=stream)
+            else:
+                da.decode_attn_splitkv(q, k, v, cu, out, ws, num_splits=S, scale=p.scale,
+                                       layout=p.layout, stream=stream)
             hout.copy_(out, non_blocking=True)
 
         with torch.cuda.stream(stream):
@@ -391,8 +412,11 @@ def main():
         "pct_of_hbm_peak": round(100.0 * value / world / peak, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": p.dtype, "data": "synthetic (seeded N(0,1), rounded to the input dtype)",
-        "config": workload_config(p, S),
-        "roofline": {"kernel": "split_kernel", "bound": "hbm", "achieved": round(achieved, 2),
+        "config": {**workload_config(p, S),
+                   **({"split_mode": "per-sequence", "split_len": split_len, "max_splits": S}
+                      if split_len else {"split_mode": "uniform"})},
+        "roofline": {"kernel": "split_kernel" if not split_len else "split_kernel+combine_kernel",
+                     "bound": "hbm", "achieved": round(achieved, 2),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
@@ -401,7 +425,8 @@ def main():
                      "launches_timed": k_split,
                      "combine_us_mean_derived": round((mean_step_ms - split_mean_ms) * 1e3, 2)},
         "e2e": e2e,
-        "gpu_launches": (1 if S == 1 else 2) * args.steps + 2 * k_split,
+        "gpu_launches": ((1 if S == 1 and not split_len else 2) * args.steps
+                         + (2 * k_split)),
         "wall_s_timed_region": round(t_wall, 3),
     }
     if sampler:

@@ -169,6 +169,45 @@ da_status decode_attn_splitkv_combine(int B, int Hq, int D, int num_splits, da_d
                                       void* out, const void* workspace, size_t workspace_bytes,
                                       void* stream);
 
+/* Largest batch accepted by decode_attn_splitkv_varsplit. */
+#define DA_MAX_VARSPLIT_BATCH 1024
+
+/*
+ * Per-sequence split counts, for ragged batches. Instead of one num_splits
+ * for every sequence, sequence b is cut into
+ *
+ *     S_b = 1 if L_b = 0, else min(max_splits, ceil(L_b / split_len))
+ *
+ * proportional splits [floor(L_b*s/S_b), floor(L_b*(s+1)/S_b)), so that work
+ * items are about split_len keys long whatever the sequence length, and the
+ * work queue balances them. The pages motivate it without specifying it: the
+ * TileLang page notes that real frameworks choose the split count in their
+ * scheduler (split kernel docstring) and the lecture page that real
+ * implementations pick splits from batch, length and SM count
+ * (04_flash_decoding.py, demo4_splits observations). No split is ever empty.
+ *   split_len      >= 1 keys per split (target); max_splits in [1, DA_MAX_SPLITS]
+ *   B              <= DA_MAX_VARSPLIT_BATCH (else DA_ERR_UNSUPPORTED)
+ *   workspace      >= decode_attn_splitkv_workspace_size(B, Hq, D, max_splits);
+ *                  lse_part/o_part use max_splits as the split stride, and
+ *                  entries s >= S_b of a row are left untouched
+ * Other arguments, results and errors as decode_attn_splitkv.
+ */
+da_status decode_attn_splitkv_varsplit(const void* q, const void* k, const void* v,
+                                       const int32_t* cu_seqlens_k, int B, int Hq, int Hkv,
+                                       int D, int kv_rows, da_dtype dtype, da_layout layout,
+                                       float scale, int split_len, int max_splits, void* out,
+                                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Picker for decode_attn_splitkv_varsplit (host only): from the batch's
+ * total and longest KV length, a split_len (a multiple of 64 keys, at least
+ * 256) that gives about eight work items per SM, and the max_splits that the
+ * longest sequence needs. sm_count 0 means: query the current device.
+ * Returns 0, or -1 (and 1, 1) if an argument is out of range.
+ */
+int decode_attn_splitkv_varsplit_plan(int B, int Hq, int Hkv, int D, int64_t total_kv, int max_kv,
+                                      int sm_count, int* split_len, int* max_splits);
+
 /*
  * Read and clear the device error word of `workspace` (DA_DEVERR_* bits).
  * Synchronises `stream` first. Errors: DA_ERR_INVALID_ARG, DA_ERR_CUDA.

@@ -57,6 +57,8 @@ def load_library(path: str):
     lib.oracle_attention_rows.restype = ctypes.c_int
     lib.oracle_split_partials.argtypes = _PROBLEM_ARGS + [_I32, _P, _P, ctypes.c_int]
     lib.oracle_split_partials.restype = ctypes.c_int
+    lib.oracle_split_partials_var.argtypes = _PROBLEM_ARGS + [_I32, _I32, _P, _P, _P, ctypes.c_int]
+    lib.oracle_split_partials_var.restype = ctypes.c_int
     lib.oracle_merge.argtypes = [_P, _P, _I64, _I32, _I32, _P, _P]
     lib.oracle_merge.restype = ctypes.c_int
     lib.oracle_weights.argtypes = _PROBLEM_ARGS + [_I32, _I32, _P]
@@ -139,6 +141,18 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle_split_partials: inconsistent problem")
         return o, lse
+
+    def split_partials_var(self, p, split_len: int, max_splits: int, nthreads: int = 0):
+        """Per-sequence split counts: (o_part[B,Hq,max_splits,D], lse_part[B,Hq,max_splits], S_b[B])."""
+        keep, args = self._args(p)
+        o = np.empty((p.B, p.Hq, max_splits, p.D), dtype=np.float64)
+        lse = np.empty((p.B, p.Hq, max_splits), dtype=np.float64)
+        sc = np.empty(p.B, dtype=np.int32)
+        rc = self.lib.oracle_split_partials_var(*args, split_len, max_splits, o.ctypes.data,
+                                                lse.ctypes.data, sc.ctypes.data, _threads(nthreads))
+        if rc != 0:
+            raise ValueError("oracle_split_partials_var: inconsistent problem")
+        return o, lse, sc
 
     def merge(self, o_part, lse_part):
         """Exact log-sum-exp combine: (out[..., D], lse[...])."""

@@ -21,6 +21,7 @@ DA_LAYOUT_VARLEN, DA_LAYOUT_BHSD = 0, 1
 DA_DEVERR_SEQLENS, DA_DEVERR_TIMEOUT = 0x1, 0x2
 DA_MAX_SPLITS = 1024
 DA_NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
+DA_MAX_VARSPLIT_BATCH = 1024
 
 EXPORTED = [
     "decode_attn_splitkv_workspace_size", "decode_attn_splitkv_lse_offset",
@@ -28,7 +29,8 @@ EXPORTED = [
     "decode_attn_splitkv_num_splits", "decode_attn_splitkv_split_range", "decode_attn_splitkv",
     "decode_attn_splitkv_partial", "decode_attn_splitkv_combine", "decode_attn_splitkv_get_error",
     "decode_attn_splitkv_selftest_timeout", "decode_attn_splitkv_status_string",
-    "decode_attn_splitkv_noalloc",
+    "decode_attn_splitkv_noalloc", "decode_attn_splitkv_varsplit",
+    "decode_attn_splitkv_varsplit_plan",
 ]
 
 _lib = None
@@ -75,6 +77,11 @@ def load(path: str = LIB):
     lib.decode_attn_splitkv_selftest_timeout.restype = I
     lib.decode_attn_splitkv_noalloc.argtypes = [P, P, P, P, I, I, I, I, I, I, I, F, I, P, P]
     lib.decode_attn_splitkv_noalloc.restype = I
+    lib.decode_attn_splitkv_varsplit.argtypes = [P, P, P, P, I, I, I, I, I, I, I, F, I, I, P, P, SZ, P]
+    lib.decode_attn_splitkv_varsplit.restype = I
+    lib.decode_attn_splitkv_varsplit_plan.argtypes = [I, I, I, I, I64, I, I, ctypes.POINTER(I),
+                                                      ctypes.POINTER(I)]
+    lib.decode_attn_splitkv_varsplit_plan.restype = I
     lib.decode_attn_splitkv_status_string.argtypes = [I]
     lib.decode_attn_splitkv_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -168,6 +175,31 @@ def decode_attn_splitkv(q, k, v, cu_seqlens_k, out, workspace, *, num_splits: in
         _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_k), B, Hq, Hkv, D, kv_rows, _dtype_code(q),
         layout, sc, num_splits, _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
     _check(st, "decode_attn_splitkv")
+    return out
+
+
+def varsplit_plan(B: int, Hq: int, Hkv: int, D: int, total_kv: int, max_kv: int,
+                  sm_count: int = 0) -> tuple:
+    """(split_len, max_splits) for decode_attn_splitkv_varsplit."""
+    a, b = ctypes.c_int(), ctypes.c_int()
+    rc = load().decode_attn_splitkv_varsplit_plan(B, Hq, Hkv, D, total_kv, max_kv, sm_count,
+                                                  ctypes.byref(a), ctypes.byref(b))
+    if rc != 0:
+        raise ValueError("decode_attn_splitkv_varsplit_plan rejected its arguments")
+    return a.value, b.value
+
+
+def decode_attn_splitkv_varsplit(q, k, v, cu_seqlens_k, out, workspace, *, split_len: int,
+                                 max_splits: int, scale: float | None = None,
+                                 layout: int = DA_LAYOUT_VARLEN, stream=None):
+    """Per-sequence split counts S_b = min(max_splits, ceil(L_b / split_len)); see the C header."""
+    B, Hq, Hkv, D, kv_rows = _shape_args(q, k, cu_seqlens_k, layout)
+    sc = 1.0 / math.sqrt(D) if scale is None else scale
+    st = load().decode_attn_splitkv_varsplit(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_k), B, Hq, Hkv, D, kv_rows, _dtype_code(q),
+        layout, sc, split_len, max_splits, _ptr(out), _ptr(workspace), workspace.numel(),
+        _stream(stream))
+    _check(st, "decode_attn_splitkv_varsplit")
     return out
 
 

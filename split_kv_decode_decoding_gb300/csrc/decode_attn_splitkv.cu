@@ -117,6 +117,7 @@ struct SplitParams {
     uint32_t* done;          // CTAs finished
     uint16_t* out;           // [B, Hq, D] when S == 1 (o_0 is the output), else nullptr
     int B, Hq, Hkv, G, S, kv_rows, layout, chunks, no_kv, n_items;
+    int split_len;           // 0: every sequence has S splits; else S_b = min(S, ceil(L_b / split_len))
     float scale_log2;        // scale * log2(e)
     unsigned long long wait_limit_ns;
 };
@@ -282,31 +283,68 @@ __device__ __forceinline__ int ld_cg_s32(const int32_t* p) {
 
 __device__ __forceinline__ void flag_error(uint32_t* err, uint32_t bits) { atomicOr(err, bits); }
 
-// Decode work item `idx` into its descriptor (reads cu_seqlens_k). Flags a
-// sequence whose range cannot be read safely and treats it as empty.
-__device__ __forceinline__ ItemSlot decode_item(const SplitParams& p, int idx) {
+// Length of sequence b, validated against the K/V extent: a range that cannot
+// be read safely counts as empty (and *bad is set).
+__device__ __forceinline__ int64_t checked_len(const int32_t* cu, int b, int layout, int kv_rows, int no_kv,
+                                               int64_t* base, bool* bad) {
+    const int64_t c0 = ld_cg_s32(cu + b), c1 = ld_cg_s32(cu + b + 1);
+    const int64_t L = c1 - c0;
+    bool ok = L >= 0;
+    if (layout == DA_LAYOUT_VARLEN) ok = ok && c0 >= 0 && c1 <= kv_rows;
+    else ok = ok && L <= kv_rows;
+    if (no_kv) ok = ok && L == 0;
+    *base = layout == DA_LAYOUT_VARLEN ? c0 : 0;
+    *bad = !ok;
+    return ok ? L : 0;
+}
+
+// Split count of a sequence of length L (per-sequence mode): 1 for an empty
+// sequence, else ceil(L / split_len) capped at max_splits; never an empty split.
+__device__ __forceinline__ int seq_splits(int64_t L, int split_len, int max_splits) {
+    if (L == 0) return 1;
+    const int64_t sb = (L + split_len - 1) / split_len;
+    return static_cast<int>(sb < max_splits ? sb : max_splits);
+}
+
+// Decode work item `idx` into its descriptor (reads cu_seqlens_k). Items run
+// split-fastest, then (KV head, head chunk), then sequence. With per-sequence
+// split counts, `prefix` holds the running sum of S_b (prefix[b] splits before
+// sequence b) and the sequence is found by binary search.
+__device__ __forceinline__ ItemSlot decode_item(const SplitParams& p, int idx, const int32_t* prefix) {
     ItemSlot it;
-    int r = idx;
-    it.s = r % p.S;
-    r /= p.S;
-    const int chunk = r % p.chunks;
-    r /= p.chunks;
-    it.kvh = r % p.Hkv;
-    it.b = r / p.Hkv;
+    int chunk, Sb;
+    const int hc_count = p.Hkv * p.chunks;
+    if (p.split_len == 0) {
+        int r = idx;
+        it.s = r % p.S;
+        r /= p.S;
+        chunk = r % p.chunks;
+        r /= p.chunks;
+        it.kvh = r % p.Hkv;
+        it.b = r / p.Hkv;
+        Sb = p.S;
+    } else {
+        int lo = 0, hi = p.B - 1;   // last b with prefix[b] * hc_count <= idx
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (static_cast<int64_t>(prefix[mid]) * hc_count <= idx) lo = mid;
+            else hi = mid - 1;
+        }
+        it.b = lo;
+        Sb = prefix[lo + 1] - prefix[lo];
+        const int r = idx - prefix[lo] * hc_count;
+        it.s = r % Sb;
+        const int hc = r / Sb;
+        chunk = hc % p.chunks;
+        it.kvh = hc / p.chunks;
+    }
     it.h0 = it.kvh * p.G + chunk * kHeadsPerCta;
     it.nh = min(kHeadsPerCta, p.G - chunk * kHeadsPerCta);
-    const int64_t c0 = ld_cg_s32(p.cu + it.b), c1 = ld_cg_s32(p.cu + it.b + 1);
-    int64_t L = c1 - c0;
-    const int64_t base = p.layout == DA_LAYOUT_VARLEN ? c0 : 0;
-    bool ok = L >= 0;
-    if (p.layout == DA_LAYOUT_VARLEN) ok = ok && c0 >= 0 && c1 <= p.kv_rows;
-    else ok = ok && L <= p.kv_rows;
-    if (p.no_kv) ok = ok && L == 0;
-    if (!ok) {
-        L = 0;
-        if (it.s == 0 && chunk == 0 && it.kvh == 0) flag_error(p.err, DA_DEVERR_SEQLENS);
-    }
-    const int64_t lo = L * it.s / p.S, hi = L * (it.s + 1) / p.S;
+    int64_t base;
+    bool bad;
+    const int64_t L = checked_len(p.cu, it.b, p.layout, p.kv_rows, p.no_kv, &base, &bad);
+    if (bad && it.s == 0 && chunk == 0 && it.kvh == 0) flag_error(p.err, DA_DEVERR_SEQLENS);
+    const int64_t lo = L * it.s / Sb, hi = L * (it.s + 1) / Sb;
     it.nkeys = static_cast<int>(hi - lo);
     it.ntiles = (it.nkeys + kStageKeys - 1) / kStageKeys;
     it.first_key = base + lo;
@@ -333,6 +371,7 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
     const uint32_t ifull0 = empty0 + 8 * kStages;       // [kItemSlots]
     const uint32_t iempty0 = ifull0 + 8 * kItemSlots;   // [kItemSlots]
     const uint32_t mfull = iempty0 + 8 * kItemSlots;    // an item's per-warp partials written
+    int32_t* prefix = reinterpret_cast<int32_t*>(smem + Sh::kEnd);   // [B + 1], per-sequence mode only
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -362,6 +401,31 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
 
     if (warp == kConsumerWarps) {
         // ---------------- producer: one lane takes items and issues every copy
+        int n_items = p.n_items;
+        if (p.split_len != 0) {
+            // per-sequence split counts: the whole warp builds prefix[] = running sum of S_b
+            int carry = 0;
+            for (int b0 = 0; b0 < p.B; b0 += 32) {
+                const int b = b0 + lane;
+                int sb = 0;
+                if (b < p.B) {
+                    int64_t base;
+                    bool bad;
+                    sb = seq_splits(checked_len(p.cu, b, p.layout, p.kv_rows, p.no_kv, &base, &bad), p.split_len,
+                                    p.S);
+                }
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, sb, off);
+                    if (lane >= off) sb += y;
+                }
+                if (b < p.B) prefix[b + 1] = carry + sb;
+                carry += __shfl_sync(0xffffffffu, sb, 31);
+            }
+            if (lane == 0) prefix[0] = 0;
+            __syncwarp();
+            n_items = carry * p.Hkv * p.chunks;
+        }
         if (lane == 0) {
             int st = 0;          // ring position of the next tile
             uint32_t ph = 0;     // its phase parity
@@ -375,12 +439,12 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
                 // the first item of each CTA is its own index; later ones come from the queue
                 const int idx = it == 0 ? static_cast<int>(blockIdx.x)
                                         : static_cast<int>(gridDim.x + atomicAdd(p.work, 1u));
-                if (idx >= p.n_items) {
+                if (idx >= n_items) {
                     slots[slot].valid = 0;
                     mbar_arrive(ifull0 + 8 * slot);
                     break;
                 }
-                const ItemSlot item = decode_item(p, idx);
+                const ItemSlot item = decode_item(p, idx, prefix);
                 slots[slot] = item;
                 const uint32_t ib = ifull0 + 8 * slot;
                 mbar_arrive_expect_tx(ib, item.nh * D * 2);
@@ -710,29 +774,42 @@ __device__ __forceinline__ void combine_fold(float lv, float4 ov, float& m, floa
 // lane owns four dims of one split at a time; 32 / (DC / 4) splits are read per
 // iteration, four iterations' loads are issued together, and the lanes' partial
 // states are merged with shuffles at the end (a fixed order: deterministic).
+struct CombineParams {
+    const float* lse;        // [rows, S]
+    const float* opart;      // [rows, S, D]
+    uint16_t* out;           // [rows, D]
+    const int32_t* cu;       // per-sequence mode: row r's split count comes from sequence r / Hq
+    int rows, S, dchunks, Hq, split_len, layout, kv_rows, no_kv;
+};
+
 template <int D, int DT>
-__global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ lse,
-                                                      const float* __restrict__ opart,
-                                                      uint16_t* __restrict__ out, int rows, int S,
-                                                      int dchunks) {
+__global__ void __launch_bounds__(128) combine_kernel(const CombineParams cp) {
     grid_dependency_wait();
     if (threadIdx.x == 0) grid_dependents_launch();
     const int warp_id = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    if (warp_id >= rows * dchunks) return;
+    if (warp_id >= cp.rows * cp.dchunks) return;
+    const int dchunks = cp.dchunks, S = cp.S;
     const int row = warp_id / dchunks, dc = warp_id % dchunks;
+    int Srow = S;   // splits present in this row
+    if (cp.split_len != 0) {
+        int64_t base;
+        bool bad;
+        Srow = seq_splits(checked_len(cp.cu, row / cp.Hq, cp.layout, cp.kv_rows, cp.no_kv, &base, &bad),
+                          cp.split_len, S);
+    }
     const int DC = D / dchunks;
     const int lps = DC / 4;               // lanes per split row
     const int spi = 32 / lps;             // splits per iteration
     const int sub = lane / lps, dv = lane % lps;
     const int d0 = dc * DC + dv * 4;
-    const float* l = lse + static_cast<int64_t>(row) * S;
-    const float* po = opart + static_cast<int64_t>(row) * S * D + d0;
+    const float* l = cp.lse + static_cast<int64_t>(row) * S;
+    const float* po = cp.opart + static_cast<int64_t>(row) * S * D + d0;
 
     float m = -INFINITY, z = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     int s = sub;
-    for (; s + 3 * spi < S; s += 4 * spi) {
+    for (; s + 3 * spi < Srow; s += 4 * spi) {
         float lv[4];
         float4 ov[4];
 #pragma unroll
@@ -743,7 +820,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
 #pragma unroll
         for (int u = 0; u < 4; ++u) combine_fold(lv[u], ov[u], m, z, acc);
     }
-    for (; s < S; s += spi)
+    for (; s < Srow; s += spi)
         combine_fold(__ldcg(l + s), __ldcg(reinterpret_cast<const float4*>(po + static_cast<int64_t>(s) * D)), m,
                      z, acc);
     // merge the lanes that hold the same dims
@@ -768,7 +845,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
         }
     }
     if (sub == 0) {
-        uint16_t* o = out + static_cast<int64_t>(row) * D + d0;
+        uint16_t* o = cp.out + static_cast<int64_t>(row) * D + d0;
         if (m == -INFINITY) {
             *reinterpret_cast<uint2*>(o) = make_uint2(0u, 0u);
         } else {
@@ -894,52 +971,69 @@ cudaLaunchAttribute pdl_attr() {
     return a;
 }
 
+// One decode call's arguments, after the host checks.
+struct Call {
+    const void *q, *k, *v;
+    const int32_t* cu;
+    int B, Hq, Hkv, D, kv_rows;
+    da_dtype dt;
+    da_layout lay;
+    float scale;
+    int S;           // splits per sequence, or the cap of S_b in per-sequence mode
+    int split_len;   // 0: S splits for every sequence; else per-sequence S_b
+    void* ws;
+};
+
+constexpr int kMaxVarsplitBatch = 1024;                                   // sequences, per-sequence mode
+constexpr int kPrefixBytes = ((kMaxVarsplitBatch + 1) * 4 + 15) / 16 * 16;  // its prefix[] in shared memory
+
+// `out` is written by the split kernel itself only with one uniform split.
 template <int D, int DT>
-da_status launch_split(const void* q, const void* k, const void* v, const int32_t* cu, int B, int Hq,
-                       int Hkv, int kv_rows, da_layout lay, float scale, int S, void* ws, void* out,
-                       cudaStream_t stream) {
+da_status launch_split(const Call& c, void* out, cudaStream_t stream) {
     // 64-key boxes for full stages, 16-key boxes for the ragged end of a split
     alignas(64) CUtensorMap mk, mv, mk16, mv16;
     std::memset(&mk, 0, sizeof(mk));
     std::memset(&mv, 0, sizeof(mv));
     std::memset(&mk16, 0, sizeof(mk16));
     std::memset(&mv16, 0, sizeof(mv16));
-    if (kv_rows > 0) {
+    if (c.kv_rows > 0) {
         const da_dtype dt = static_cast<da_dtype>(DT);
-        if (!make_kv_map(&mk, k, dt, lay, B, Hkv, D, kv_rows, kStageKeys) ||
-            !make_kv_map(&mv, v, dt, lay, B, Hkv, D, kv_rows, kStageKeys) ||
-            !make_kv_map(&mk16, k, dt, lay, B, Hkv, D, kv_rows, kBoxKeys) ||
-            !make_kv_map(&mv16, v, dt, lay, B, Hkv, D, kv_rows, kBoxKeys))
+        if (!make_kv_map(&mk, c.k, dt, c.lay, c.B, c.Hkv, D, c.kv_rows, kStageKeys) ||
+            !make_kv_map(&mv, c.v, dt, c.lay, c.B, c.Hkv, D, c.kv_rows, kStageKeys) ||
+            !make_kv_map(&mk16, c.k, dt, c.lay, c.B, c.Hkv, D, c.kv_rows, kBoxKeys) ||
+            !make_kv_map(&mv16, c.v, dt, c.lay, c.B, c.Hkv, D, c.kv_rows, kBoxKeys))
             return DA_ERR_CUDA;
     }
     SplitParams p;
-    uint8_t* wsb = static_cast<uint8_t*>(ws);
-    p.q = static_cast<const uint16_t*>(q);
-    p.cu = cu;
+    uint8_t* wsb = static_cast<uint8_t*>(c.ws);
+    p.q = static_cast<const uint16_t*>(c.q);
+    p.cu = c.cu;
     p.err = reinterpret_cast<uint32_t*>(wsb);
     p.work = reinterpret_cast<uint32_t*>(wsb + kWorkCounterOff);
     p.done = reinterpret_cast<uint32_t*>(wsb + kDoneCounterOff);
-    p.out = S == 1 ? static_cast<uint16_t*>(out) : nullptr;
+    p.out = (c.S == 1 && c.split_len == 0) ? static_cast<uint16_t*>(out) : nullptr;
     p.lse = reinterpret_cast<float*>(wsb + decode_attn_splitkv_lse_offset());
-    p.opart = reinterpret_cast<float*>(wsb + decode_attn_splitkv_opart_offset(B, Hq, S));
-    p.B = B;
-    p.Hq = Hq;
-    p.Hkv = Hkv;
-    p.G = Hq / Hkv;
-    p.S = S;
-    p.kv_rows = kv_rows;
-    p.layout = lay;
+    p.opart = reinterpret_cast<float*>(wsb + decode_attn_splitkv_opart_offset(c.B, c.Hq, c.S));
+    p.B = c.B;
+    p.Hq = c.Hq;
+    p.Hkv = c.Hkv;
+    p.G = c.Hq / c.Hkv;
+    p.S = c.S;
+    p.kv_rows = c.kv_rows;
+    p.layout = c.lay;
     p.chunks = (p.G + kHeadsPerCta - 1) / kHeadsPerCta;
-    p.no_kv = kv_rows == 0;
-    p.n_items = B * Hkv * p.chunks * S;
-    p.scale_log2 = scale * kLog2e;
+    p.no_kv = c.kv_rows == 0;
+    p.n_items = c.B * c.Hkv * p.chunks * c.S;   // per-sequence mode: an upper bound (the kernel counts)
+    p.split_len = c.split_len;
+    p.scale_log2 = c.scale * kLog2e;
     p.wait_limit_ns = kWaitLimitNs;
 
-    const int smem = Shape<D>::kSmemBytes;
+    const bool var = c.split_len != 0;
+    const int smem = Shape<D>::kSmemBytes + (var ? kPrefixBytes : 0);
     auto kern = split_kernel<D, DT>;
-    static DeviceCache cache;
+    static DeviceCache cache_uniform, cache_var;
     int grid = 0;
-    if (persistent_grid(kern, smem, cache, &grid) != cudaSuccess) return DA_ERR_CUDA;
+    if (persistent_grid(kern, smem, var ? cache_var : cache_uniform, &grid) != cudaSuccess) return DA_ERR_CUDA;
     grid = std::min(grid, p.n_items);
     cudaLaunchAttribute attrs[1] = {pdl_attr()};
     cudaLaunchConfig_t cfg = {};
@@ -960,14 +1054,22 @@ int combine_dchunks(int rows, int D, int S) {
 }
 
 template <int D, int DT>
-da_status launch_combine(int B, int Hq, int S, void* out, const void* ws, cudaStream_t stream) {
-    const float* lse = reinterpret_cast<const float*>(static_cast<const uint8_t*>(ws) +
-                                                      decode_attn_splitkv_lse_offset());
-    const float* opart = reinterpret_cast<const float*>(static_cast<const uint8_t*>(ws) +
-                                                        decode_attn_splitkv_opart_offset(B, Hq, S));
-    const int rows = B * Hq;
-    const int dchunks = combine_dchunks(rows, D, S);
-    const int64_t warps = static_cast<int64_t>(rows) * dchunks;
+da_status launch_combine(const Call& c, void* out, cudaStream_t stream) {
+    CombineParams cp;
+    const uint8_t* wsb = static_cast<const uint8_t*>(c.ws);
+    cp.lse = reinterpret_cast<const float*>(wsb + decode_attn_splitkv_lse_offset());
+    cp.opart = reinterpret_cast<const float*>(wsb + decode_attn_splitkv_opart_offset(c.B, c.Hq, c.S));
+    cp.out = static_cast<uint16_t*>(out);
+    cp.cu = c.cu;
+    cp.rows = c.B * c.Hq;
+    cp.S = c.S;
+    cp.dchunks = combine_dchunks(cp.rows, D, c.S);
+    cp.Hq = c.Hq;
+    cp.split_len = c.split_len;
+    cp.layout = c.lay;
+    cp.kv_rows = c.kv_rows;
+    cp.no_kv = c.kv_rows == 0;
+    const int64_t warps = static_cast<int64_t>(cp.rows) * cp.dchunks;
     cudaLaunchAttribute attrs[1] = {pdl_attr()};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>((warps + 3) / 4));
@@ -976,39 +1078,47 @@ da_status launch_combine(int B, int Hq, int S, void* out, const void* ws, cudaSt
     cfg.stream = stream;
     cfg.attrs = attrs;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, combine_kernel<D, DT>, lse, opart, static_cast<uint16_t*>(out), rows, S,
-                              dchunks) == cudaSuccess
-               ? DA_OK
-               : DA_ERR_CUDA;
+    return cudaLaunchKernelEx(&cfg, combine_kernel<D, DT>, cp) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
 }
 
-// `out` may be nullptr (split step only); with one split the split kernel writes it.
-da_status dispatch_split(const void* q, const void* k, const void* v, const int32_t* cu, int B, int Hq,
-                         int Hkv, int D, int kv_rows, da_dtype dt, da_layout lay, float scale, int S,
-                         void* ws, void* out, cudaStream_t st) {
-    if (D == 128)
-        return dt == DA_F16 ? launch_split<128, DA_F16>(q, k, v, cu, B, Hq, Hkv, kv_rows, lay, scale, S, ws, out, st)
-                            : launch_split<128, DA_BF16>(q, k, v, cu, B, Hq, Hkv, kv_rows, lay, scale, S, ws, out, st);
-    return dt == DA_F16 ? launch_split<64, DA_F16>(q, k, v, cu, B, Hq, Hkv, kv_rows, lay, scale, S, ws, out, st)
-                        : launch_split<64, DA_BF16>(q, k, v, cu, B, Hq, Hkv, kv_rows, lay, scale, S, ws, out, st);
+da_status dispatch_split(const Call& c, void* out, cudaStream_t st) {
+    if (c.D == 128)
+        return c.dt == DA_F16 ? launch_split<128, DA_F16>(c, out, st) : launch_split<128, DA_BF16>(c, out, st);
+    return c.dt == DA_F16 ? launch_split<64, DA_F16>(c, out, st) : launch_split<64, DA_BF16>(c, out, st);
 }
 
-da_status dispatch_combine(int B, int Hq, int D, int S, da_dtype dt, void* out, const void* ws,
-                           cudaStream_t st) {
-    if (D == 128)
-        return dt == DA_F16 ? launch_combine<128, DA_F16>(B, Hq, S, out, ws, st)
-                            : launch_combine<128, DA_BF16>(B, Hq, S, out, ws, st);
-    return dt == DA_F16 ? launch_combine<64, DA_F16>(B, Hq, S, out, ws, st)
-                        : launch_combine<64, DA_BF16>(B, Hq, S, out, ws, st);
+da_status dispatch_combine(const Call& c, void* out, cudaStream_t st) {
+    if (c.D == 128)
+        return c.dt == DA_F16 ? launch_combine<128, DA_F16>(c, out, st) : launch_combine<128, DA_BF16>(c, out, st);
+    return c.dt == DA_F16 ? launch_combine<64, DA_F16>(c, out, st) : launch_combine<64, DA_BF16>(c, out, st);
 }
 
-// Split step, then the combine step unless a single split already wrote `out`.
-da_status run_decode(const void* q, const void* k, const void* v, const int32_t* cu, int B, int Hq, int Hkv,
-                     int D, int kv_rows, da_dtype dt, da_layout lay, float scale, int S, void* out, void* ws,
-                     cudaStream_t st) {
-    da_status r = dispatch_split(q, k, v, cu, B, Hq, Hkv, D, kv_rows, dt, lay, scale, S, ws, out, st);
-    if (r != DA_OK || S == 1) return r;
-    return dispatch_combine(B, Hq, D, S, dt, out, ws, st);
+// Split step, then the combine step unless a single uniform split already wrote `out`.
+da_status run_decode(const Call& c, void* out, cudaStream_t st) {
+    da_status r = dispatch_split(c, out, st);
+    if (r != DA_OK || (c.S == 1 && c.split_len == 0)) return r;
+    return dispatch_combine(c, out, st);
+}
+
+Call make_call(const void* q, const void* k, const void* v, const int32_t* cu, int B, int Hq, int Hkv, int D,
+               int kv_rows, da_dtype dt, da_layout lay, float scale, int S, int split_len, void* ws) {
+    Call c;
+    c.q = q;
+    c.k = k;
+    c.v = v;
+    c.cu = cu;
+    c.B = B;
+    c.Hq = Hq;
+    c.Hkv = Hkv;
+    c.D = D;
+    c.kv_rows = kv_rows;
+    c.dt = dt;
+    c.lay = lay;
+    c.scale = scale;
+    c.S = S;
+    c.split_len = split_len;
+    c.ws = ws;
+    return c;
 }
 
 }  // namespace
@@ -1086,8 +1196,9 @@ da_status decode_attn_splitkv_partial(const void* q, const void* k, const void* 
     da_status st = check_common(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale,
                                 num_splits, workspace, workspace_bytes);
     if (st != DA_OK) return st;
-    return dispatch_split(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale,
-                          num_splits, workspace, nullptr, static_cast<cudaStream_t>(stream));
+    return dispatch_split(make_call(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale,
+                                    num_splits, 0, workspace),
+                          nullptr, static_cast<cudaStream_t>(stream));
 }
 
 da_status decode_attn_splitkv_combine(int B, int Hq, int D, int num_splits, da_dtype dtype, void* out,
@@ -1100,7 +1211,9 @@ da_status decode_attn_splitkv_combine(int B, int Hq, int D, int num_splits, da_d
     if (workspace_bytes < decode_attn_splitkv_workspace_size(B, Hq, D, num_splits))
         return DA_ERR_WORKSPACE_TOO_SMALL;
     if (static_cast<int64_t>(B) * Hq * D > 0x7fffffffll) return DA_ERR_INVALID_ARG;
-    return dispatch_combine(B, Hq, D, num_splits, dtype, out, workspace, static_cast<cudaStream_t>(stream));
+    return dispatch_combine(make_call(nullptr, nullptr, nullptr, nullptr, B, Hq, 1, D, 0, dtype,
+                                      DA_LAYOUT_VARLEN, 1.f, num_splits, 0, const_cast<void*>(workspace)),
+                            out, static_cast<cudaStream_t>(stream));
 }
 
 da_status decode_attn_splitkv(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_k,
@@ -1113,8 +1226,52 @@ da_status decode_attn_splitkv(const void* q, const void* k, const void* v, const
     if (!out) return DA_ERR_INVALID_ARG;
     if (!aligned(out, 16)) return DA_ERR_ALIGNMENT;
     if (static_cast<int64_t>(B) * Hq * D > 0x7fffffffll) return DA_ERR_INVALID_ARG;
-    return run_decode(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale, num_splits, out,
-                      workspace, static_cast<cudaStream_t>(stream));
+    return run_decode(make_call(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale, num_splits, 0,
+                                workspace),
+                      out, static_cast<cudaStream_t>(stream));
+}
+
+int decode_attn_splitkv_varsplit_plan(int B, int Hq, int Hkv, int D, int64_t total_kv, int max_kv,
+                                      int sm_count, int* split_len, int* max_splits) {
+    if (!split_len || !max_splits) return -1;
+    *split_len = 1;
+    *max_splits = 1;
+    if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || (D != 64 && D != 128) || total_kv < 0 || max_kv < 0)
+        return -1;
+    if (sm_count <= 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            sm_count <= 0)
+            sm_count = 148;
+    }
+    const int64_t chunks = (Hq / Hkv + kHeadsPerCta - 1) / kHeadsPerCta;
+    const int64_t key_units = total_kv * Hkv * chunks;      // keys to stream, summed over (KV head, chunk)
+    const int64_t target = 8 * static_cast<int64_t>(sm_count);   // about four items per resident CTA
+    int64_t len = (key_units + target - 1) / std::max<int64_t>(1, target);
+    len = std::max<int64_t>(256, (len + kStageKeys - 1) / kStageKeys * kStageKeys);   // whole stages
+    int64_t ms = max_kv > 0 ? (max_kv + len - 1) / len : 1;
+    ms = std::max<int64_t>(1, std::min<int64_t>(ms, DA_MAX_SPLITS));
+    *split_len = static_cast<int>(std::min<int64_t>(len, 1 << 30));
+    *max_splits = static_cast<int>(ms);
+    return 0;
+}
+
+da_status decode_attn_splitkv_varsplit(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_k,
+                                       int B, int Hq, int Hkv, int D, int kv_rows, da_dtype dtype,
+                                       da_layout layout, float scale, int split_len, int max_splits, void* out,
+                                       void* workspace, size_t workspace_bytes, void* stream) {
+    if (split_len < 1) return DA_ERR_INVALID_ARG;
+    if (B > kMaxVarsplitBatch) return DA_ERR_UNSUPPORTED;
+    da_status st = check_common(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale, max_splits,
+                                workspace, workspace_bytes);
+    if (st != DA_OK) return st;
+    if (!out) return DA_ERR_INVALID_ARG;
+    if (!aligned(out, 16)) return DA_ERR_ALIGNMENT;
+    if (static_cast<int64_t>(B) * Hq * D > 0x7fffffffll) return DA_ERR_INVALID_ARG;
+    return run_decode(make_call(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale, max_splits,
+                                split_len, workspace),
+                      out, static_cast<cudaStream_t>(stream));
 }
 
 da_status decode_attn_splitkv_get_error(void* workspace, uint32_t* device_error_bits, void* stream) {
@@ -1209,6 +1366,7 @@ extern "C" da_status decode_attn_splitkv_noalloc(const void* q, const void* k, c
     if (!aligned(out, 16)) return DA_ERR_ALIGNMENT;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(ws, 0, kHeaderBytes, s) != cudaSuccess) return DA_ERR_CUDA;
-    return run_decode(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale, num_splits, out, ws,
-                      s);
+    return run_decode(make_call(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale, num_splits, 0,
+                                ws),
+                      out, s);
 }

@@ -121,6 +121,7 @@ def workload(name: str, data: bool = True, seed: int = 0) -> Problem:
     qwen_varlen          B=64, 28 q / 4 kv heads, D=128, lengths uniform on [512, 8192], fp16
     codellama_B{b}_S{s}  16 q / 2 kv heads, D=128, b sequences of length s, fp16
     llama_S{s}_B{b}      32 q / 8 kv heads, D=128, b sequences of length s, bf16
+    llama_skewed         32 q / 8 kv heads, D=128, bf16, one sequence of 131072 and 15 of 512
     """
     if name == "tiny":
         return custom(name, 2, 4, 1, 64, [37, 200], "f16", LAYOUT_VARLEN, 4, seed, data=data)
@@ -134,6 +135,11 @@ def workload(name: str, data: bool = True, seed: int = 0) -> Problem:
         b, s = name[len("codellama_B"):].split("_S")
         return custom(name, int(b), 16, 2, 128, [int(s)] * int(b), "f16", LAYOUT_VARLEN,
                       None, seed, data=data)
+    if name == "llama_skewed":
+        # one long-context sequence in a batch of short ones: the case per-sequence
+        # split counts are for (a uniform count is capped by the shortest sequence)
+        return custom(name, 16, 32, 8, 128, [131072] + [512] * 15, "bf16", LAYOUT_VARLEN, None,
+                      seed, data=data)
     if name.startswith("llama_S"):
         s, b = name[len("llama_S"):].split("_B")
         return custom(name, int(b), 32, 8, 128, [int(s)] * int(b), "bf16", LAYOUT_VARLEN,

@@ -345,10 +345,56 @@ def pin_rows_match_full(o):
     assert np.array_equal(out, full[rb, rh]) and np.array_equal(lse, full_lse[rb, rh])
 
 
+def read_count_golden():
+    rows = []
+    with open(os.path.join(GOLDEN, "split_counts.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            v = [int(x) for x in line.split()]
+            rows.append((v[0], v[1], v[2], v[3], v[4:]))
+    return rows
+
+
+def pin_split_counts_golden(o):
+    """Per-sequence split counts and bounds, pinned by q = 0: lse_s = ln(split length)."""
+    for L, n, m, sb, bounds in read_count_golden():
+        assert len(bounds) == sb + 1
+        p = custom("cnt", 1, 2, 1, 64, [L], "f16", seed=5, q_std=0.0)
+        op, lp, sc = o.split_partials_var(p, n, m)
+        assert sc[0] == sb, (L, n, m)
+        v = _dec(p, p.v)
+        for s_ in range(m):
+            if s_ < sb and bounds[s_ + 1] > bounds[s_]:
+                ln = bounds[s_ + 1] - bounds[s_]
+                assert abs(lp[0, 1, s_] - math.log(ln)) <= 1e-13, (L, n, m, s_)
+                mean = v[bounds[s_]: bounds[s_ + 1], 0, :].mean(axis=0)
+                assert np.abs(op[0, 1, s_] - mean).max() <= 1e-14
+            else:
+                assert lp[0, 1, s_] == -math.inf and not op[0, 1, s_].any()
+
+
+def pin_varsplit_merge_invariance(o):
+    """Per-sequence split counts merge back to the unsplit result (ragged batch, GQA)."""
+    p = custom("vs", 5, 8, 2, 64, [1, 90, 1000, 333, 0], "f16", seed=17)
+    ref, ref_lse = o.attention(p)
+    for n, m in ((16, 64), (100, 4), (64, 1), (7, 200)):
+        op, lp, sc = o.split_partials_var(p, n, m)
+        out, lse = o.merge(op, lp)
+        assert np.abs(out - ref).max() <= 1e-12, (n, m)
+        fin = np.isfinite(ref_lse)
+        assert np.array_equal(fin, np.isfinite(lse))
+        assert np.abs(lse[fin] - ref_lse[fin]).max() <= 1e-12
+        for b, L in enumerate(p.lens):
+            assert sc[b] == (1 if L == 0 else min(m, -(-L // n)))
+
+
 ALL_PINS = [
     pin_f16_decoder, pin_bf16_decoder, pin_split_bounds_golden, pin_split_bounds_partition,
     pin_split_invariance, pin_weights_sum_to_one, pin_single_key, pin_single_key_lse,
     pin_constant_v, pin_gqa_packing, pin_hand_example, pin_q_zero_closed_form,
     pin_one_hot_dominance, pin_library_cross_check, pin_bhsd_matches_varlen,
     pin_empty_splits_and_sequences, pin_threads_deterministic, pin_rows_match_full,
+    pin_split_counts_golden, pin_varsplit_merge_invariance,
 ]

@@ -31,7 +31,7 @@ def header_functions():
 
 def test_exports_every_declared_symbol(lib):
     names = header_functions()
-    assert len(names) == 13
+    assert len(names) == 15
     assert sorted(names) == sorted(da.EXPORTED)
     for n in names:
         assert hasattr(lib, n), n
@@ -161,3 +161,27 @@ def test_binding_refuses_without_library(tmp_path):
             mod.load(str(tmp_path / "missing.so"))
     finally:
         mod._lib = saved
+
+
+def test_varsplit_plan(lib):
+    n, m = da.varsplit_plan(64, 28, 4, 128, 64 * 4352, 8192, 152)
+    assert n % 64 == 0 and n >= 256 and m == -(-8192 // n)
+    # about eight items per SM over the whole batch
+    items = 64 * 4352 * 4 / n
+    assert 8 * 152 * 0.8 <= items <= 8 * 152 * 1.2
+    n, m = da.varsplit_plan(2, 4, 1, 64, 237, 200, 152)
+    assert (n, m) == (256, 1)
+    with pytest.raises(ValueError):
+        da.varsplit_plan(2, 4, 3, 64, 237, 200, 152)
+
+
+def test_varsplit_host_checks(lib):
+    v = ctypes.c_void_p
+    args = lambda **kw: [v(kw.get("q", FAKE)), v(FAKE + 0x100000), v(FAKE + 0x200000), v(FAKE + 0x300000),
+                         kw.get("B", 2), 4, 1, 64, 237, 0, 0, 0.125, kw.get("n", 64), kw.get("m", 4),
+                         v(FAKE + 0x400000), v(FAKE + 0x500000), 1 << 20, None]
+    assert lib.decode_attn_splitkv_varsplit(*args(n=0)) == da.DA_ERR_INVALID_ARG
+    assert lib.decode_attn_splitkv_varsplit(*args(m=0)) == da.DA_ERR_INVALID_ARG
+    assert lib.decode_attn_splitkv_varsplit(*args(m=da.DA_MAX_SPLITS + 1)) == da.DA_ERR_INVALID_ARG
+    assert lib.decode_attn_splitkv_varsplit(*args(B=da.DA_MAX_VARSPLIT_BATCH + 1)) == da.DA_ERR_UNSUPPORTED
+    assert lib.decode_attn_splitkv_varsplit(*args(q=FAKE + 2)) == da.DA_ERR_ALIGNMENT

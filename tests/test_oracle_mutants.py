@@ -30,6 +30,10 @@ MUTANTS = {
     "softmax_not_normalized": ("double pj = s[j] / z;", "double pj = s[j];"),
     "max_not_subtracted": ("s[j] = std::exp(s[j] - m);", "s[j] = std::exp(s[j]);"),
     "q_row_transposed": ("((int64_t)b * p.Hq + h) * p.D", "((int64_t)h * p.B + b) * p.D"),
+    "split_count_floor": ("int64_t sb = L == 0 ? 1 : (L + split_len - 1) / split_len;",
+                          "int64_t sb = L == 0 ? 1 : (L + split_len / 2) / split_len;"),
+    "split_count_cap_off_by_one": ("s_count[b] = (int32_t)(sb < max_splits ? sb : max_splits);",
+                             "s_count[b] = (int32_t)(sb < max_splits ? sb : max_splits - 1);"),
     "merge_skips_last_split": ("for (int s = 0; s < S; ++s) {\n            if (ls[s] == kNegInf) continue;",
                                "for (int s = 0; s + 1 < S; ++s) {\n            if (ls[s] == kNegInf) continue;"),
 }
