@@ -75,7 +75,8 @@ typedef enum {
 
 /* Bits of the device error word (see decode_attn_splitkv_get_error). */
 #define DA_DEVERR_SEQLENS 0x1u /* a sequence's cu_seqlens_k range fell outside K/V; it was treated as empty */
-#define DA_DEVERR_TIMEOUT 0x2u /* a pipeline wait exceeded its time limit; the outputs of that call are invalid */
+#define DA_DEVERR_TIMEOUT 0x2u /* a pipeline wait exceeded its time limit; the outputs of that call are
+                                  invalid and the workspace must be initialised again before reuse */
 
 /* Largest num_splits accepted. */
 #define DA_MAX_SPLITS 1024
@@ -83,7 +84,9 @@ typedef enum {
 /*
  * Workspace layout (all offsets from the workspace base, which must be
  * 256-byte aligned):
- *   [0, 256)            header: uint32 device error word at offset 0, rest reserved
+ *   [0, 256)            header: uint32 device error word at offset 0, the split step's
+ *                       work-queue counters at offsets 64 and 128 (zero between calls:
+ *                       the last CTA of each call re-arms them), rest reserved
  *   [256, 256 + A)      lse_part, float32 [B, Hq, num_splits], natural log of the
  *                       scaled scores, A = round_up(B*Hq*num_splits*4, 256)
  *   [256 + A, total)    o_part, float32 [B, Hq, num_splits, D], normalised per split
@@ -96,8 +99,9 @@ size_t decode_attn_splitkv_lse_offset(void);
 size_t decode_attn_splitkv_opart_offset(int B, int Hq, int num_splits);
 
 /*
- * Zero the workspace header (the device error word). Call once on a freshly
- * allocated workspace before its first use. Enqueued on `stream`.
+ * Zero the workspace header (the device error word and the work-queue
+ * counters). Call once on a freshly allocated workspace before its first use,
+ * and again after a DA_DEVERR_TIMEOUT. Enqueued on `stream`.
  * Errors: DA_ERR_INVALID_ARG (NULL, or fewer than 256 bytes),
  * DA_ERR_ALIGNMENT (not 256-byte aligned), DA_ERR_CUDA.
  */
