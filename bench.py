@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--varsplit", action="store_true",
                     help="per-sequence split counts (decode_attn_splitkv_varsplit) with its planner")
     ap.add_argument("--split-len", type=int, default=0, help="override the planner's split_len")
+    ap.add_argument("--tq", type=int, default=1,
+                    help="query tokens per sequence (decode_attn_splitkv_multiquery when > 1)")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
@@ -245,6 +247,7 @@ def workload_config(p, S):
             "head_dim": p.D, "kv_lens": (p.lens[0] if len(set(p.lens)) == 1 else
                                          f"{min(p.lens)}..{max(p.lens)} (mean {sum(p.lens) / len(p.lens):.0f})"),
             "layout": "bhsd" if p.layout == 1 else "varlen", "in_dtype": p.dtype,
+            "query_tokens": p.tq,
             "num_splits": S, "kv_bytes": p.kv_bytes,
             "l2": "flushed between steps (write then read of 2x L2 size)"}
 
@@ -252,8 +255,14 @@ def workload_config(p, S):
 def main():
     args = parse()
     world, rank, local = dist_env()
-    from synth.workloads import workload
-    p = workload(args.workload)
+    from synth.workloads import materialize, workload
+    if args.tq > 1:
+        p = workload(args.workload, data=False)
+        p.tq = args.tq
+        p.name = f"{p.name}_tq{args.tq}"
+        materialize(p)
+    else:
+        p = workload(args.workload)
 
     if world > 1:
         import torch.distributed as dist
@@ -281,11 +290,23 @@ def main():
             split_len = args.split_len
             S = min(da.DA_MAX_SPLITS, -(-max(p.lens) // split_len))
     else:
-        S = args.splits or p.num_splits or da.num_splits(p.B, p.Hq, p.Hkv, p.D, min(p.lens), max(p.lens))
+        S = args.splits or p.num_splits or da.num_splits(p.B, p.Hq * p.tq, p.Hkv, p.D, min(p.lens),
+                                                          max(p.lens))
     hq, hk, hv, hcu = problem_tensors(p, dev)
     q, k, v, cu = hq.to(dev), hk.to(dev), hv.to(dev), hcu.to(dev)
-    out = torch.empty(p.B, p.Hq, p.D, dtype=q.dtype, device=dev)
-    ws = da.alloc_workspace(p.B, p.Hq, p.D, S, device=dev, stream=stream)
+    out = torch.empty(*p.q.shape, dtype=q.dtype, device=dev)
+    ws = da.alloc_workspace(p.B * p.tq, p.Hq, p.D, S, device=dev, stream=stream)
+
+    def call():
+        if split_len:
+            da.decode_attn_splitkv_varsplit(q, k, v, cu, out, ws, split_len=split_len, max_splits=S,
+                                            scale=p.scale, layout=p.layout, stream=stream)
+        elif p.tq > 1:
+            da.decode_attn_splitkv_multiquery(q, k, v, cu, out, ws, num_splits=S, scale=p.scale,
+                                              layout=p.layout, stream=stream)
+        else:
+            da.decode_attn_splitkv(q, k, v, cu, out, ws, num_splits=S, scale=p.scale,
+                                   layout=p.layout, stream=stream)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     # L2 flush: write one buffer twice the L2 size, then read another one, so the
     # timed kernel starts with none of its inputs cached and no dirty lines to write back
@@ -303,19 +324,14 @@ def main():
         flush()
         if ev0 is not None:
             ev0.record(stream)
-        if split_len:
-            da.decode_attn_splitkv_varsplit(q, k, v, cu, out, ws, split_len=split_len, max_splits=S,
-                                            scale=p.scale, layout=p.layout, stream=stream)
-        else:
-            da.decode_attn_splitkv(q, k, v, cu, out, ws, num_splits=S, scale=p.scale,
-                                   layout=p.layout, stream=stream)
+        call()
         if ev1 is not None:
             ev1.record(stream)
 
     def split_step(ev0, ev1):
         # the split kernel alone, for its roofline; the combine follows untimed
-        if split_len:
-            return step(ev0, ev1)   # per-sequence mode has no split-only entry point: time the call
+        if split_len or p.tq > 1:
+            return step(ev0, ev1)   # these modes have no split-only entry point: time the call
         flush()
         ev0.record(stream)
         da.decode_attn_splitkv_partial(q, k, v, cu, ws, num_splits=S, scale=p.scale,
@@ -368,13 +384,7 @@ def main():
             k.copy_(pk, non_blocking=True)
             v.copy_(pv, non_blocking=True)
             cu.copy_(pcu, non_blocking=True)
-            if split_len:
-                da.decode_attn_splitkv_varsplit(q, k, v, cu, out, ws, split_len=split_len,
-                                                max_splits=S, scale=p.scale, layout=p.layout,
-                                                stream=stream)
-            else:
-                da.decode_attn_splitkv(q, k, v, cu, out, ws, num_splits=S, scale=p.scale,
-                                       layout=p.layout, stream=stream)
+            call()
             hout.copy_(out, non_blocking=True)
 
         with torch.cuda.stream(stream):
@@ -398,9 +408,11 @@ def main():
     if rank != 0:
         return
     peak, peak_kind = measured_peaks()
+    per_call = 1 if (S == 1 and not split_len) else 2          # one split writes the output itself
+    per_split_step = per_call if (split_len or p.tq > 1) else 2
     split_mean_ms = sum(split_ms) / len(split_ms)
-    ws_bytes = p.B * p.Hq * S * (p.D + 1) * 4
-    q_bytes = p.B * p.Hq * p.D * 2
+    ws_bytes = p.B * p.tq * p.Hq * S * (p.D + 1) * 4
+    q_bytes = p.B * p.tq * p.Hq * p.D * 2
     alg_bytes = p.kv_bytes + q_bytes + 4 * (p.B + 1) + ws_bytes
     achieved = alg_bytes / (split_mean_ms * 1e-3) / 1e9
     traffic = recorded_traffic(p.name, S)
@@ -415,7 +427,8 @@ def main():
         "config": {**workload_config(p, S),
                    **({"split_mode": "per-sequence", "split_len": split_len, "max_splits": S}
                       if split_len else {"split_mode": "uniform"})},
-        "roofline": {"kernel": "split_kernel" if not split_len else "split_kernel+combine_kernel",
+        "roofline": {"kernel": ("split_kernel" if not (split_len or p.tq > 1)
+                                else "split_kernel+combine_kernel"),
                      "bound": "hbm", "achieved": round(achieved, 2),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
@@ -425,8 +438,7 @@ def main():
                      "launches_timed": k_split,
                      "combine_us_mean_derived": round((mean_step_ms - split_mean_ms) * 1e3, 2)},
         "e2e": e2e,
-        "gpu_launches": ((1 if S == 1 and not split_len else 2) * args.steps
-                         + (2 * k_split)),
+        "gpu_launches": per_call * args.steps + per_split_step * k_split,
         "wall_s_timed_region": round(t_wall, 3),
     }
     if sampler:

@@ -212,6 +212,34 @@ da_status decode_attn_splitkv_varsplit(const void* q, const void* k, const void*
 int decode_attn_splitkv_varsplit_plan(int B, int Hq, int Hkv, int D, int64_t total_kv, int max_kv,
                                       int sm_count, int* split_len, int* max_splits);
 
+/* Largest T_q accepted by decode_attn_splitkv_multiquery. */
+#define DA_MAX_QUERY_TOKENS 16
+
+/*
+ * Several new query tokens per sequence (speculative or multi-token decoding).
+ * Each sequence has T_q query tokens whose keys and values are already the
+ * last T_q entries of its cache; token t sits at position L_b - T_q + t and
+ * attends causally to keys [0, L_b - T_q + t] (a token that sees no key gets
+ * out = 0). Splits still cut each sequence's whole range [0, L_b) as in
+ * decode_attn_splitkv; a split holding no key a token may see is empty for
+ * that token (lse = -inf, weight 0). The (token, head) pairs of one KV head's
+ * group are packed together into the tensor-core columns, so with
+ * G * T_q <= 8 each K/V byte is still read once. The pages' split kernel has
+ * query blocking only in the official examples it refers to (TileLang page,
+ * module docstring item 1); the masking follows its split segment's -inf rule.
+ *   q, out         device, [B, T_q, Hq, D] elements of `dtype`, 16-byte aligned
+ *   T_q            in [1, DA_MAX_QUERY_TOKENS]
+ *   workspace      >= decode_attn_splitkv_workspace_size(B * T_q, Hq, D, num_splits);
+ *                  rows of lse_part/o_part are (b * T_q + t) * Hq + h
+ * Pick num_splits with decode_attn_splitkv_num_splits(B, Hq * T_q, Hkv, ...).
+ * Other arguments, results and errors as decode_attn_splitkv.
+ */
+da_status decode_attn_splitkv_multiquery(const void* q, const void* k, const void* v,
+                                         const int32_t* cu_seqlens_k, int B, int T_q, int Hq,
+                                         int Hkv, int D, int kv_rows, da_dtype dtype,
+                                         da_layout layout, float scale, int num_splits, void* out,
+                                         void* workspace, size_t workspace_bytes, void* stream);
+
 /*
  * Read and clear the device error word of `workspace` (DA_DEVERR_* bits).
  * Synchronises `stream` first. Errors: DA_ERR_INVALID_ARG, DA_ERR_CUDA.

@@ -59,6 +59,13 @@ def load_library(path: str):
     lib.oracle_split_partials.restype = ctypes.c_int
     lib.oracle_split_partials_var.argtypes = _PROBLEM_ARGS + [_I32, _I32, _P, _P, _P, ctypes.c_int]
     lib.oracle_split_partials_var.restype = ctypes.c_int
+    lib.oracle_attention_mq.argtypes = _PROBLEM_ARGS + [_I32, _P, _P, ctypes.c_int]
+    lib.oracle_attention_mq.restype = ctypes.c_int
+    lib.oracle_attention_rows_mq.argtypes = _PROBLEM_ARGS + [_I32, _P, _P, _P, _I32, _P, _P,
+                                                             ctypes.c_int]
+    lib.oracle_attention_rows_mq.restype = ctypes.c_int
+    lib.oracle_split_partials_mq.argtypes = _PROBLEM_ARGS + [_I32, _I32, _P, _P, ctypes.c_int]
+    lib.oracle_split_partials_mq.restype = ctypes.c_int
     lib.oracle_merge.argtypes = [_P, _P, _I64, _I32, _I32, _P, _P]
     lib.oracle_merge.restype = ctypes.c_int
     lib.oracle_weights.argtypes = _PROBLEM_ARGS + [_I32, _I32, _P]
@@ -153,6 +160,43 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle_split_partials_var: inconsistent problem")
         return o, lse, sc
+
+    # ---- several query tokens per sequence (q, out [B, tq, Hq, D]) ----------
+    def attention_mq(self, p, tq: int, nthreads: int = 0):
+        """Causal multi-token decode: (out[B,tq,Hq,D], lse[B,tq,Hq])."""
+        keep, args = self._args(p)
+        out = np.empty((p.B, tq, p.Hq, p.D), dtype=np.float64)
+        lse = np.empty((p.B, tq, p.Hq), dtype=np.float64)
+        rc = self.lib.oracle_attention_mq(*args, tq, out.ctypes.data, lse.ctypes.data,
+                                          _threads(nthreads))
+        if rc != 0:
+            raise ValueError("oracle_attention_mq: inconsistent problem")
+        return out, lse
+
+    def attention_rows_mq(self, p, tq: int, rows_b, rows_t, rows_h, nthreads: int = 0):
+        keep, args = self._args(p)
+        rb = np.ascontiguousarray(rows_b, dtype=np.int32)
+        rt = np.ascontiguousarray(rows_t, dtype=np.int32)
+        rh = np.ascontiguousarray(rows_h, dtype=np.int32)
+        out = np.empty((rb.size, p.D), dtype=np.float64)
+        lse = np.empty(rb.size, dtype=np.float64)
+        rc = self.lib.oracle_attention_rows_mq(*args, tq, rb.ctypes.data, rt.ctypes.data,
+                                               rh.ctypes.data, rb.size, out.ctypes.data,
+                                               lse.ctypes.data, _threads(nthreads))
+        if rc != 0:
+            raise ValueError("oracle_attention_rows_mq: inconsistent problem")
+        return out, lse
+
+    def split_partials_mq(self, p, tq: int, S: int, nthreads: int = 0):
+        """(o_part[B,tq,Hq,S,D], lse_part[B,tq,Hq,S])."""
+        keep, args = self._args(p)
+        o = np.empty((p.B, tq, p.Hq, S, p.D), dtype=np.float64)
+        lse = np.empty((p.B, tq, p.Hq, S), dtype=np.float64)
+        rc = self.lib.oracle_split_partials_mq(*args, tq, S, o.ctypes.data, lse.ctypes.data,
+                                               _threads(nthreads))
+        if rc != 0:
+            raise ValueError("oracle_split_partials_mq: inconsistent problem")
+        return o, lse
 
     def merge(self, o_part, lse_part):
         """Exact log-sum-exp combine: (out[..., D], lse[...])."""

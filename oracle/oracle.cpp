@@ -29,6 +29,15 @@
 //    convention of the MiniInfer reduce kernel (m = -inf, l = 0 gives the
 //    split weight 0).
 //
+//  * Several new query tokens per sequence (the _mq functions): each sequence
+//    has tq query tokens, stored [B, tq, Hq, D], whose keys and values are
+//    already the last tq rows of its cache. Token t sits at position L - tq + t
+//    and sees the keys before and at it, j < L - tq + t + 1 (causal decoding
+//    of several tokens at once); a token that sees no key gets out = 0. The
+//    splits still cut the whole range [0, L); a split holding no key a token
+//    may see is empty for that token. With tq = 1 every function reduces to
+//    the single-query one above.
+//
 //  * oracle_merge: the exact log-sum-exp combine of the same observation:
 //        lse = ln sum_s exp(lse_s),   o = sum_s exp(lse_s - lse) * o_s,
 //    with the maximum subtracted first, as the TileLang combine segment does.
@@ -57,6 +66,7 @@ struct Problem {
     int32_t dtype;   // 0 binary16, 1 bfloat16
     int32_t layout;  // 0 varlen [kv_rows, Hkv, D]; 1 bhsd [B, Hkv, kv_rows, D]
     double scale;
+    int32_t tq;      // query tokens per sequence, q and out [B, tq, Hq, D]
 };
 
 const double kNegInf = -std::numeric_limits<double>::infinity();
@@ -85,6 +95,12 @@ inline double dec(const Problem& p, uint16_t bits) {
 
 inline int64_t seq_len(const Problem& p, int b) { return (int64_t)p.cu[b + 1] - (int64_t)p.cu[b]; }
 
+// Keys query token t of sequence b may see: [0, L - tq + t + 1), clamped to [0, L].
+inline int64_t visible(const Problem& p, int b, int t) {
+    int64_t v = seq_len(p, b) - p.tq + t + 1;
+    return v < 0 ? 0 : v;
+}
+
 // Element offset of (sequence b, key j, KV head kvh, dim 0).
 inline int64_t kv_offset(const Problem& p, int b, int64_t j, int kvh) {
     if (p.layout == 0) return (((int64_t)p.cu[b] + j) * p.Hkv + kvh) * (int64_t)p.D;
@@ -105,10 +121,10 @@ bool valid(const Problem& p) {
 }
 
 // s_j for one (b, h) over [lo, hi): scale * q . k_j, in double.
-void scores(const Problem& p, int b, int h, int64_t lo, int64_t hi, std::vector<double>& qd,
+void scores(const Problem& p, int b, int t, int h, int64_t lo, int64_t hi, std::vector<double>& qd,
             double* s) {
     int kvh = h / (p.Hq / p.Hkv);
-    const uint16_t* qrow = p.q + ((int64_t)b * p.Hq + h) * p.D;
+    const uint16_t* qrow = p.q + (((int64_t)b * p.tq + t) * p.Hq + h) * p.D;
     qd.resize(p.D);
     for (int d = 0; d < p.D; ++d) qd[d] = dec(p, qrow[d]);
     for (int64_t j = lo; j < hi; ++j) {
@@ -119,9 +135,9 @@ void scores(const Problem& p, int b, int h, int64_t lo, int64_t hi, std::vector<
     }
 }
 
-// The plain definition for one (b, h): out[D] and lse.
-void attend_row(const Problem& p, int b, int h, double* out, double* lse) {
-    int64_t L = seq_len(p, b);
+// The plain definition for one (b, t, h): out[D] and lse.
+void attend_row(const Problem& p, int b, int t, int h, double* out, double* lse) {
+    int64_t L = visible(p, b, t);
     int kvh = h / (p.Hq / p.Hkv);
     for (int d = 0; d < p.D; ++d) out[d] = 0.0;
     if (L == 0) {
@@ -129,7 +145,7 @@ void attend_row(const Problem& p, int b, int h, double* out, double* lse) {
         return;
     }
     std::vector<double> s((size_t)L), qd;
-    scores(p, b, h, 0, L, qd, s.data());
+    scores(p, b, t, h, 0, L, qd, s.data());
     double m = kNegInf;
     for (int64_t j = 0; j < L; ++j) m = s[j] > m ? s[j] : m;
     double z = 0.0;
@@ -150,9 +166,9 @@ void split_bounds(int64_t L, int64_t S, int64_t s, int64_t* lo, int64_t* hi) {
     *hi = L * (s + 1) / S;
 }
 
-// Per-split partials for one (b, h): o_part[S][D], lse[S].
-void split_row(const Problem& p, int b, int h, int S, double* o_part, double* lse) {
-    int64_t L = seq_len(p, b);
+// Per-split partials for one (b, t, h): o_part[S][D], lse[S].
+void split_row(const Problem& p, int b, int t, int h, int S, double* o_part, double* lse) {
+    int64_t L = seq_len(p, b), vis = visible(p, b, t);
     int kvh = h / (p.Hq / p.Hkv);
     std::vector<double> s, qd;
     for (int sp = 0; sp < S; ++sp) {
@@ -160,12 +176,13 @@ void split_row(const Problem& p, int b, int h, int S, double* o_part, double* ls
         for (int d = 0; d < p.D; ++d) o[d] = 0.0;
         int64_t lo, hi;
         split_bounds(L, S, sp, &lo, &hi);
+        if (hi > vis) hi = vis;   // keys this token may not see
         if (hi <= lo) {
             lse[sp] = kNegInf;
             continue;
         }
         s.resize((size_t)(hi - lo));
-        scores(p, b, h, lo, hi, qd, s.data());
+        scores(p, b, t, h, lo, hi, qd, s.data());
         double m = kNegInf;
         for (double x : s) m = x > m ? x : m;
         double z = 0.0;
@@ -214,6 +231,7 @@ Problem make(const void* q, const void* k, const void* v, const int32_t* cu, int
     p.dtype = dtype;
     p.layout = layout;
     p.scale = scale;
+    p.tq = 1;
     return p;
 }
 
@@ -238,7 +256,7 @@ int oracle_attention(const void* q, const void* k, const void* v, const int32_t*
     if (!valid(p)) return -1;
     parallel_rows((int64_t)B * Hq, nthreads, [&](int64_t r) {
         int b = (int)(r / Hq), h = (int)(r % Hq);
-        attend_row(p, b, h, out + r * D, lse + r);
+        attend_row(p, b, 0, h, out + r * D, lse + r);
     });
     return 0;
 }
@@ -254,7 +272,7 @@ int oracle_attention_rows(const void* q, const void* k, const void* v, const int
     for (int i = 0; i < n; ++i)
         if (rows_b[i] < 0 || rows_b[i] >= B || rows_h[i] < 0 || rows_h[i] >= Hq) return -1;
     parallel_rows(n, nthreads, [&](int64_t i) {
-        attend_row(p, rows_b[i], rows_h[i], out + i * D, lse + i);
+        attend_row(p, rows_b[i], 0, rows_h[i], out + i * D, lse + i);
     });
     return 0;
 }
@@ -268,7 +286,7 @@ int oracle_split_partials(const void* q, const void* k, const void* v, const int
     if (!valid(p) || S < 1) return -1;
     parallel_rows((int64_t)B * Hq, nthreads, [&](int64_t r) {
         int b = (int)(r / Hq), h = (int)(r % Hq);
-        split_row(p, b, h, S, o_part + r * S * D, lse_part + r * S);
+        split_row(p, b, 0, h, S, o_part + r * S * D, lse_part + r * S);
     });
     return 0;
 }
@@ -294,11 +312,60 @@ int oracle_split_partials_var(const void* q, const void* k, const void* v, const
         int b = (int)(r / Hq), h = (int)(r % Hq);
         double* o = o_part + r * max_splits * D;
         double* l = lse_part + r * max_splits;
-        split_row(p, b, h, s_count[b], o, l);
+        split_row(p, b, 0, h, s_count[b], o, l);
         for (int sp = s_count[b]; sp < max_splits; ++sp) {
             l[sp] = kNegInf;
             for (int d = 0; d < D; ++d) o[(int64_t)sp * D + d] = 0.0;
         }
+    });
+    return 0;
+}
+
+// Several query tokens per sequence: out[B, tq, Hq, D], lse[B, tq, Hq].
+int oracle_attention_mq(const void* q, const void* k, const void* v, const int32_t* cu, int32_t B,
+                        int32_t Hq, int32_t Hkv, int32_t D, int64_t kv_rows, int32_t dtype,
+                        int32_t layout, double scale, int32_t tq, double* out, double* lse,
+                        int nthreads) {
+    Problem p = make(q, k, v, cu, B, Hq, Hkv, D, kv_rows, dtype, layout, scale);
+    if (!valid(p) || tq < 1) return -1;
+    p.tq = tq;
+    parallel_rows((int64_t)B * tq * Hq, nthreads, [&](int64_t r) {
+        int h = (int)(r % Hq), t = (int)((r / Hq) % tq), b = (int)(r / ((int64_t)Hq * tq));
+        attend_row(p, b, t, h, out + r * D, lse + r);
+    });
+    return 0;
+}
+
+// The same on selected (b, t, h) triples: out[n, D], lse[n].
+int oracle_attention_rows_mq(const void* q, const void* k, const void* v, const int32_t* cu,
+                             int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int64_t kv_rows,
+                             int32_t dtype, int32_t layout, double scale, int32_t tq,
+                             const int32_t* rows_b, const int32_t* rows_t, const int32_t* rows_h,
+                             int32_t n, double* out, double* lse, int nthreads) {
+    Problem p = make(q, k, v, cu, B, Hq, Hkv, D, kv_rows, dtype, layout, scale);
+    if (!valid(p) || tq < 1) return -1;
+    p.tq = tq;
+    for (int i = 0; i < n; ++i)
+        if (rows_b[i] < 0 || rows_b[i] >= B || rows_t[i] < 0 || rows_t[i] >= tq || rows_h[i] < 0 ||
+            rows_h[i] >= Hq)
+            return -1;
+    parallel_rows(n, nthreads, [&](int64_t i) {
+        attend_row(p, rows_b[i], rows_t[i], rows_h[i], out + i * D, lse + i);
+    });
+    return 0;
+}
+
+// Per-split partials with several query tokens: o_part[B, tq, Hq, S, D], lse_part[B, tq, Hq, S].
+int oracle_split_partials_mq(const void* q, const void* k, const void* v, const int32_t* cu,
+                             int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int64_t kv_rows,
+                             int32_t dtype, int32_t layout, double scale, int32_t tq, int32_t S,
+                             double* o_part, double* lse_part, int nthreads) {
+    Problem p = make(q, k, v, cu, B, Hq, Hkv, D, kv_rows, dtype, layout, scale);
+    if (!valid(p) || tq < 1 || S < 1) return -1;
+    p.tq = tq;
+    parallel_rows((int64_t)B * tq * Hq, nthreads, [&](int64_t r) {
+        int h = (int)(r % Hq), t = (int)((r / Hq) % tq), b = (int)(r / ((int64_t)Hq * tq));
+        split_row(p, b, t, h, S, o_part + r * S * D, lse_part + r * S);
     });
     return 0;
 }
@@ -341,7 +408,7 @@ int oracle_weights(const void* q, const void* k, const void* v, const int32_t* c
     int64_t L = seq_len(p, b);
     if (L == 0) return 0;
     std::vector<double> qd;
-    scores(p, b, h, 0, L, qd, p_out);
+    scores(p, b, 0, h, 0, L, qd, p_out);
     double m = kNegInf;
     for (int64_t j = 0; j < L; ++j) m = p_out[j] > m ? p_out[j] : m;
     double z = 0.0;

@@ -22,6 +22,7 @@ DA_DEVERR_SEQLENS, DA_DEVERR_TIMEOUT = 0x1, 0x2
 DA_MAX_SPLITS = 1024
 DA_NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 DA_MAX_VARSPLIT_BATCH = 1024
+DA_MAX_QUERY_TOKENS = 16
 
 EXPORTED = [
     "decode_attn_splitkv_workspace_size", "decode_attn_splitkv_lse_offset",
@@ -30,7 +31,7 @@ EXPORTED = [
     "decode_attn_splitkv_partial", "decode_attn_splitkv_combine", "decode_attn_splitkv_get_error",
     "decode_attn_splitkv_selftest_timeout", "decode_attn_splitkv_status_string",
     "decode_attn_splitkv_noalloc", "decode_attn_splitkv_varsplit",
-    "decode_attn_splitkv_varsplit_plan",
+    "decode_attn_splitkv_varsplit_plan", "decode_attn_splitkv_multiquery",
 ]
 
 _lib = None
@@ -82,6 +83,9 @@ def load(path: str = LIB):
     lib.decode_attn_splitkv_varsplit_plan.argtypes = [I, I, I, I, I64, I, I, ctypes.POINTER(I),
                                                       ctypes.POINTER(I)]
     lib.decode_attn_splitkv_varsplit_plan.restype = I
+    lib.decode_attn_splitkv_multiquery.argtypes = [P, P, P, P, I, I, I, I, I, I, I, I, F, I, P, P,
+                                                   SZ, P]
+    lib.decode_attn_splitkv_multiquery.restype = I
     lib.decode_attn_splitkv_status_string.argtypes = [I]
     lib.decode_attn_splitkv_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -200,6 +204,23 @@ def decode_attn_splitkv_varsplit(q, k, v, cu_seqlens_k, out, workspace, *, split
         layout, sc, split_len, max_splits, _ptr(out), _ptr(workspace), workspace.numel(),
         _stream(stream))
     _check(st, "decode_attn_splitkv_varsplit")
+    return out
+
+
+def decode_attn_splitkv_multiquery(q, k, v, cu_seqlens_k, out, workspace, *, num_splits: int,
+                                   scale: float | None = None, layout: int = DA_LAYOUT_VARLEN,
+                                   stream=None):
+    """Several query tokens per sequence: q and out are [B, T_q, Hq, D]; see the C header."""
+    B, T, Hq, D = q.shape
+    if layout == DA_LAYOUT_VARLEN:
+        kv_rows, Hkv = k.shape[0], k.shape[1]
+    else:
+        Hkv, kv_rows = k.shape[1], k.shape[2]
+    sc = 1.0 / math.sqrt(D) if scale is None else scale
+    st = load().decode_attn_splitkv_multiquery(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_k), B, T, Hq, Hkv, D, kv_rows, _dtype_code(q),
+        layout, sc, num_splits, _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "decode_attn_splitkv_multiquery")
     return out
 
 

@@ -75,10 +75,11 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
 struct ItemSlot {          // one work item, as the producer decoded it
-    int32_t b, kvh, h0, nh;
+    int32_t b, kvh, h0, nh;            // h0: first query head of the KV head's group; nh columns
     int32_t s, nkeys, ntiles, valid;   // valid = 0 marks the end of the queue
     int64_t first_key;                 // varlen: K/V row of the split start; bhsd: position
-    int64_t pad;
+    int32_t c0;                        // first packed (token, head) column of this item
+    int32_t vis0;                      // keys of the split query token 0 may see (may be <= 0)
 };
 static_assert(sizeof(ItemSlot) == 48, "ItemSlot layout");
 
@@ -118,6 +119,7 @@ struct SplitParams {
     uint16_t* out;           // [B, Hq, D] when S == 1 (o_0 is the output), else nullptr
     int B, Hq, Hkv, G, S, kv_rows, layout, chunks, no_kv, n_items;
     int split_len;           // 0: every sequence has S splits; else S_b = min(S, ceil(L_b / split_len))
+    int tq;                  // query tokens per sequence; columns per KV head = G * tq
     float scale_log2;        // scale * log2(e)
     unsigned long long wait_limit_ns;
 };
@@ -338,8 +340,9 @@ __device__ __forceinline__ ItemSlot decode_item(const SplitParams& p, int idx, c
         chunk = hc % p.chunks;
         it.kvh = hc / p.chunks;
     }
-    it.h0 = it.kvh * p.G + chunk * kHeadsPerCta;
-    it.nh = min(kHeadsPerCta, p.G - chunk * kHeadsPerCta);
+    it.h0 = it.kvh * p.G;
+    it.c0 = chunk * kHeadsPerCta;
+    it.nh = min(kHeadsPerCta, p.G * p.tq - it.c0);
     int64_t base;
     bool bad;
     const int64_t L = checked_len(p.cu, it.b, p.layout, p.kv_rows, p.no_kv, &base, &bad);
@@ -348,9 +351,18 @@ __device__ __forceinline__ ItemSlot decode_item(const SplitParams& p, int idx, c
     it.nkeys = static_cast<int>(hi - lo);
     it.ntiles = (it.nkeys + kStageKeys - 1) / kStageKeys;
     it.first_key = base + lo;
+    // query token t sits at position L - tq + t and sees keys up to it
+    const int64_t vis0 = L - p.tq + 1 - lo;
+    it.vis0 = static_cast<int>(vis0 < -(1 << 30) ? -(1 << 30) : vis0);
     it.valid = 1;
-    it.pad = 0;
     return it;
+}
+
+// Workspace/output row of packed column c of an item: token t = c / G, head
+// h = h0 + c % G, row = (b * tq + t) * Hq + h.
+__device__ __forceinline__ int64_t column_row(const SplitParams& p, const ItemSlot& it, int c) {
+    const int cg = it.c0 + c;
+    return (static_cast<int64_t>(it.b) * p.tq + cg / p.G) * p.Hq + it.h0 + cg % p.G;
 }
 
 // ------------------------------------------------------------ split step
@@ -448,8 +460,13 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
                 slots[slot] = item;
                 const uint32_t ib = ifull0 + 8 * slot;
                 mbar_arrive_expect_tx(ib, item.nh * D * 2);
-                bulk_load(qbuf + slot * Sh::kQBytes, p.q + (static_cast<int64_t>(item.b) * p.Hq + item.h0) * D,
-                          item.nh * D * 2, ib);
+                if (p.tq == 1) {
+                    // one query token: the item's heads are contiguous rows of q
+                    bulk_load(qbuf + slot * Sh::kQBytes, p.q + column_row(p, item, 0) * D, item.nh * D * 2, ib);
+                } else {
+                    for (int c = 0; c < item.nh; ++c)
+                        bulk_load(qbuf + slot * Sh::kQBytes + c * D * 2, p.q + column_row(p, item, c) * D, D * 2, ib);
+                }
                 bool ok = true;
                 for (int t = 0; t < item.ntiles; ++t) {
                     if (!mbar_wait(empty0 + 8 * st, ph ^ 1, p.wait_limit_ns)) {
@@ -555,6 +572,12 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
         if (lane == 0) mbar_arrive(iempty0 + 8 * slot);
         if (!item.valid) break;
 
+        // keys (relative to the split start) visible to this thread's two columns
+        int visA = item.nkeys, visB = item.nkeys;
+        if (p.tq > 1) {
+            visA = min(item.nkeys, item.vis0 + (item.c0 + 2 * t4) / p.G);
+            visB = min(item.nkeys, item.vis0 + (item.c0 + 2 * t4 + 1) / p.G);
+        }
         float acc[D / 16][4];
 #pragma unroll
         for (int i = 0; i < D / 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
@@ -604,11 +627,10 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
                 }
                 // scores -> exp2 domain, mask keys past the split end
                 const int key_lo = t * kStageKeys + warp * kBoxKeys + g;   // relative to split start
-                const bool va = key_lo < item.nkeys, vb = key_lo + 8 < item.nkeys;
-                const float x0 = va ? (sc[0] + sd[0]) * p.scale_log2 : -INFINITY;
-                const float x1 = va ? (sc[1] + sd[1]) * p.scale_log2 : -INFINITY;
-                const float x2 = vb ? (sc[2] + sd[2]) * p.scale_log2 : -INFINITY;
-                const float x3 = vb ? (sc[3] + sd[3]) * p.scale_log2 : -INFINITY;
+                const float x0 = key_lo < visA ? (sc[0] + sd[0]) * p.scale_log2 : -INFINITY;
+                const float x1 = key_lo < visB ? (sc[1] + sd[1]) * p.scale_log2 : -INFINITY;
+                const float x2 = key_lo + 8 < visA ? (sc[2] + sd[2]) * p.scale_log2 : -INFINITY;
+                const float x3 = key_lo + 8 < visB ? (sc[3] + sd[3]) * p.scale_log2 : -INFINITY;
                 float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
                 for (int off = 4; off < 32; off <<= 1) {
@@ -616,10 +638,13 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
                     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
                 }
                 const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
-                const float p0 = fast_exp2(x0 - mn0), p1 = fast_exp2(x1 - mn1);
-                const float p2 = fast_exp2(x2 - mn0), p3 = fast_exp2(x3 - mn1);
+                // a column that has seen no key yet (several query tokens) keeps -inf: use 0 as
+                // its reference so that every weight below is 0 rather than NaN
+                const float ms0 = mn0 == -INFINITY ? 0.f : mn0, ms1 = mn1 == -INFINITY ? 0.f : mn1;
+                const float p0 = fast_exp2(x0 - ms0), p1 = fast_exp2(x1 - ms1);
+                const float p2 = fast_exp2(x2 - ms0), p3 = fast_exp2(x3 - ms1);
                 if (mn0 != m_run[0] || mn1 != m_run[1]) {
-                    const float al0 = fast_exp2(m_run[0] - mn0), al1 = fast_exp2(m_run[1] - mn1);
+                    const float al0 = fast_exp2(m_run[0] - ms0), al1 = fast_exp2(m_run[1] - ms1);
                     l_run[0] *= al0;
                     l_run[1] *= al1;
 #pragma unroll
@@ -714,11 +739,12 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
                 }
                 o = o / lsum;
             }
-            const int64_t row = (static_cast<int64_t>(item.b) * p.Hq + item.h0 + hh) * p.S + item.s;
+            const int64_t qrow = column_row(p, item, hh);
+            const int64_t row = qrow * p.S + item.s;
             p.opart[row * D + d] = o;
             if (d == 0) p.lse[row] = M == -INFINITY ? -INFINITY : (M + log2f(lsum)) * kLn2;
             // one split: its weight exp(lse_0 - lse) is 1, so o_0 is the answer
-            if (p.out != nullptr) p.out[(static_cast<int64_t>(item.b) * p.Hq + item.h0 + hh) * D + d] = to_bits<DT>(o);
+            if (p.out != nullptr) p.out[qrow * D + d] = to_bits<DT>(o);
         }
         // release the stage: order these generic-proxy stores before the TMA writes that refill it
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -981,6 +1007,7 @@ struct Call {
     float scale;
     int S;           // splits per sequence, or the cap of S_b in per-sequence mode
     int split_len;   // 0: S splits for every sequence; else per-sequence S_b
+    int tq;          // query tokens per sequence
     void* ws;
 };
 
@@ -1013,7 +1040,7 @@ da_status launch_split(const Call& c, void* out, cudaStream_t stream) {
     p.done = reinterpret_cast<uint32_t*>(wsb + kDoneCounterOff);
     p.out = (c.S == 1 && c.split_len == 0) ? static_cast<uint16_t*>(out) : nullptr;
     p.lse = reinterpret_cast<float*>(wsb + decode_attn_splitkv_lse_offset());
-    p.opart = reinterpret_cast<float*>(wsb + decode_attn_splitkv_opart_offset(c.B, c.Hq, c.S));
+    p.opart = reinterpret_cast<float*>(wsb + decode_attn_splitkv_opart_offset(c.B * c.tq, c.Hq, c.S));
     p.B = c.B;
     p.Hq = c.Hq;
     p.Hkv = c.Hkv;
@@ -1021,7 +1048,8 @@ da_status launch_split(const Call& c, void* out, cudaStream_t stream) {
     p.S = c.S;
     p.kv_rows = c.kv_rows;
     p.layout = c.lay;
-    p.chunks = (p.G + kHeadsPerCta - 1) / kHeadsPerCta;
+    p.tq = c.tq;
+    p.chunks = (p.G * c.tq + kHeadsPerCta - 1) / kHeadsPerCta;
     p.no_kv = c.kv_rows == 0;
     p.n_items = c.B * c.Hkv * p.chunks * c.S;   // per-sequence mode: an upper bound (the kernel counts)
     p.split_len = c.split_len;
@@ -1058,13 +1086,13 @@ da_status launch_combine(const Call& c, void* out, cudaStream_t stream) {
     CombineParams cp;
     const uint8_t* wsb = static_cast<const uint8_t*>(c.ws);
     cp.lse = reinterpret_cast<const float*>(wsb + decode_attn_splitkv_lse_offset());
-    cp.opart = reinterpret_cast<const float*>(wsb + decode_attn_splitkv_opart_offset(c.B, c.Hq, c.S));
+    cp.opart = reinterpret_cast<const float*>(wsb + decode_attn_splitkv_opart_offset(c.B * c.tq, c.Hq, c.S));
     cp.out = static_cast<uint16_t*>(out);
     cp.cu = c.cu;
-    cp.rows = c.B * c.Hq;
+    cp.rows = c.B * c.tq * c.Hq;
     cp.S = c.S;
     cp.dchunks = combine_dchunks(cp.rows, D, c.S);
-    cp.Hq = c.Hq;
+    cp.Hq = c.Hq * c.tq;   // rows per sequence
     cp.split_len = c.split_len;
     cp.layout = c.lay;
     cp.kv_rows = c.kv_rows;
@@ -1101,8 +1129,9 @@ da_status run_decode(const Call& c, void* out, cudaStream_t st) {
 }
 
 Call make_call(const void* q, const void* k, const void* v, const int32_t* cu, int B, int Hq, int Hkv, int D,
-               int kv_rows, da_dtype dt, da_layout lay, float scale, int S, int split_len, void* ws) {
+               int kv_rows, da_dtype dt, da_layout lay, float scale, int S, int split_len, void* ws, int tq = 1) {
     Call c;
+    c.tq = tq;
     c.q = q;
     c.k = k;
     c.v = v;
@@ -1271,6 +1300,29 @@ da_status decode_attn_splitkv_varsplit(const void* q, const void* k, const void*
     if (static_cast<int64_t>(B) * Hq * D > 0x7fffffffll) return DA_ERR_INVALID_ARG;
     return run_decode(make_call(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale, max_splits,
                                 split_len, workspace),
+                      out, static_cast<cudaStream_t>(stream));
+}
+
+da_status decode_attn_splitkv_multiquery(const void* q, const void* k, const void* v,
+                                         const int32_t* cu_seqlens_k, int B, int T_q, int Hq, int Hkv,
+                                         int D, int kv_rows, da_dtype dtype, da_layout layout, float scale,
+                                         int num_splits, void* out, void* workspace, size_t workspace_bytes,
+                                         void* stream) {
+    if (T_q < 1 || T_q > DA_MAX_QUERY_TOKENS) return DA_ERR_INVALID_ARG;
+    if (B < 1 || static_cast<int64_t>(B) * T_q > 0x7fffffffll) return DA_ERR_INVALID_ARG;
+    // the workspace holds B * T_q rows of Hq heads
+    const size_t need = decode_attn_splitkv_workspace_size(B * T_q, Hq, D, num_splits);
+    da_status st = check_common(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale, num_splits,
+                                workspace, need == 0 ? workspace_bytes : std::max(workspace_bytes, need));
+    if (st != DA_OK) return st;
+    if (workspace_bytes < need) return DA_ERR_WORKSPACE_TOO_SMALL;
+    if (!out) return DA_ERR_INVALID_ARG;
+    if (!aligned(out, 16)) return DA_ERR_ALIGNMENT;
+    const int64_t chunks = (static_cast<int64_t>(Hq / Hkv) * T_q + kHeadsPerCta - 1) / kHeadsPerCta;
+    if (static_cast<int64_t>(B) * Hkv * chunks * num_splits > 0x7fffffffll) return DA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(B) * T_q * Hq * D > 0x7fffffffll) return DA_ERR_INVALID_ARG;
+    return run_decode(make_call(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale, num_splits, 0,
+                                workspace, T_q),
                       out, static_cast<cudaStream_t>(stream));
 }
 

@@ -43,6 +43,7 @@ class Problem:
     num_splits: int | None   # None: use the split-count picker
     seed: int = 0
     kv_rows: int = 0
+    tq: int = 1              # query tokens per sequence; q is [B, tq, Hq, D] when tq > 1
     q: np.ndarray | None = field(default=None, repr=False)
     k: np.ndarray | None = field(default=None, repr=False)
     v: np.ndarray | None = field(default=None, repr=False)
@@ -84,19 +85,20 @@ def materialize(p: Problem, q_mean: float = 0.0, q_std: float = 1.0,
         if p.kv_rows < max(p.lens, default=0):
             p.kv_rows = max(p.lens, default=0)
         kv_shape = (p.B, p.Hkv, p.kv_rows, p.D)
-    nq = p.B * p.Hq * p.D
+    nq = p.B * p.tq * p.Hq * p.D
+    q_shape = (p.B, p.Hq, p.D) if p.tq == 1 else (p.B, p.tq, p.Hq, p.D)
     nkv = int(np.prod(kv_shape))
-    p.q = normal_bits(p.seed, 1, nq, p.dtype, q_mean, q_std).reshape(p.B, p.Hq, p.D)
+    p.q = normal_bits(p.seed, 1, nq, p.dtype, q_mean, q_std).reshape(q_shape)
     p.k = normal_bits(p.seed, 2, nkv, p.dtype, k_mean, k_std).reshape(kv_shape)
     p.v = normal_bits(p.seed, 3, nkv, p.dtype, v_mean, v_std).reshape(kv_shape)
     return p
 
 
 def custom(name, B, Hq, Hkv, D, lens, dtype="f16", layout=LAYOUT_VARLEN, num_splits=None,
-           seed=0, kv_rows=0, scale=None, data=True, **dist) -> Problem:
+           seed=0, kv_rows=0, scale=None, data=True, tq=1, **dist) -> Problem:
     p = Problem(name=name, B=B, Hq=Hq, Hkv=Hkv, D=D, lens=[int(x) for x in lens], dtype=dtype,
                 layout=layout, scale=(1.0 / math.sqrt(D)) if scale is None else scale,
-                num_splits=num_splits, seed=seed, kv_rows=kv_rows)
+                num_splits=num_splits, seed=seed, kv_rows=kv_rows, tq=tq)
     if data:
         materialize(p, **dist)
     return p

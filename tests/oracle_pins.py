@@ -390,6 +390,106 @@ def pin_varsplit_merge_invariance(o):
             assert sc[b] == (1 if L == 0 else min(m, -(-L // n)))
 
 
+def read_causal_golden():
+    rows = []
+    with open(os.path.join(GOLDEN, "causal_splits.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            parts = [x.split() for x in line.split("|")]
+            L, tq, S = (int(x) for x in parts[0])
+            rows.append((L, tq, S, [[int(x) for x in c] for c in parts[1:]]))
+    return rows
+
+
+def pin_mq_causal_counts_golden(o):
+    """Several query tokens: q = 0 gives lse = ln(keys seen) per token and split (hand-worked)."""
+    for L, tq, S, counts in read_causal_golden():
+        assert len(counts) == tq and all(len(c) == S for c in counts)
+        p = custom("cz", 1, 2, 1, 64, [L], "f16", seed=3, q_std=0.0, tq=tq)
+        op, lp = o.split_partials_mq(p, tq, S)
+        out, lse = o.attention_mq(p, tq)
+        v = _dec(p, p.v)
+        for t in range(tq):
+            for s_ in range(S):
+                n = counts[t][s_]
+                if n == 0:
+                    assert np.isneginf(lp[0, t, :, s_]).all() and not op[0, t, :, s_].any()
+                else:
+                    assert np.abs(lp[0, t, :, s_] - math.log(n)).max() <= 1e-13, (L, tq, S, t, s_)
+            vis = sum(counts[t])
+            if vis == 0:
+                assert not out[0, t].any() and np.isneginf(lse[0, t]).all()
+            else:
+                assert np.abs(lse[0, t] - math.log(vis)).max() <= 1e-13
+                assert np.abs(out[0, t] - v[:vis, 0, :].mean(axis=0)).max() <= 1e-14
+
+
+def pin_mq_tq1_equals_single(o):
+    p = custom("t1", 3, 8, 2, 64, [9, 100, 1], "bf16", seed=12)
+    a, la = o.attention(p)
+    b, lb = o.attention_mq(p, 1)
+    assert np.array_equal(a, b[:, 0]) and np.array_equal(la, lb[:, 0])
+    pa, pla = o.split_partials(p, 4)
+    pb, plb = o.split_partials_mq(p, 1, 4)
+    assert np.array_equal(pa, pb[:, 0]) and np.array_equal(pla, plb[:, 0])
+
+
+def pin_mq_token_equals_truncated_single(o):
+    """Token t equals a single-query problem whose cache stops at the token's own position."""
+    for layout in (LAYOUT_VARLEN, LAYOUT_BHSD):
+        lens = [40, 7, 3]
+        tq = 4
+        p = custom("mq", 3, 8, 2, 64, lens, "f16", layout=layout, seed=8, tq=tq,
+                   kv_rows=48 if layout == LAYOUT_BHSD else 0)
+        out, lse = o.attention_mq(p, tq)
+        for b, L in enumerate(lens):
+            for t in range(tq):
+                vis = max(0, L - tq + t + 1)
+                s1 = custom("one", 1, 8, 2, 64, [vis], "f16", data=False)
+                s1.q = np.ascontiguousarray(p.q[b, t][None])
+                if layout == LAYOUT_VARLEN:
+                    s1.k = np.ascontiguousarray(p.k[p.cu[b]: p.cu[b] + vis])
+                    s1.v = np.ascontiguousarray(p.v[p.cu[b]: p.cu[b] + vis])
+                else:
+                    s1.k = np.ascontiguousarray(p.k[b, :, :vis].transpose(1, 0, 2))
+                    s1.v = np.ascontiguousarray(p.v[b, :, :vis].transpose(1, 0, 2))
+                s1.cu = np.array([0, vis], dtype=np.int32)
+                s1.kv_rows = vis
+                ref, rl = o.attention(s1)
+                assert np.array_equal(out[b, t], ref[0]), (layout, b, t)
+                assert np.array_equal(lse[b, t], rl[0])
+
+
+def pin_mq_split_invariance(o):
+    p = custom("mqs", 2, 6, 3, 64, [300, 17], "f16", seed=14, tq=5)
+    ref, ref_lse = o.attention_mq(p, 5)
+    for S in (1, 3, 8, 40):
+        op, lp = o.split_partials_mq(p, 5, S)
+        out, lse = o.merge(op, lp)
+        assert np.abs(out - ref).max() <= 1e-12, S
+        assert np.abs(lse - ref_lse).max() <= 1e-12, S
+
+
+def pin_mq_library_cross_check(o):
+    p = custom("mqt", 2, 4, 2, 64, [50, 6], "f16", seed=15, tq=3)
+    out, lse = o.attention_mq(p, 3)
+    q = torch.from_numpy(_dec(p, p.q))
+    k = torch.from_numpy(_dec(p, p.k))
+    v = torch.from_numpy(_dec(p, p.v))
+    for b, L in enumerate(p.lens):
+        kk = k[int(p.cu[b]): int(p.cu[b + 1])]
+        vv = v[int(p.cu[b]): int(p.cu[b + 1])]
+        for t in range(3):
+            mask = torch.arange(L) <= (L - 3 + t)
+            for h in range(4):
+                sc = (kk[:, h // 2, :] @ q[b, t, h]) * p.scale
+                sc = sc.masked_fill(~mask, -math.inf)
+                ref = torch.softmax(sc, 0) @ vv[:, h // 2, :]
+                assert (out[b, t, h] - ref.numpy()).__abs__().max() <= 1e-12
+
+
 ALL_PINS = [
     pin_f16_decoder, pin_bf16_decoder, pin_split_bounds_golden, pin_split_bounds_partition,
     pin_split_invariance, pin_weights_sum_to_one, pin_single_key, pin_single_key_lse,
@@ -397,4 +497,6 @@ ALL_PINS = [
     pin_one_hot_dominance, pin_library_cross_check, pin_bhsd_matches_varlen,
     pin_empty_splits_and_sequences, pin_threads_deterministic, pin_rows_match_full,
     pin_split_counts_golden, pin_varsplit_merge_invariance,
+    pin_mq_causal_counts_golden, pin_mq_tq1_equals_single, pin_mq_token_equals_truncated_single,
+    pin_mq_split_invariance, pin_mq_library_cross_check,
 ]

@@ -1,0 +1,109 @@
+"""Several query tokens per sequence (decode_attn_splitkv_multiquery) vs the float64 oracle."""
+import math
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import split_kv_decode_decoding_gb300 as da
+from gpu_util import LSE_TOL, OUT_TOL, max_abs, opart_tol, out_excess, to_device, torch_dtype
+from oracle_pins import read_causal_golden
+from synth.workloads import LAYOUT_BHSD, LAYOUT_VARLEN, custom
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    da.build()
+    da.load()
+
+
+def run_mq(p, tq, S, tensors=None):
+    q, k, v, cu = tensors if tensors is not None else to_device(p)
+    q = q.view(p.B, tq, p.Hq, p.D)
+    ws = da.alloc_workspace(p.B * tq, p.Hq, p.D, S)
+    out = torch.empty(p.B, tq, p.Hq, p.D, dtype=torch_dtype(p), device="cuda")
+    da.decode_attn_splitkv_multiquery(q, k, v, cu, out, ws, num_splits=S, scale=p.scale,
+                                      layout=p.layout)
+    err = da.decode_attn_splitkv_get_error(ws)
+    lse, opart = da.workspace_views(ws, p.B * tq, p.Hq, p.D, S)
+    return (out.to(torch.float64).cpu().numpy(),
+            lse.to(torch.float64).cpu().numpy().reshape(p.B, tq, p.Hq, S),
+            opart.to(torch.float64).cpu().numpy().reshape(p.B, tq, p.Hq, S, p.D), err)
+
+
+CASES = [
+    # name, B, tq, Hq, Hkv, D, lens, dtype, layout, S, kv_rows
+    ("llama_g4_tq2", 3, 2, 32, 8, 128, [1000, 5, 130], "bf16", LAYOUT_VARLEN, 4, 0),
+    ("qwen_g7_tq4", 2, 4, 28, 4, 128, [700, 64], "f16", LAYOUT_VARLEN, 3, 0),
+    ("mha_tq8_bhsd", 2, 8, 8, 8, 128, [300, 9], "f16", LAYOUT_BHSD, 2, 320),
+    ("short_seq_more_splits", 2, 3, 4, 1, 64, [2, 50], "f16", LAYOUT_VARLEN, 5, 0),
+    ("tq16_g8", 1, 16, 16, 2, 128, [4096], "f16", LAYOUT_VARLEN, 8, 0),
+    ("one_split_direct", 3, 2, 8, 2, 64, [1, 2, 3], "bf16", LAYOUT_VARLEN, 1, 0),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_multiquery_parity(case):
+    name, B, tq, Hq, Hkv, D, lens, dtype, layout, S, kv_rows = case
+    p = custom(name, B, Hq, Hkv, D, lens, dtype, layout, S, seed=zlib.crc32(name.encode()) % 991,
+               kv_rows=kv_rows, tq=tq)
+    if layout == LAYOUT_BHSD:
+        for b, L in enumerate(lens):
+            p.k[b, :, L:, :] = 0x7E00
+            p.v[b, :, L:, :] = 0x7E00
+    out, lse, opart, err = run_mq(p, tq, S)
+    assert err == 0
+    orc = oracle.default()
+    ref, _ = orc.attention_mq(p, tq)
+    ref_op, ref_lse = orc.split_partials_mq(p, tq, S)
+    assert out_excess(out, ref, p.dtype) <= OUT_TOL
+    assert np.array_equal(np.isneginf(lse), np.isneginf(ref_lse)), "empty-split pattern differs"
+    assert max_abs(lse, ref_lse) <= LSE_TOL
+    assert max_abs(opart, ref_op) <= opart_tol(p)
+
+
+def test_multiquery_causal_bounds_q_zero():
+    """q = 0: lse = ln(keys the token sees in the split), -inf where it sees none (hand-worked)."""
+    for L, tq, S, counts in read_causal_golden():
+        p = custom("cz", 2, 4, 1, 64, [L, L + 3], "f16", seed=4, q_std=0.0, tq=tq)
+        out, lse, opart, err = run_mq(p, tq, S)
+        assert err == 0
+        for t in range(tq):
+            for s in range(S):
+                n = counts[t][s]
+                if n == 0:
+                    assert np.isneginf(lse[0, t, :, s]).all()
+                else:
+                    assert np.abs(lse[0, t, :, s] - math.log(n)).max() <= 1e-5, (L, tq, S, t, s)
+
+
+def test_multiquery_one_token_matches_single_query_bit_for_bit():
+    p = custom("t1", 3, 28, 4, 128, [900, 64, 2000], "f16", LAYOUT_VARLEN, 4, seed=6)
+    q, k, v, cu = to_device(p)
+    a = run_mq(p, 1, 4, tensors=(q.view(p.B, 1, p.Hq, p.D), k, v, cu))[0][:, 0]
+    ws = da.alloc_workspace(p.B, p.Hq, p.D, 4)
+    out = torch.empty(p.B, p.Hq, p.D, dtype=torch.float16, device="cuda")
+    da.decode_attn_splitkv(q, k, v, cu, out, ws, num_splits=4, scale=p.scale)
+    assert np.array_equal(a, out.to(torch.float64).cpu().numpy())
+
+
+def test_multiquery_long_context_sampled():
+    """Llama heads, 16 sequences of 32768 keys, two query tokens each (speculative decoding)."""
+    tq = 2
+    p = custom("llama_S32768_B16_tq2", 16, 32, 8, 128, [32768] * 16, "bf16", LAYOUT_VARLEN, None,
+               seed=0, tq=tq)
+    S = da.num_splits(p.B, p.Hq * tq, p.Hkv, p.D, 32768, 32768)
+    out, lse, opart, err = run_mq(p, tq, S)
+    assert err == 0
+    rng = np.random.default_rng(2)
+    rb = rng.integers(0, p.B, 16).astype(np.int32)
+    rt = rng.integers(0, tq, 16).astype(np.int32)
+    rh = rng.integers(0, p.Hq, 16).astype(np.int32)
+    ref, _ = oracle.default().attention_rows_mq(p, tq, rb, rt, rh)
+    assert out_excess(out[rb, rt, rh], ref, p.dtype) <= OUT_TOL

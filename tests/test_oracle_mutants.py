@@ -29,11 +29,17 @@ MUTANTS = {
     "bf16_exponent_bias": ("e - 134);", "e - 133);"),
     "softmax_not_normalized": ("double pj = s[j] / z;", "double pj = s[j];"),
     "max_not_subtracted": ("s[j] = std::exp(s[j] - m);", "s[j] = std::exp(s[j]);"),
-    "q_row_transposed": ("((int64_t)b * p.Hq + h) * p.D", "((int64_t)h * p.B + b) * p.D"),
+    "q_row_transposed": ("(((int64_t)b * p.tq + t) * p.Hq + h) * p.D",
+                         "(((int64_t)h * p.tq + t) * p.B + b) * p.D"),
     "split_count_floor": ("int64_t sb = L == 0 ? 1 : (L + split_len - 1) / split_len;",
                           "int64_t sb = L == 0 ? 1 : (L + split_len / 2) / split_len;"),
     "split_count_cap_off_by_one": ("s_count[b] = (int32_t)(sb < max_splits ? sb : max_splits);",
                              "s_count[b] = (int32_t)(sb < max_splits ? sb : max_splits - 1);"),
+    "token_sees_one_key_less": ("int64_t v = seq_len(p, b) - p.tq + t + 1;",
+                                "int64_t v = seq_len(p, b) - p.tq + t;"),
+    "split_ignores_causal_limit": ("if (hi > vis) hi = vis;", "if (false) hi = vis;"),
+    "query_token_ignored": ("(((int64_t)b * p.tq + t) * p.Hq + h) * p.D",
+                            "(((int64_t)b * p.tq) * p.Hq + h) * p.D"),
     "merge_skips_last_split": ("for (int s = 0; s < S; ++s) {\n            if (ls[s] == kNegInf) continue;",
                                "for (int s = 0; s + 1 < S; ++s) {\n            if (ls[s] == kNegInf) continue;"),
 }
