@@ -50,6 +50,10 @@ def parse():
     ap.add_argument("--varsplit", action="store_true",
                     help="per-sequence split counts (decode_attn_splitkv_varsplit) with its planner")
     ap.add_argument("--split-len", type=int, default=0, help="override the planner's split_len")
+    ap.add_argument("--fa2-style", action="store_true",
+                    help="comparison: no split and one query head per unit (K/V repeated per "
+                         "query head, as FlashAttention-style decode reads them); GB/s still "
+                         "counts the GQA cache bytes")
     ap.add_argument("--tq", type=int, default=1,
                     help="query tokens per sequence (decode_attn_splitkv_multiquery when > 1)")
     ap.add_argument("--e2e-steps", type=int, default=30)
@@ -263,6 +267,16 @@ def main():
         materialize(p)
     else:
         p = workload(args.workload)
+    kv_bytes_gqa = p.kv_bytes
+    if args.fa2_style:
+        import numpy as np
+        G = p.Hq // p.Hkv
+        axis = 1 if p.layout == 0 else 1
+        p.k = np.repeat(p.k, G, axis=axis)
+        p.v = np.repeat(p.v, G, axis=axis)
+        p.Hkv = p.Hq
+        p.num_splits = 1
+        p.name = f"{p.name}_fa2style"
 
     if world > 1:
         import torch.distributed as dist
@@ -292,6 +306,8 @@ def main():
     else:
         S = args.splits or p.num_splits or da.num_splits(p.B, p.Hq * p.tq, p.Hkv, p.D, min(p.lens),
                                                           max(p.lens))
+    if args.fa2_style:
+        S = 1
     hq, hk, hv, hcu = problem_tensors(p, dev)
     q, k, v, cu = hq.to(dev), hk.to(dev), hv.to(dev), hcu.to(dev)
     out = torch.empty(*p.q.shape, dtype=q.dtype, device=dev)
@@ -371,7 +387,7 @@ def main():
     split_ms = [evk[i][0].elapsed_time(evk[i][1]) for i in range(k_split)]
     total_ms = max_over_ranks(sum(step_ms), dev)
     mean_step_ms = total_ms / args.steps
-    value = world * p.kv_bytes / (mean_step_ms * 1e-3) / 1e9
+    value = world * kv_bytes_gqa / (mean_step_ms * 1e-3) / 1e9
 
     # ---- end to end through the public call, host buffers, copies inside each step
     e2e = None

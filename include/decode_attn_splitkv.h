@@ -297,6 +297,35 @@ da_status decode_attn_splitkv_noalloc(const void* q, const void* k, const void* 
                                       int D, int kv_rows, da_dtype dtype, da_layout layout,
                                       float scale, int num_splits, void* out, void* stream);
 
+/*
+ * Time model of one decode_attn_splitkv (or _multiquery) call on GB300, in
+ * microseconds: a restatement of the lecture page's decode time model
+ * (04_flash_decoding.py, decode_attention_time, best_splits; its A100/H100
+ * constants are not on the page) for this library's persistent kernel:
+ *
+ *   T = t0 + max(W / bw, makespan) + [S > 1] * (t_comb + W_ws / bw_comb)
+ *
+ * W: K/V bytes streamed (each split's keys rounded up to 16, times 4*D bytes);
+ * makespan: greedy list schedule of the work items, in queue order, over
+ * (2 at D = 128, 4 at D = 64) * sm_count persistent CTAs, item cost
+ * t_item + bytes / r_cta; W_ws = B*T_q*Hq*S*(D+1)*4 workspace bytes combined.
+ *   kv_lens   host, int32 [B] sequence lengths (negative counts as 0)
+ *   params    host, double[6] {t0 us, t_item us, r_cta B/us, bw B/us, t_comb us,
+ *             bw_comb B/us}, or NULL for the built-in GB300 calibration
+ * Returns the predicted time, or a negative value if an argument is out of range.
+ */
+double decode_attn_splitkv_model_us(const int32_t* kv_lens, int B, int Hq, int Hkv, int D, int T_q,
+                                    int num_splits, int sm_count, const double* params);
+
+/*
+ * The split count (up to min(shortest length, 256)) that the built-in time model
+ * predicts fastest, and the predicted time in *predicted_us (may be NULL): the
+ * model-driven counterpart of decode_attn_splitkv_num_splits (the lecture
+ * page's best_splits). Returns 1 on out-of-range arguments.
+ */
+int decode_attn_splitkv_model_best_splits(const int32_t* kv_lens, int B, int Hq, int Hkv, int D,
+                                          int T_q, int sm_count, double* predicted_us);
+
 /* Static, human-readable name of a status code. */
 const char* decode_attn_splitkv_status_string(da_status status);
 

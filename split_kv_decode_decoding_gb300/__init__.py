@@ -32,6 +32,7 @@ EXPORTED = [
     "decode_attn_splitkv_selftest_timeout", "decode_attn_splitkv_status_string",
     "decode_attn_splitkv_noalloc", "decode_attn_splitkv_varsplit",
     "decode_attn_splitkv_varsplit_plan", "decode_attn_splitkv_multiquery",
+    "decode_attn_splitkv_model_us", "decode_attn_splitkv_model_best_splits",
 ]
 
 _lib = None
@@ -86,6 +87,11 @@ def load(path: str = LIB):
     lib.decode_attn_splitkv_multiquery.argtypes = [P, P, P, P, I, I, I, I, I, I, I, I, F, I, P, P,
                                                    SZ, P]
     lib.decode_attn_splitkv_multiquery.restype = I
+    lib.decode_attn_splitkv_model_us.argtypes = [P, I, I, I, I, I, I, I, P]
+    lib.decode_attn_splitkv_model_us.restype = ctypes.c_double
+    lib.decode_attn_splitkv_model_best_splits.argtypes = [P, I, I, I, I, I, I,
+                                                          ctypes.POINTER(ctypes.c_double)]
+    lib.decode_attn_splitkv_model_best_splits.restype = I
     lib.decode_attn_splitkv_status_string.argtypes = [I]
     lib.decode_attn_splitkv_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -134,6 +140,26 @@ def split_range(L: int, S: int, s: int) -> tuple:
     a, b = ctypes.c_int64(), ctypes.c_int64()
     load().decode_attn_splitkv_split_range(L, S, s, ctypes.byref(a), ctypes.byref(b))
     return a.value, b.value
+
+
+def model_us(lens, Hq: int, Hkv: int, D: int, num_splits: int, sm_count: int, T_q: int = 1,
+             params=None) -> float:
+    """Predicted µs of one call (the GB300 time model; params None = built-in calibration)."""
+    import numpy as np
+    ln = np.ascontiguousarray(lens, dtype=np.int32)
+    pa = None if params is None else np.ascontiguousarray(params, dtype=np.float64)
+    return load().decode_attn_splitkv_model_us(ln.ctypes.data, ln.size, Hq, Hkv, D, T_q, num_splits,
+                                               sm_count, None if pa is None else pa.ctypes.data)
+
+
+def model_best_splits(lens, Hq: int, Hkv: int, D: int, sm_count: int, T_q: int = 1) -> tuple:
+    """(split count, predicted µs) minimising the GB300 time model."""
+    import numpy as np
+    ln = np.ascontiguousarray(lens, dtype=np.int32)
+    t = ctypes.c_double()
+    S = load().decode_attn_splitkv_model_best_splits(ln.ctypes.data, ln.size, Hq, Hkv, D, T_q, sm_count,
+                                                     ctypes.byref(t))
+    return S, t.value
 
 
 def alloc_workspace(B: int, Hq: int, D: int, num_splits_: int, device="cuda", stream=None):

@@ -50,6 +50,9 @@
 
 #include <algorithm>
 #include <atomic>
+#include <climits>
+#include <functional>
+#include <vector>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -73,6 +76,8 @@ constexpr size_t kDoneCounterOff = 128;  // header: uint32 count of CTAs finishe
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
+constexpr int kMaxStagedBatch = 1024;                          // B up to which cu_seqlens_k is staged in smem
+constexpr int kStagedBytes = ((kMaxStagedBatch + 1) * 4 + 15) / 16 * 16;   // one [B + 1] int32 array
 
 struct ItemSlot {          // one work item, as the producer decoded it
     int32_t b, kvh, h0, nh;            // h0: first query head of the KV head's group; nh columns
@@ -119,6 +124,7 @@ struct SplitParams {
     uint16_t* out;           // [B, Hq, D] when S == 1 (o_0 is the output), else nullptr
     int B, Hq, Hkv, G, S, kv_rows, layout, chunks, no_kv, n_items;
     int split_len;           // 0: every sequence has S splits; else S_b = min(S, ceil(L_b / split_len))
+    int stage_cu;            // cu_seqlens_k staged in shared memory (B small enough)
     int tq;                  // query tokens per sequence; columns per KV head = G * tq
     float scale_log2;        // scale * log2(e)
     unsigned long long wait_limit_ns;
@@ -285,11 +291,11 @@ __device__ __forceinline__ int ld_cg_s32(const int32_t* p) {
 
 __device__ __forceinline__ void flag_error(uint32_t* err, uint32_t bits) { atomicOr(err, bits); }
 
-// Length of sequence b, validated against the K/V extent: a range that cannot
-// be read safely counts as empty (and *bad is set).
-__device__ __forceinline__ int64_t checked_len(const int32_t* cu, int b, int layout, int kv_rows, int no_kv,
-                                               int64_t* base, bool* bad) {
-    const int64_t c0 = ld_cg_s32(cu + b), c1 = ld_cg_s32(cu + b + 1);
+// Length of a sequence whose cu_seqlens_k entries are c0, c1, validated
+// against the K/V extent: a range that cannot be read safely counts as empty
+// (and *bad is set).
+__device__ __forceinline__ int64_t checked_len_of(int64_t c0, int64_t c1, int layout, int kv_rows, int no_kv,
+                                                  int64_t* base, bool* bad) {
     const int64_t L = c1 - c0;
     bool ok = L >= 0;
     if (layout == DA_LAYOUT_VARLEN) ok = ok && c0 >= 0 && c1 <= kv_rows;
@@ -300,6 +306,11 @@ __device__ __forceinline__ int64_t checked_len(const int32_t* cu, int b, int lay
     return ok ? L : 0;
 }
 
+__device__ __forceinline__ int64_t checked_len(const int32_t* cu, int b, int layout, int kv_rows, int no_kv,
+                                               int64_t* base, bool* bad) {
+    return checked_len_of(ld_cg_s32(cu + b), ld_cg_s32(cu + b + 1), layout, kv_rows, no_kv, base, bad);
+}
+
 // Split count of a sequence of length L (per-sequence mode): 1 for an empty
 // sequence, else ceil(L / split_len) capped at max_splits; never an empty split.
 __device__ __forceinline__ int seq_splits(int64_t L, int split_len, int max_splits) {
@@ -308,20 +319,24 @@ __device__ __forceinline__ int seq_splits(int64_t L, int split_len, int max_spli
     return static_cast<int>(sb < max_splits ? sb : max_splits);
 }
 
-// Decode work item `idx` into its descriptor (reads cu_seqlens_k). Items run
-// split-fastest, then (KV head, head chunk), then sequence. With per-sequence
-// split counts, `prefix` holds the running sum of S_b (prefix[b] splits before
-// sequence b) and the sequence is found by binary search.
-__device__ __forceinline__ ItemSlot decode_item(const SplitParams& p, int idx, const int32_t* prefix) {
+// Decode work item `idx` into its descriptor. Items run head-chunk fastest
+// (the chunks of one split read the same K/V at the same time, the second
+// read coming from L2), then split, then KV head, then sequence. `cus` is
+// cu_seqlens_k staged in shared memory (nullptr: read it from global memory).
+// With per-sequence split counts, `prefix` holds the running sum of S_b
+// (prefix[b] splits before sequence b) and the sequence is found by binary
+// search.
+__device__ __forceinline__ ItemSlot decode_item(const SplitParams& p, int idx, const int32_t* cus,
+                                                const int32_t* prefix) {
     ItemSlot it;
     int chunk, Sb;
     const int hc_count = p.Hkv * p.chunks;
     if (p.split_len == 0) {
         int r = idx;
-        it.s = r % p.S;
-        r /= p.S;
         chunk = r % p.chunks;
         r /= p.chunks;
+        it.s = r % p.S;
+        r /= p.S;
         it.kvh = r % p.Hkv;
         it.b = r / p.Hkv;
         Sb = p.S;
@@ -334,18 +349,20 @@ __device__ __forceinline__ ItemSlot decode_item(const SplitParams& p, int idx, c
         }
         it.b = lo;
         Sb = prefix[lo + 1] - prefix[lo];
-        const int r = idx - prefix[lo] * hc_count;
+        int r = idx - prefix[lo] * hc_count;
+        chunk = r % p.chunks;
+        r /= p.chunks;
         it.s = r % Sb;
-        const int hc = r / Sb;
-        chunk = hc % p.chunks;
-        it.kvh = hc / p.chunks;
+        it.kvh = r / Sb;
     }
     it.h0 = it.kvh * p.G;
     it.c0 = chunk * kHeadsPerCta;
     it.nh = min(kHeadsPerCta, p.G * p.tq - it.c0);
     int64_t base;
     bool bad;
-    const int64_t L = checked_len(p.cu, it.b, p.layout, p.kv_rows, p.no_kv, &base, &bad);
+    const int64_t L = cus != nullptr
+                          ? checked_len_of(cus[it.b], cus[it.b + 1], p.layout, p.kv_rows, p.no_kv, &base, &bad)
+                          : checked_len(p.cu, it.b, p.layout, p.kv_rows, p.no_kv, &base, &bad);
     if (bad && it.s == 0 && chunk == 0 && it.kvh == 0) flag_error(p.err, DA_DEVERR_SEQLENS);
     const int64_t lo = L * it.s / Sb, hi = L * (it.s + 1) / Sb;
     it.nkeys = static_cast<int>(hi - lo);
@@ -383,7 +400,9 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
     const uint32_t ifull0 = empty0 + 8 * kStages;       // [kItemSlots]
     const uint32_t iempty0 = ifull0 + 8 * kItemSlots;   // [kItemSlots]
     const uint32_t mfull = iempty0 + 8 * kItemSlots;    // an item's per-warp partials written
-    int32_t* prefix = reinterpret_cast<int32_t*>(smem + Sh::kEnd);   // [B + 1], per-sequence mode only
+    // past the fixed layout: cu_seqlens_k [B + 1] (when staged), then prefix[B + 1] (per-sequence mode)
+    int32_t* cus = p.stage_cu ? reinterpret_cast<int32_t*>(smem + Sh::kEnd) : nullptr;
+    int32_t* prefix = reinterpret_cast<int32_t*>(smem + Sh::kEnd + (p.stage_cu ? kStagedBytes : 0));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -414,6 +433,11 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
     if (warp == kConsumerWarps) {
         // ---------------- producer: one lane takes items and issues every copy
         int n_items = p.n_items;
+        if (cus != nullptr) {
+            // one coalesced read of cu_seqlens_k per CTA; every item is then decoded from shared memory
+            for (int i = lane; i <= p.B; i += 32) cus[i] = ld_cg_s32(p.cu + i);
+            __syncwarp();
+        }
         if (p.split_len != 0) {
             // per-sequence split counts: the whole warp builds prefix[] = running sum of S_b
             int carry = 0;
@@ -423,8 +447,10 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
                 if (b < p.B) {
                     int64_t base;
                     bool bad;
-                    sb = seq_splits(checked_len(p.cu, b, p.layout, p.kv_rows, p.no_kv, &base, &bad), p.split_len,
-                                    p.S);
+                    const int64_t L = cus != nullptr ? checked_len_of(cus[b], cus[b + 1], p.layout, p.kv_rows,
+                                                                      p.no_kv, &base, &bad)
+                                                     : checked_len(p.cu, b, p.layout, p.kv_rows, p.no_kv, &base, &bad);
+                    sb = seq_splits(L, p.split_len, p.S);
                 }
 #pragma unroll
                 for (int off = 1; off < 32; off <<= 1) {
@@ -441,6 +467,7 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
         if (lane == 0) {
             int st = 0;          // ring position of the next tile
             uint32_t ph = 0;     // its phase parity
+            int idx = static_cast<int>(blockIdx.x);   // the first item of each CTA is its own index
             for (uint32_t it = 0;; ++it) {
                 const int slot = it % kItemSlots;
                 const uint32_t iph = (it / kItemSlots) & 1;
@@ -448,15 +475,12 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
                     flag_error(p.err, DA_DEVERR_TIMEOUT);
                     break;
                 }
-                // the first item of each CTA is its own index; later ones come from the queue
-                const int idx = it == 0 ? static_cast<int>(blockIdx.x)
-                                        : static_cast<int>(gridDim.x + atomicAdd(p.work, 1u));
                 if (idx >= n_items) {
                     slots[slot].valid = 0;
                     mbar_arrive(ifull0 + 8 * slot);
                     break;
                 }
-                const ItemSlot item = decode_item(p, idx, prefix);
+                const ItemSlot item = decode_item(p, idx, cus, prefix);
                 slots[slot] = item;
                 const uint32_t ib = ifull0 + 8 * slot;
                 mbar_arrive_expect_tx(ib, item.nh * D * 2);
@@ -467,8 +491,16 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
                     for (int c = 0; c < item.nh; ++c)
                         bulk_load(qbuf + slot * Sh::kQBytes + c * D * 2, p.q + column_row(p, item, c) * D, D * 2, ib);
                 }
+                // The next item is taken from the queue a few stages before this one's
+                // last tile: the atomic's round trip then overlaps the last copies, yet a
+                // CTA never holds a reserved item for long (which would hurt the balance
+                // at the end of the queue).
+                const int fetch_at = max(0, item.ntiles - kStages);
+                int next_idx = 0;
+                if (item.ntiles == 0) next_idx = static_cast<int>(gridDim.x + atomicAdd(p.work, 1u));
                 bool ok = true;
                 for (int t = 0; t < item.ntiles; ++t) {
+                    if (t == fetch_at) next_idx = static_cast<int>(gridDim.x + atomicAdd(p.work, 1u));
                     if (!mbar_wait(empty0 + 8 * st, ph ^ 1, p.wait_limit_ns)) {
                         flag_error(p.err, DA_DEVERR_TIMEOUT);
                         ok = false;
@@ -527,6 +559,7 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
                     st = 0;
                     ph ^= 1;
                 }
+                idx = next_idx;
             }
         }
         return;
@@ -1012,7 +1045,6 @@ struct Call {
 };
 
 constexpr int kMaxVarsplitBatch = 1024;                                   // sequences, per-sequence mode
-constexpr int kPrefixBytes = ((kMaxVarsplitBatch + 1) * 4 + 15) / 16 * 16;  // its prefix[] in shared memory
 
 // `out` is written by the split kernel itself only with one uniform split.
 template <int D, int DT>
@@ -1053,15 +1085,17 @@ da_status launch_split(const Call& c, void* out, cudaStream_t stream) {
     p.no_kv = c.kv_rows == 0;
     p.n_items = c.B * c.Hkv * p.chunks * c.S;   // per-sequence mode: an upper bound (the kernel counts)
     p.split_len = c.split_len;
+    p.stage_cu = c.B <= kMaxStagedBatch;
     p.scale_log2 = c.scale * kLog2e;
     p.wait_limit_ns = kWaitLimitNs;
 
     const bool var = c.split_len != 0;
-    const int smem = Shape<D>::kSmemBytes + (var ? kPrefixBytes : 0);
+    const int smem = Shape<D>::kSmemBytes + (p.stage_cu ? kStagedBytes : 0) + (var ? kStagedBytes : 0);
     auto kern = split_kernel<D, DT>;
-    static DeviceCache cache_uniform, cache_var;
+    static DeviceCache caches[3];   // by the number of staged [B + 1] arrays
     int grid = 0;
-    if (persistent_grid(kern, smem, var ? cache_var : cache_uniform, &grid) != cudaSuccess) return DA_ERR_CUDA;
+    if (persistent_grid(kern, smem, caches[(p.stage_cu ? 1 : 0) + (var ? 1 : 0)], &grid) != cudaSuccess)
+        return DA_ERR_CUDA;
     grid = std::min(grid, p.n_items);
     cudaLaunchAttribute attrs[1] = {pdl_attr()};
     cudaLaunchConfig_t cfg = {};
@@ -1367,6 +1401,84 @@ const char* decode_attn_splitkv_status_string(da_status status) {
                    "8 MiB built-in array (use decode_attn_splitkv with a workspace)";
     }
     return "unknown da_status";
+}
+
+// ---------------------------------------------------------------- time model
+// A GB300 restatement of the lecture page's decode time model
+// (04_flash_decoding.py: decode_attention_time / best_splits, whose A100/H100
+// constants are not on the page): the call is modelled as
+//   T = t0 + max(W / bw, makespan) + [S > 1] (t_comb + W_ws / bw_comb)
+// where W is the K/V bytes streamed (each split's key count rounded up to the
+// 16-key TMA box), makespan is the greedy list schedule of the work items, in
+// queue order, over the persistent CTAs, each item costing t_item + bytes / r_cta,
+// and W_ws the workspace bytes the combine reads. The parameters were fitted
+// (least squares in log time) to 230 calls measured on one GB300: 14 workloads
+// of the CodeLlama, Llama and Qwen shapes, split counts 1 to 256, L2 flushed,
+// CUDA-event time per call; median error 3.4 %, 90th percentile 11 %.
+static const double kModelGb300[7] = {
+    /* t0 us      */ 14.17,
+    /* t_item us  */ 1.300,
+    /* r_cta B/us */ 73315,
+    /* bw B/us    */ 7.277e+06,
+    /* t_comb us  */ 0.979,
+    /* bw_comb    */ 3.537e+05,
+    /* unused     */ 0.0};
+
+double decode_attn_splitkv_model_us(const int32_t* kv_lens, int B, int Hq, int Hkv, int D, int T_q, int num_splits,
+                                    int sm_count, const double* params) {
+    if (!kv_lens || B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || (D != 64 && D != 128) || T_q < 1 ||
+        num_splits < 1 || num_splits > DA_MAX_SPLITS || sm_count < 1)
+        return -1.0;
+    const double* m = params ? params : kModelGb300;
+    const double t0 = m[0], t_item = m[1], r_cta = m[2], bw = m[3], t_comb = m[4], bw_comb = m[5];
+    if (!(r_cta > 0) || !(bw > 0) || !(bw_comb > 0)) return -1.0;
+    const int S = num_splits;
+    const int chunks = (Hq / Hkv * T_q + kHeadsPerCta - 1) / kHeadsPerCta;
+    const int slots = sm_count * (D == 128 ? 2 : 4);
+    const double key_bytes = 4.0 * D;   // K and V rows of one key and KV head
+    // greedy list schedule: a min-heap of slot free times
+    std::vector<double> heap(static_cast<size_t>(slots), 0.0);
+    auto take = [&](double cost) {
+        std::pop_heap(heap.begin(), heap.end(), std::greater<double>());
+        heap.back() += cost;
+        std::push_heap(heap.begin(), heap.end(), std::greater<double>());
+    };
+    double W = 0.0;
+    for (int b = 0; b < B; ++b) {
+        const int64_t L = kv_lens[b] < 0 ? 0 : kv_lens[b];
+        for (int kvh = 0; kvh < Hkv; ++kvh)
+            for (int s = 0; s < S; ++s) {
+                const int64_t n = L * (s + 1) / S - L * s / S;
+                const double bytes = static_cast<double>((n + kBoxKeys - 1) / kBoxKeys * kBoxKeys) * key_bytes;
+                for (int c = 0; c < chunks; ++c) {
+                    W += c == 0 ? bytes : 0.0;   // later chunks of a split re-read it from L2
+                    take(t_item + bytes / r_cta);
+                }
+            }
+    }
+    const double makespan = *std::max_element(heap.begin(), heap.end());
+    double t = t0 + std::max(W / bw, makespan);
+    if (S > 1) t += t_comb + static_cast<double>(B) * T_q * Hq * S * (D + 1) * 4.0 / bw_comb;
+    return t;
+}
+
+int decode_attn_splitkv_model_best_splits(const int32_t* kv_lens, int B, int Hq, int Hkv, int D, int T_q,
+                                          int sm_count, double* predicted_us) {
+    if (!kv_lens || B < 1) return 1;
+    int min_kv = INT32_MAX;
+    for (int b = 0; b < B; ++b) min_kv = std::min(min_kv, kv_lens[b] < 0 ? 0 : kv_lens[b]);
+    const int s_max = std::max(1, std::min(min_kv, 256));
+    int best = 1;
+    double best_t = decode_attn_splitkv_model_us(kv_lens, B, Hq, Hkv, D, T_q, 1, sm_count, nullptr);
+    for (int S = 2; S <= s_max; S += (S < 16 ? 1 : S < 64 ? 4 : 16)) {
+        const double t = decode_attn_splitkv_model_us(kv_lens, B, Hq, Hkv, D, T_q, S, sm_count, nullptr);
+        if (t > 0 && (best_t < 0 || t < best_t)) {
+            best_t = t;
+            best = S;
+        }
+    }
+    if (predicted_us) *predicted_us = best_t;
+    return best;
 }
 
 }  // extern "C"

@@ -31,7 +31,7 @@ def header_functions():
 
 def test_exports_every_declared_symbol(lib):
     names = header_functions()
-    assert len(names) == 16
+    assert len(names) == 18
     assert sorted(names) == sorted(da.EXPORTED)
     for n in names:
         assert hasattr(lib, n), n
@@ -201,3 +201,32 @@ def test_multiquery_host_checks(lib):
     assert call(q=FAKE + 4) == da.DA_ERR_ALIGNMENT
     need = da.workspace_size(2 * 2, 4, 64, 4)
     assert call(ws_bytes=need - 1) == da.DA_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_time_model_formula_by_hand(lib):
+    """One sequence, one KV head, D = 128, explicit parameters: the formula worked by hand.
+
+    L = 1000, S = 2: splits of 500 keys, rounded up to 512 (16-key boxes), 4*128 = 512 B
+    per key -> 262144 B each. With t0 = 5, t_item = 1, r_cta = 65536 B/us, bw = 1e6,
+    t_comb = 2, bw_comb = 1e6: two items on two free CTAs, each 1 + 4 = 5 us, so the
+    makespan is 5 us; W / bw = 0.524 us; workspace 1*1*1*2*129*4 = 1032 B.
+    T = 5 + 5 + 2 + 0.001032 = 12.001032 us.
+    """
+    params = [5.0, 1.0, 65536.0, 1e6, 2.0, 1e6]
+    t = da.model_us([1000], 1, 1, 128, 2, 152, params=params)
+    assert abs(t - 12.001032) < 1e-9
+    # one split: no combine term, one 1008-key item (1000 rounded up): 1 + 1008*512/65536
+    t1 = da.model_us([1000], 1, 1, 128, 1, 152, params=params)
+    assert abs(t1 - (5 + 1 + 1008 * 512 / 65536)) < 1e-9
+
+
+def test_time_model_properties(lib):
+    base = da.model_us([4096] * 8, 32, 32, 128, 1, 152)
+    assert base > 0
+    assert da.model_us([8192] * 8, 32, 32, 128, 1, 152) > 1.5 * base   # twice the bytes
+    # one long sequence: splitting it helps a lot
+    assert da.model_us([131072], 16, 2, 128, 64, 152) < 0.2 * da.model_us([131072], 16, 2, 128, 1, 152)
+    S, t = da.model_best_splits([131072], 16, 2, 128, 152)
+    assert 8 <= S <= 256 and t > 0
+    assert da.model_us([100], 4, 3, 128, 1, 152) < 0          # Hq % Hkv != 0
+    assert da.model_best_splits([5, 3], 4, 1, 128, 152)[0] <= 3
