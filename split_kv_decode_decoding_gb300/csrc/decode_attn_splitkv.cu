@@ -867,21 +867,25 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams cp) {
 
     float m = -INFINITY, z = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    int s = sub;
-    for (; s + 3 * spi < Srow; s += 4 * spi) {
+    // four iterations' loads are issued before any is folded (a missing one reads
+    // as an empty split), so a row of up to 4 * spi splits costs one L2 round trip
+    for (int s0 = sub; s0 < Srow; s0 += 4 * spi) {
         float lv[4];
         float4 ov[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            lv[u] = __ldcg(l + s + u * spi);
-            ov[u] = __ldcg(reinterpret_cast<const float4*>(po + static_cast<int64_t>(s + u * spi) * D));
+            const int s = s0 + u * spi;
+            if (s < Srow) {
+                lv[u] = __ldcg(l + s);
+                ov[u] = __ldcg(reinterpret_cast<const float4*>(po + static_cast<int64_t>(s) * D));
+            } else {
+                lv[u] = -INFINITY;
+                ov[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) combine_fold(lv[u], ov[u], m, z, acc);
     }
-    for (; s < Srow; s += spi)
-        combine_fold(__ldcg(l + s), __ldcg(reinterpret_cast<const float4*>(po + static_cast<int64_t>(s) * D)), m,
-                     z, acc);
     // merge the lanes that hold the same dims
     for (int off = lps; off < 32; off <<= 1) {
         const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
