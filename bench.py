@@ -478,7 +478,8 @@ def main():
                      "traffic": traffic, "alg_bytes_per_launch": alg_bytes,
                      "launch_us_mean": round(split_mean_ms * 1e3, 2),
                      "launches_timed": k_split,
-                     "combine_us_mean_derived": round((mean_step_ms - split_mean_ms) * 1e3, 2)},
+                     **({"combine_us_mean_derived": round((mean_step_ms - split_mean_ms) * 1e3, 2)}
+                        if per_call == 2 and not (split_len or p.tq > 1) else {})},
         "e2e": e2e,
         "gpu_launches": per_call * args.steps + per_split_step * k_split,
         "wall_s_timed_region": round(t_wall, 3),

@@ -65,3 +65,24 @@ def test_recorded_traffic_needs_current_kernel(tmp_path, monkeypatch):
     f.write_text('{"entries": [{"kernel_sha": "old", "workload": "w", "num_splits": 3, '
                  '"dram_bytes_per_launch": 1.0}]}')
     assert bench.recorded_traffic("w", 3) is None
+
+
+def test_reference_arm_prints_one_json_line():
+    """bench.py --impl reference times the float64 oracle and prints the contract's line."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny", "--steps", "2", "--warmup", "1"],
+                       capture_output=True, text=True, timeout=300, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
+    assert d["steps"] == 2 and d["warmup"] == 1 and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"] == "tiny"
