@@ -482,6 +482,10 @@ def main():
                         if per_call == 2 and not (split_len or p.tq > 1) else {})},
         "e2e": e2e,
         "gpu_launches": per_call * args.steps + per_split_step * k_split,
+        "model_us": (round(da.model_us(p.lens, p.Hq, p.Hkv, p.D, S,
+                                       torch.cuda.get_device_properties(dev).multi_processor_count,
+                                       T_q=p.tq), 1)
+                     if not (split_len or args.fa2_style) else None),
         "wall_s_timed_region": round(t_wall, 3),
     }
     if sampler:

@@ -107,3 +107,32 @@ def test_multiquery_long_context_sampled():
     rh = rng.integers(0, p.Hq, 16).astype(np.int32)
     ref, _ = oracle.default().attention_rows_mq(p, tq, rb, rt, rh)
     assert out_excess(out[rb, rt, rh], ref, p.dtype) <= OUT_TOL
+
+
+def test_multiquery_d64_bhsd_bf16():
+    p = custom("mq64", 3, 12, 3, 64, [40, 3, 200], "bf16", LAYOUT_BHSD, 3, seed=41, kv_rows=210, tq=3)
+    for b, L in enumerate(p.lens):
+        p.k[b, :, L:, :] = 0x7E00
+        p.v[b, :, L:, :] = 0x7E00
+    out, lse, opart, err = run_mq(p, 3, 3)
+    assert err == 0
+    ref, _ = oracle.default().attention_mq(p, 3)
+    assert out_excess(out, ref, p.dtype) <= OUT_TOL
+
+
+def test_multiquery_cuda_graph_replay():
+    p = custom("mqg", 2, 16, 4, 128, [1000, 333], "f16", LAYOUT_VARLEN, 4, seed=42, tq=2)
+    q, k, v, cu = to_device(p)
+    q = q.view(p.B, 2, p.Hq, p.D)
+    ws = da.alloc_workspace(p.B * 2, p.Hq, p.D, 4)
+    out = torch.empty(p.B, 2, p.Hq, p.D, dtype=torch.float16, device="cuda")
+    da.decode_attn_splitkv_multiquery(q, k, v, cu, out, ws, num_splits=4, scale=p.scale)
+    torch.cuda.synchronize()
+    eager = out.clone()
+    g = torch.cuda.CUDAGraph()
+    out.zero_()
+    with torch.cuda.graph(g):
+        da.decode_attn_splitkv_multiquery(q, k, v, cu, out, ws, num_splits=4, scale=p.scale)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)

@@ -187,3 +187,33 @@ def test_cuda_graph_capture_and_side_stream():
     assert torch.equal(out, eager)
     ref, _ = oracle.default().attention(p)
     assert max_abs(out.to(torch.float64).cpu().numpy(), ref) <= OUT_TOL
+
+
+def test_large_batch_reads_cu_from_global_memory():
+    """More than 1024 sequences: the split kernel reads cu_seqlens_k from global memory
+    instead of staging it in shared memory."""
+    rng = np.random.default_rng(5)
+    lens = [int(x) for x in rng.integers(0, 90, 1500)]
+    p = custom("bigB", 1500, 8, 2, 64, lens, "f16", LAYOUT_VARLEN, 2, seed=21)
+    check_full(p, 2)
+
+
+def test_empty_cache_without_kv_buffers():
+    """kv_rows = 0: every sequence is empty, K/V may be NULL; out = 0, every lse = -inf."""
+    B, Hq, D, S = 3, 8, 128, 2
+    q = torch.randn(B, Hq, D, device="cuda").to(torch.float16)
+    k = torch.empty(0, 2, D, dtype=torch.float16, device="cuda")
+    v = torch.empty(0, 2, D, dtype=torch.float16, device="cuda")
+    cu = torch.zeros(B + 1, dtype=torch.int32, device="cuda")
+    ws = da.alloc_workspace(B, Hq, D, S)
+    out = torch.full((B, Hq, D), float("nan"), dtype=torch.float16, device="cuda")
+    da.decode_attn_splitkv(q, k, v, cu, out, ws, num_splits=S)
+    assert da.decode_attn_splitkv_get_error(ws) == 0
+    assert not out.any()
+    lse, _ = da.workspace_views(ws, B, Hq, D, S)
+    assert torch.isneginf(lse).all()
+    # a non-empty sequence with no K/V behind it is flagged and stays empty
+    cu2 = torch.tensor([0, 0, 5, 5], dtype=torch.int32, device="cuda")
+    da.decode_attn_splitkv(q, k, v, cu2, out, ws, num_splits=S)
+    assert da.decode_attn_splitkv_get_error(ws) & da.DA_DEVERR_SEQLENS
+    assert not out.any()

@@ -123,3 +123,33 @@ def test_varsplit_skewed_long_context_sampled():
     rh = np.array([0, 13, 31, 5, 20, 31], dtype=np.int32)
     ref, _ = oracle.default().attention_rows(p, rb, rh)
     assert max_abs(out[rb, rh], ref) <= OUT_TOL
+
+
+def test_varsplit_bad_seqlens_flagged_and_contained():
+    p = custom("vbad", 3, 8, 2, 128, [300, 400, 500], "f16", LAYOUT_VARLEN, None, seed=31)
+    q, k, v, cu = to_device(p)
+    cu_bad = cu.clone()
+    cu_bad[3] = p.total_kv + 64
+    out, lse, opart, err = run_var(p, 128, 8, tensors=(q, k, v, cu_bad))
+    assert err & da.DA_DEVERR_SEQLENS
+    ref, _ = oracle.default().attention(p)
+    assert out_excess(out[:2], ref[:2], p.dtype) <= OUT_TOL
+    assert not out[2].any()
+
+
+def test_varsplit_cuda_graph_replay():
+    p = custom("vgraph", 4, 28, 4, 128, [3000, 100, 900, 2500], "f16", LAYOUT_VARLEN, None, seed=32)
+    q, k, v, cu = to_device(p)
+    ws = da.alloc_workspace(p.B, p.Hq, p.D, 12)
+    out = torch.empty(p.B, p.Hq, p.D, dtype=torch.float16, device="cuda")
+    da.decode_attn_splitkv_varsplit(q, k, v, cu, out, ws, split_len=256, max_splits=12, scale=p.scale)
+    torch.cuda.synchronize()
+    eager = out.clone()
+    g = torch.cuda.CUDAGraph()
+    out.zero_()
+    with torch.cuda.graph(g):
+        da.decode_attn_splitkv_varsplit(q, k, v, cu, out, ws, split_len=256, max_splits=12, scale=p.scale)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
