@@ -283,6 +283,20 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// log2(x) on the SFU (lg2.approx; relative error about 2^-22).
+__device__ __forceinline__ float fast_log2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// 1/x on the SFU (rcp.approx; within one ulp).
+__device__ __forceinline__ float fast_rcp(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ int ld_cg_s32(const int32_t* p) {
     int v;
     asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p));
@@ -379,6 +393,7 @@ __device__ __forceinline__ ItemSlot decode_item(const SplitParams& p, int idx, c
 // h = h0 + c % G, row = (b * tq + t) * Hq + h.
 __device__ __forceinline__ int64_t column_row(const SplitParams& p, const ItemSlot& it, int c) {
     const int cg = it.c0 + c;
+    if (p.tq == 1) return static_cast<int64_t>(it.b) * p.Hq + it.h0 + cg;   // token 0: cg < G
     return (static_cast<int64_t>(it.b) * p.tq + cg / p.G) * p.Hq + it.h0 + cg % p.G;
 }
 
@@ -467,20 +482,22 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
         if (lane == 0) {
             int st = 0;          // ring position of the next tile
             uint32_t ph = 0;     // its phase parity
-            int idx = static_cast<int>(blockIdx.x);   // the first item of each CTA is its own index
-            for (uint32_t it = 0;; ++it) {
+            // Put work item `idx` in descriptor slot `it % kItemSlots` and start the
+            // copy of its Q rows. Returns 1 for an item, 0 at the end of the queue
+            // (the slot then says so), -1 when the wait for a free slot timed out.
+            auto publish = [&](uint32_t it, int idx, ItemSlot& item) -> int {
                 const int slot = it % kItemSlots;
                 const uint32_t iph = (it / kItemSlots) & 1;
                 if (!mbar_wait(iempty0 + 8 * slot, iph ^ 1, p.wait_limit_ns)) {
                     flag_error(p.err, DA_DEVERR_TIMEOUT);
-                    break;
+                    return -1;
                 }
                 if (idx >= n_items) {
                     slots[slot].valid = 0;
                     mbar_arrive(ifull0 + 8 * slot);
-                    break;
+                    return 0;
                 }
-                const ItemSlot item = decode_item(p, idx, cus, prefix);
+                item = decode_item(p, idx, cus, prefix);
                 slots[slot] = item;
                 const uint32_t ib = ifull0 + 8 * slot;
                 mbar_arrive_expect_tx(ib, item.nh * D * 2);
@@ -491,6 +508,12 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
                     for (int c = 0; c < item.nh; ++c)
                         bulk_load(qbuf + slot * Sh::kQBytes + c * D * 2, p.q + column_row(p, item, c) * D, D * 2, ib);
                 }
+                return 1;
+            };
+            ItemSlot item;
+            // the first item of each CTA is its own index
+            int state = publish(0, static_cast<int>(blockIdx.x), item);
+            for (uint32_t it = 0; state == 1; ++it) {
                 // The next item is taken from the queue a few stages before this one's
                 // last tile: the atomic's round trip then overlaps the last copies, yet a
                 // CTA never holds a reserved item for long (which would hurt the balance
@@ -549,6 +572,11 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
                     }
                 }
                 if (!ok) break;
+                // The next item's descriptor and Q copy go out before this item's merge
+                // stage, so both are in place when the consumers finish the merge.
+                ItemSlot next;
+                const int next_state = publish(it + 1, next_idx, next);
+                if (next_state < 0) break;
                 // Hand the next stage to the consumers, empty, for this item's merge.
                 if (!mbar_wait(empty0 + 8 * st, ph ^ 1, p.wait_limit_ns)) {
                     flag_error(p.err, DA_DEVERR_TIMEOUT);
@@ -559,7 +587,8 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
                     st = 0;
                     ph ^= 1;
                 }
-                idx = next_idx;
+                item = next;
+                state = next_state;
             }
         }
         return;
@@ -757,27 +786,57 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
             ok = false;
             if (lane == 0) flag_error(p.err, DA_DEVERR_TIMEOUT);
         }
-        for (int idx = threadIdx.x; idx < item.nh * D; idx += kConsumerWarps * 32) {
-            const int hh = idx / D, d = idx % D;
-            float M = -INFINITY;
+        // Warp w writes heads w and w + 4; a lane owns four consecutive dims, read
+        // from each warp's row as one 16-byte load and stored as one vector. The
+        // passes are predicated rather than skipped, so their latencies overlap.
+        {
+            constexpr int kLanesPerHead = D / 4;
+            constexpr int kHeadsPerPass = 32 / kLanesPerHead;   // 1 at head_dim 128, 2 at 64
+            constexpr int kPasses = (kHeadsPerCta / kConsumerWarps) / kHeadsPerPass;
+            const int d0 = (lane % kLanesPerHead) * 4;
 #pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, red_m[w * kHeadsPerCta + hh]);
-            float o = 0.f, lsum = 0.f;
-            if (M != -INFINITY) {
+            for (int pass = 0; pass < kPasses; ++pass) {
+                const int hh = warp + kConsumerWarps * (pass * kHeadsPerPass + lane / kLanesPerHead);
+                const bool live = hh < item.nh;
+                float mw[kConsumerWarps];
+                float M = -INFINITY;
 #pragma unroll
                 for (int w = 0; w < kConsumerWarps; ++w) {
-                    const float wt = fast_exp2(red_m[w * kHeadsPerCta + hh] - M);
-                    lsum += wt * red_l[w * kHeadsPerCta + hh];
-                    o += wt * red_acc[(w * kHeadsPerCta + hh) * Sh::kMergeRow + d];
+                    mw[w] = red_m[w * kHeadsPerCta + hh];
+                    M = fmaxf(M, mw[w]);
                 }
-                o = o / lsum;
+                // a head that saw no key keeps M = -inf: weights 0, output 0, lse -inf
+                const float Ms = M == -INFINITY ? 0.f : M;
+                float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+                float lsum = 0.f;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) {
+                    const float wt = fast_exp2(mw[w] - Ms);
+                    lsum = fmaf(wt, red_l[w * kHeadsPerCta + hh], lsum);
+                    const float4 a = *reinterpret_cast<const float4*>(
+                        red_acc + (w * kHeadsPerCta + hh) * Sh::kMergeRow + d0);
+                    o.x = fmaf(wt, a.x, o.x);
+                    o.y = fmaf(wt, a.y, o.y);
+                    o.z = fmaf(wt, a.z, o.z);
+                    o.w = fmaf(wt, a.w, o.w);
+                }
+                // lsum >= 1 whenever M is finite (the largest score weighs 1)
+                const float inv = M == -INFINITY ? 0.f : fast_rcp(lsum);
+                o.x *= inv;
+                o.y *= inv;
+                o.z *= inv;
+                o.w *= inv;
+                if (live) {
+                    const int64_t qrow = column_row(p, item, hh);
+                    const int64_t row = qrow * p.S + item.s;
+                    *reinterpret_cast<float4*>(p.opart + row * D + d0) = o;
+                    if (d0 == 0) p.lse[row] = M == -INFINITY ? -INFINITY : (M + fast_log2(lsum)) * kLn2;
+                    // one split: its weight exp(lse_0 - lse) is 1, so o_0 is the answer
+                    if (p.out != nullptr)
+                        *reinterpret_cast<uint2*>(p.out + qrow * D + d0) =
+                            make_uint2(pack2<DT>(o.x, o.y), pack2<DT>(o.z, o.w));
+                }
             }
-            const int64_t qrow = column_row(p, item, hh);
-            const int64_t row = qrow * p.S + item.s;
-            p.opart[row * D + d] = o;
-            if (d == 0) p.lse[row] = M == -INFINITY ? -INFINITY : (M + log2f(lsum)) * kLn2;
-            // one split: its weight exp(lse_0 - lse) is 1, so o_0 is the answer
-            if (p.out != nullptr) p.out[qrow * D + d] = to_bits<DT>(o);
         }
         // release the stage: order these generic-proxy stores before the TMA writes that refill it
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
