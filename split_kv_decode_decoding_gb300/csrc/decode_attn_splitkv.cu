@@ -853,12 +853,13 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
         if (bad_bar != 0) mbar_wait(bad_bar, bad_ph, p.wait_limit_ns);
         return;
     }
-    // The last CTA to finish re-arms the work queue for the next call.
+    // The last CTA to finish re-arms the work queue for the next call. No fence:
+    // the counters order no data (the outputs are read only after this grid
+    // completes), and every CTA's last queue atomic has returned before its
+    // producer published the end of the queue, which precedes this increment.
     if (threadIdx.x == 0) {
-        __threadfence();
         const uint32_t prev = atomicAdd(p.done, 1u);
         if (prev == gridDim.x - 1) {
-            __threadfence();
             atomicExch(p.work, 0u);
             atomicExch(p.done, 0u);
         }
