@@ -110,13 +110,20 @@ da_status decode_attn_splitkv_workspace_init(void* workspace, size_t workspace_b
 /*
  * Split-count picker (host only, enqueues nothing). Chooses num_splits for a
  * batch whose KV lengths lie in [min_kv, max_kv]. The split step has
- * B * Hkv * ceil(G/8) * num_splits work items. For even lengths it aims at
- * about one item per SM with splits of 256 to 1024 keys; for ragged lengths
- * (max_kv >= 2 * min_kv) at about eight items per SM, so the work queue can
- * balance unequal splits. No split is ever empty (num_splits <= min_kv; the
- * TileLang page's scheduling constraint, split kernel docstring). sm_count 0
- * means: query the current device. Returns a value in [1, DA_MAX_SPLITS]; 1
- * when min_kv <= 0 or an argument is out of range.
+ * U * num_splits work items, U = B * Hkv * ceil(G/8), run by R = sm_count *
+ * (2 at head_dim 128, 4 at 64) persistent CTAs.
+ *   Even lengths (max_kv < 2 * min_kv), U >= 0.8 * sm_count: 1, unless the
+ *     K/V stream exceeds 1.5e9 bytes; then round(1.68 * R / U), about 1.7 waves
+ *     of items, so the work queue evens out unequal SM rates.
+ *   Even lengths, fewer units: about one item per SM, ceil(sm_count / U),
+ *     with splits of 256 to 1024 keys.
+ *   Ragged lengths: about eight items per SM (splits of at least 64 keys),
+ *     raised until the longest sequence's splits are at most twice one CTA's
+ *     share of a lower bound of the total keys (max_kv + (B-1) * min_kv).
+ * No split is ever empty (num_splits <= min_kv; the TileLang page's scheduling
+ * constraint, split kernel docstring). sm_count 0 means: query the current
+ * device. Returns a value in [1, DA_MAX_SPLITS]; 1 when min_kv <= 0 or an
+ * argument is out of range.
  */
 int decode_attn_splitkv_num_splits(int B, int Hq, int Hkv, int D, int min_kv, int max_kv,
                                    int sm_count);

@@ -1109,6 +1109,7 @@ struct Call {
 };
 
 constexpr int kMaxVarsplitBatch = 1024;                                   // sequences, per-sequence mode
+constexpr double kLongStreamBytes = 1.5e9;   // K/V bytes above which even batches are split for balance
 
 // `out` is written by the split kernel itself only with one uniform split.
 template <int D, int DT>
@@ -1295,20 +1296,35 @@ int decode_attn_splitkv_num_splits(int B, int Hq, int Hkv, int D, int min_kv, in
     }
     const int64_t chunks = (Hq / Hkv + kHeadsPerCta - 1) / kHeadsPerCta;
     const int64_t units = static_cast<int64_t>(B) * Hkv * chunks;   // (sequence, KV head, chunk)
-    int64_t target, min_len;
+    const int64_t slots = static_cast<int64_t>(sm_count) * (D == 128 ? 2 : 4);   // persistent CTAs
+    int64_t S;
     if (2 * static_cast<int64_t>(min_kv) <= max_kv) {
-        // Ragged lengths: about four items per resident CTA (two per SM), so the
-        // work queue can even out splits of unequal length; splits may be short.
-        target = 8 * static_cast<int64_t>(sm_count);
-        min_len = 64;
+        // Ragged lengths: about eight items per SM, so the work queue can even
+        // out splits of unequal length; splits may be short ...
+        S = (8 * static_cast<int64_t>(sm_count) + units - 1) / units;
+        S = std::min<int64_t>(S, std::max<int64_t>(1, min_kv / 64));
+        // ... and the longest sequence's splits at most about twice one CTA's
+        // share of the keys (the share taken from a lower bound of the total),
+        // so that no single split outlasts the rest of the batch.
+        const double total = static_cast<double>(max_kv) + static_cast<double>(B - 1) * min_kv;
+        const double share = total * Hkv * chunks / static_cast<double>(slots);
+        S = std::max<int64_t>(S, static_cast<int64_t>(std::ceil(max_kv / (2.0 * share))));
+    } else if (5 * units >= 4 * static_cast<int64_t>(sm_count)) {
+        // Even lengths, about one unit per SM or more: one split (no combine)
+        // while the stream is short; for a long stream about 1.7 waves of items,
+        // so the work queue evens out the SMs' unequal rates and the last wave
+        // still keeps a third of the CTAs busy.
+        const double kv_bytes = static_cast<double>(B) * Hkv * min_kv * 4.0 * D;
+        S = kv_bytes <= kLongStreamBytes ? 1 : std::max<int64_t>(1, std::llround(1.68 * slots / units));
     } else {
-        // Even lengths: about one item per SM, each split long enough (256 to
-        // 1024 keys) that its start-up and merge stay small next to its stream.
-        target = sm_count;
-        min_len = std::min<int64_t>(1024, std::max<int64_t>(256, static_cast<int64_t>(min_kv) * units / sm_count));
+        // Even lengths, fewer units than SMs: about one item per SM, each split
+        // long enough (256 to 1024 keys) that its start-up and merge stay small
+        // next to its stream.
+        S = (static_cast<int64_t>(sm_count) + units - 1) / units;
+        const int64_t min_len =
+            std::min<int64_t>(1024, std::max<int64_t>(256, static_cast<int64_t>(min_kv) * units / sm_count));
+        S = std::min<int64_t>(S, std::max<int64_t>(1, min_kv / min_len));
     }
-    int64_t S = (target + units - 1) / units;
-    S = std::min<int64_t>(S, std::max<int64_t>(1, min_kv / min_len));
     // never an empty split (the TileLang page's num_splits <= min_kv rule)
     S = std::min<int64_t>(S, min_kv);
     S = std::max<int64_t>(1, std::min<int64_t>(S, DA_MAX_SPLITS));

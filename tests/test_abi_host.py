@@ -76,12 +76,30 @@ def test_picker_properties(lib, shape):
         assert 1 <= S <= min(mn, da.DA_MAX_SPLITS)
         assert S == da.num_splits(B, Hq, Hkv, D, mn, mx, sm)
         units = B * Hkv * math.ceil(Hq // Hkv / 8)
-        # never more splits than needed for about eight items per SM
-        assert units * (S - 1) < 8 * sm
+        slots = sm * (2 if D == 128 else 4)
         if 2 * mn > mx:
-            # even lengths: about one item per SM, splits of at least 256 keys
-            assert units * (S - 1) < sm
-            assert S == 1 or mn // S >= 256
+            if 5 * units >= 4 * sm:
+                # enough units for one wave: one split, or about 1.7 waves for a long stream
+                kv_bytes = B * Hkv * mn * 4 * D
+                assert S == (1 if kv_bytes <= 1.5e9 else max(1, round(1.68 * slots / units)))
+            else:
+                # about one item per SM, splits of at least 256 keys
+                assert units * (S - 1) < sm
+                assert S == 1 or mn // S >= 256
+        else:
+            # eight items per SM, or as many as keep the longest splits near two CTA shares
+            share = (mx + (B - 1) * mn) * Hkv * math.ceil(Hq // Hkv / 8) / slots
+            assert units * (S - 1) < 8 * sm or S == math.ceil(mx / (2 * share))
+
+
+def test_picker_choices_on_measured_workloads(lib):
+    """Split counts the picker gives for shapes whose best split count was measured on a GB300."""
+    sm = 152
+    assert da.num_splits(16, 32, 8, 128, 8192, 8192, sm) == 1        # one wave of 128 items, no combine
+    assert da.num_splits(16, 32, 8, 128, 32768, 32768, sm) == 4      # 2.1 GB stream: 512 items
+    assert da.num_splits(16, 32, 8, 128, 131072, 131072, sm) == 4
+    assert da.num_splits(8, 32, 32, 128, 4096, 4096, sm) == 1
+    assert 16 <= da.num_splits(16, 32, 8, 128, 512, 131072, sm) <= 24   # one 128K sequence among 512s
 
 
 def test_picker_degenerate(lib):
