@@ -310,15 +310,18 @@ da_status decode_attn_splitkv_noalloc(const void* q, const void* k, const void* 
  * (04_flash_decoding.py, decode_attention_time, best_splits; its A100/H100
  * constants are not on the page) for this library's persistent kernel:
  *
- *   T = t0 + max(W / bw, makespan) + [S > 1] * (t_comb + W_ws / bw_comb)
+ *   T = t0 + makespan + kappa * B_max / (bw / min(n_items, R))
+ *         + [S > 1] * (t_comb + W_ws / bw_comb)
  *
- * W: K/V bytes streamed (each split's keys rounded up to 16, times 4*D bytes);
- * makespan: greedy list schedule of the work items, in queue order, over
- * (2 at D = 128, 4 at D = 64) * sm_count persistent CTAs, item cost
- * t_item + bytes / r_cta; W_ws = B*T_q*Hq*S*(D+1)*4 workspace bytes combined.
+ * makespan: a processor-sharing run of the n_items work items, in queue order,
+ * over R = (2 at D = 128, 4 at D = 64) * sm_count persistent CTAs; before each
+ * item a CTA spends t_item, then streams the item's K/V bytes (its keys rounded
+ * up to 16, times 4*D) at min(r_cta, bw / number of CTAs streaming). B_max: the
+ * largest item's bytes (kappa charges the last item for unequal CTA rates);
+ * W_ws = B*T_q*Hq*S*(D+1)*4 workspace bytes combined.
  *   kv_lens   host, int32 [B] sequence lengths (negative counts as 0)
- *   params    host, double[6] {t0 us, t_item us, r_cta B/us, bw B/us, t_comb us,
- *             bw_comb B/us}, or NULL for the built-in GB300 calibration
+ *   params    host, double[7] {t0 us, t_item us, r_cta B/us, bw B/us, t_comb us,
+ *             bw_comb B/us, kappa}, or NULL for the built-in GB300 calibration
  * Returns the predicted time, or a negative value if an argument is out of range.
  */
 double decode_attn_splitkv_model_us(const int32_t* kv_lens, int B, int Hq, int Hkv, int D, int T_q,

@@ -57,6 +57,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <queue>
 
 #include "decode_attn_splitkv.h"
 
@@ -1487,22 +1488,25 @@ const char* decode_attn_splitkv_status_string(da_status status) {
 // A GB300 restatement of the lecture page's decode time model
 // (04_flash_decoding.py: decode_attention_time / best_splits, whose A100/H100
 // constants are not on the page): the call is modelled as
-//   T = t0 + max(W / bw, makespan) + [S > 1] (t_comb + W_ws / bw_comb)
-// where W is the K/V bytes streamed (each split's key count rounded up to the
-// 16-key TMA box), makespan is the greedy list schedule of the work items, in
-// queue order, over the persistent CTAs, each item costing t_item + bytes / r_cta,
-// and W_ws the workspace bytes the combine reads. The parameters were fitted
-// (least squares in log time) to 230 calls measured on one GB300: 14 workloads
-// of the CodeLlama, Llama and Qwen shapes, split counts 1 to 256, L2 flushed,
-// CUDA-event time per call; median error 3.4 %, 90th percentile 11 %.
+//   T = t0 + makespan + kappa * (largest item's bytes) / (bw / min(items, CTAs))
+//         + [S > 1] (t_comb + W_ws / bw_comb)
+// where makespan is a processor-sharing run of the work items, in queue order,
+// over the persistent CTAs: each CTA spends t_item before an item and then
+// streams its bytes (each split's key count rounded up to the 16-key TMA box)
+// at min(r_cta, bw / streaming CTAs); kappa charges the last item for the CTAs'
+// unequal rates, and W_ws is the workspace bytes the combine reads. Fitted (least
+// squares in log time) on one GB300 to the 203 calls, of 357 measured (17
+// workloads of the CodeLlama, Llama, Qwen and MHA shapes x split counts 1 to
+// 256, L2 flushed, CUDA-event median per call), that lie within 30 % of their
+// workload's fastest split count: median error 2.6 %, 90th percentile 6.1 %.
 static const double kModelGb300[7] = {
-    /* t0 us      */ 14.17,
-    /* t_item us  */ 1.300,
-    /* r_cta B/us */ 73315,
-    /* bw B/us    */ 7.277e+06,
-    /* t_comb us  */ 0.979,
-    /* bw_comb    */ 3.537e+05,
-    /* unused     */ 0.0};
+    /* t0 us      */ 13.73,
+    /* t_item us  */ 0.2623,
+    /* r_cta B/us */ 72540,
+    /* bw B/us    */ 7.459e+06,
+    /* t_comb us  */ 0.07119,
+    /* bw_comb    */ 1.083e+06,
+    /* kappa      */ 0.04376};
 
 double decode_attn_splitkv_model_us(const int32_t* kv_lens, int B, int Hq, int Hkv, int D, int T_q, int num_splits,
                                     int sm_count, const double* params) {
@@ -1510,35 +1514,67 @@ double decode_attn_splitkv_model_us(const int32_t* kv_lens, int B, int Hq, int H
         num_splits < 1 || num_splits > DA_MAX_SPLITS || sm_count < 1)
         return -1.0;
     const double* m = params ? params : kModelGb300;
-    const double t0 = m[0], t_item = m[1], r_cta = m[2], bw = m[3], t_comb = m[4], bw_comb = m[5];
-    if (!(r_cta > 0) || !(bw > 0) || !(bw_comb > 0)) return -1.0;
+    const double t0 = m[0], t_item = m[1], r_cta = m[2], bw = m[3], t_comb = m[4], bw_comb = m[5], kappa = m[6];
+    if (!(r_cta > 0) || !(bw > 0) || !(bw_comb > 0) || !(t_item >= 0) || !(kappa >= 0)) return -1.0;
     const int S = num_splits;
     const int chunks = (Hq / Hkv * T_q + kHeadsPerCta - 1) / kHeadsPerCta;
     const int slots = sm_count * (D == 128 ? 2 : 4);
     const double key_bytes = 4.0 * D;   // K and V rows of one key and KV head
-    // greedy list schedule: a min-heap of slot free times
-    std::vector<double> heap(static_cast<size_t>(slots), 0.0);
-    auto take = [&](double cost) {
-        std::pop_heap(heap.begin(), heap.end(), std::greater<double>());
-        heap.back() += cost;
-        std::push_heap(heap.begin(), heap.end(), std::greater<double>());
-    };
-    double W = 0.0;
+    // the work items in queue order: the bytes each streams (later chunks of a
+    // split re-read its keys from L2 and are not counted in W)
+    std::vector<double> items;
+    double W = 0.0, biggest = 0.0;
     for (int b = 0; b < B; ++b) {
         const int64_t L = kv_lens[b] < 0 ? 0 : kv_lens[b];
         for (int kvh = 0; kvh < Hkv; ++kvh)
             for (int s = 0; s < S; ++s) {
                 const int64_t n = L * (s + 1) / S - L * s / S;
                 const double bytes = static_cast<double>((n + kBoxKeys - 1) / kBoxKeys * kBoxKeys) * key_bytes;
-                for (int c = 0; c < chunks; ++c) {
-                    W += c == 0 ? bytes : 0.0;   // later chunks of a split re-read it from L2
-                    take(t_item + bytes / r_cta);
-                }
+                biggest = std::max(biggest, bytes);
+                W += bytes;
+                for (int c = 0; c < chunks; ++c) items.push_back(bytes);
             }
     }
-    const double makespan = *std::max_element(heap.begin(), heap.end());
-    double t = t0 + std::max(W / bw, makespan);
+    // Processor sharing: every CTA that is streaming gets min(r_cta, bw / streaming)
+    // bytes per us; before each item a CTA spends t_item not streaming. All
+    // streaming CTAs advance together, so their progress is one "virtual bytes"
+    // clock V and a CTA's stream ends at a fixed V.
+    using Ev = std::pair<double, int>;
+    std::priority_queue<Ev, std::vector<Ev>, std::greater<Ev>> streams;    // (V at end, cta)
+    std::priority_queue<Ev, std::vector<Ev>, std::greater<Ev>> overheads;  // (time at end, cta)
+    size_t next = 0;
+    double now = 0.0, V = 0.0;
+    for (int c = 0; c < slots && next < items.size(); ++c) overheads.push({t_item, c}), ++next;
+    std::vector<double> pending(static_cast<size_t>(slots), 0.0);   // bytes of the item a CTA prepares
+    for (int c = 0; c < slots && c < static_cast<int>(items.size()); ++c) pending[c] = items[c];
+    while (!streams.empty() || !overheads.empty()) {
+        const double rate = streams.empty() ? 0.0 : std::min(r_cta, bw / static_cast<double>(streams.size()));
+        const double t_stream = streams.empty() ? INFINITY : now + (streams.top().first - V) / rate;
+        const double t_over = overheads.empty() ? INFINITY : overheads.top().first;
+        if (t_stream <= t_over) {
+            V = streams.top().first;
+            now = t_stream;
+            const int c = streams.top().second;
+            streams.pop();
+            if (next < items.size()) {
+                pending[c] = items[next++];
+                overheads.push({now + t_item, c});
+            }
+        } else {
+            V += rate * (t_over - now);
+            now = t_over;
+            const int c = overheads.top().second;
+            overheads.pop();
+            streams.push({V + pending[c], c});
+        }
+    }
+    const double makespan = now;
+    // CTAs stream at unequal rates; the work queue evens them out except over
+    // the last item, which costs a fraction kappa of its time at the fair share
+    const double fair = bw / static_cast<double>(std::max<size_t>(1, std::min<size_t>(items.size(), slots)));
+    double t = t0 + makespan + kappa * biggest / fair;
     if (S > 1) t += t_comb + static_cast<double>(B) * T_q * Hq * S * (D + 1) * 4.0 / bw_comb;
+    (void)W;
     return t;
 }
 

@@ -226,16 +226,24 @@ def test_time_model_formula_by_hand(lib):
 
     L = 1000, S = 2: splits of 500 keys, rounded up to 512 (16-key boxes), 4*128 = 512 B
     per key -> 262144 B each. With t0 = 5, t_item = 1, r_cta = 65536 B/us, bw = 1e6,
-    t_comb = 2, bw_comb = 1e6: two items on two free CTAs, each 1 + 4 = 5 us, so the
-    makespan is 5 us; W / bw = 0.524 us; workspace 1*1*1*2*129*4 = 1032 B.
-    T = 5 + 5 + 2 + 0.001032 = 12.001032 us.
+    t_comb = 2, bw_comb = 1e6, kappa = 0.5: two items on two free CTAs; each CTA waits
+    t_item = 1 us, then the two stream together at min(65536, 1e6 / 2) = 65536 B/us for
+    4 us, so the makespan is 5 us. The last-item term is 0.5 * 262144 / (1e6 / 2) =
+    0.262144 us; workspace 1*1*1*2*129*4 = 1032 B. T = 5 + 5 + 0.262144 + 2 + 0.001032.
     """
-    params = [5.0, 1.0, 65536.0, 1e6, 2.0, 1e6]
+    params = [5.0, 1.0, 65536.0, 1e6, 2.0, 1e6, 0.5]
     t = da.model_us([1000], 1, 1, 128, 2, 152, params=params)
-    assert abs(t - 12.001032) < 1e-9
-    # one split: no combine term, one 1008-key item (1000 rounded up): 1 + 1008*512/65536
+    assert abs(t - (5 + 5 + 0.262144 + 2 + 0.001032)) < 1e-9
+    # one split: no combine term, one 1008-key item (1000 rounded up): 1 + 1008*512/65536,
+    # last-item term 0.5 * 516096 / 1e6
     t1 = da.model_us([1000], 1, 1, 128, 1, 152, params=params)
-    assert abs(t1 - (5 + 1 + 1008 * 512 / 65536)) < 1e-9
+    assert abs(t1 - (5 + 1 + 1008 * 512 / 65536 + 0.5 * 516096 / 1e6)) < 1e-9
+    # bandwidth-bound: four items streaming together share bw = 1e5 B/us (25000 each,
+    # below r_cta): 1 + 262144 / 25000 us; last-item term 0.5 * 262144 / 25000; the
+    # combine reads 2*1*2*129*4 = 2064 B
+    params_bw = [5.0, 1.0, 65536.0, 1e5, 2.0, 1e6, 0.5]
+    t4 = da.model_us([1000, 1000], 1, 1, 128, 2, 152, params=params_bw)
+    assert abs(t4 - (5 + 1 + 262144 / 25000 + 0.5 * 262144 / 25000 + 2 + 0.002064)) < 1e-9
 
 
 def test_time_model_properties(lib):
