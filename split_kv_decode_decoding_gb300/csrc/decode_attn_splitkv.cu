@@ -69,6 +69,7 @@ constexpr int kConsumerWarps = 4;   // each owns 16 keys of a stage
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kHeadsPerCta = 8;     // mma N: packed query heads per item
 constexpr int kStages = 3;          // pipeline depth (two CTAs per SM at head_dim 128)
+constexpr int kPrefetchStages = 4;  // BHSD: first stages pulled into L2 while cu_seqlens_k is read
 constexpr int kMinBlocksPerSm = 2;
 constexpr int kItemSlots = 2;       // item descriptors the producer may run ahead
 constexpr size_t kHeaderBytes = 256;
@@ -204,6 +205,14 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
         : "memory");
+}
+
+// Pull one tile of a tensor into L2 (no shared-memory destination, no barrier).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
@@ -449,6 +458,21 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
     if (warp == kConsumerWarps) {
         // ---------------- producer: one lane takes items and issues every copy
         int n_items = p.n_items;
+        if (lane == 0 && p.layout == DA_LAYOUT_BHSD && p.no_kv == 0 && p.split_len == 0 &&
+            static_cast<int>(blockIdx.x) < n_items) {
+            // This CTA's first item is its own index. When that is a sequence's first
+            // split, its keys start at position 0 of its slab whatever the length:
+            // start pulling its first stages into L2 while cu_seqlens_k is read.
+            const int r = static_cast<int>(blockIdx.x) / p.chunks;   // (b * Hkv + kvh) * S + s
+            if (r % p.S == 0) {
+                const int slab = r / p.S;
+                for (int t = 0; t < kPrefetchStages; ++t)
+                    for (int hf = 0; hf < Sh::kHalves; ++hf) {
+                        tma_prefetch_3d(&tmK, hf * 64, t * kStageKeys, slab);
+                        tma_prefetch_3d(&tmV, hf * 64, t * kStageKeys, slab);
+                    }
+            }
+        }
         if (cus != nullptr) {
             // one coalesced read of cu_seqlens_k per CTA; every item is then decoded from shared memory
             for (int i = lane; i <= p.B; i += 32) cus[i] = ld_cg_s32(p.cu + i);
