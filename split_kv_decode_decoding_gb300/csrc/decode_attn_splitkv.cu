@@ -67,7 +67,7 @@ constexpr int kBoxKeys = 16;        // keys per TMA box = rows of one mma m-tile
 constexpr int kStageKeys = 64;      // keys per pipeline stage
 constexpr int kConsumerWarps = 4;   // each owns 16 keys of a stage
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kHeadsPerCta = 8;     // mma N: packed query heads per item
+constexpr int kHeadsPerCta = 8;     // mma N: packed (token, head) columns per n-tile
 constexpr int kStages = 3;          // pipeline depth (two CTAs per SM at head_dim 128)
 constexpr int kPrefetchStages = 4;  // BHSD: first stages pulled into L2 while cu_seqlens_k is read
 constexpr int kMinBlocksPerSm = 2;
@@ -90,7 +90,16 @@ struct ItemSlot {          // one work item, as the producer decoded it
 };
 static_assert(sizeof(ItemSlot) == 48, "ItemSlot layout");
 
-template <int D>
+// Columns (packed query token x head pairs) of one work item: one n-tile of 8,
+// or two when a KV head serves more than 8 columns, so that K and V are read
+// and multiplied once for up to 16 columns.
+inline int item_cols(int64_t cols) { return cols > kHeadsPerCta ? 2 * kHeadsPerCta : kHeadsPerCta; }
+inline int64_t item_chunks(int64_t cols) {
+    const int c = item_cols(cols);
+    return (cols + c - 1) / c;
+}
+
+template <int D, int NT>
 struct Shape {
     static constexpr int kHalves = D / 64;                         // 128-byte column slices
     static constexpr int kSliceBytes = kStageKeys * 128;           // one slice of a stage tile
@@ -105,11 +114,11 @@ struct Shape {
     static constexpr int kMergeRow = D + 4;
     static constexpr int kMergeBytes = (kConsumerWarps * kHeadsPerCta * kMergeRow + 2 * kConsumerWarps * kHeadsPerCta) * 4;
     static_assert(kMergeBytes <= kStageBytes, "item merge must fit in one ring stage");
-    static constexpr int kQBytes = kHeadsPerCta * D * 2;           // Q rows of one item
+    static constexpr int kQBytes = NT * kHeadsPerCta * D * 2;      // Q rows of one item
     static constexpr int kQOff = kRingBytes;
     static constexpr int kSlotOff = kQOff + kItemSlots * kQBytes;
     static constexpr int kBarOff = kSlotOff + kItemSlots * (int)sizeof(ItemSlot);
-    static constexpr int kNumBars = 2 * kStages + 2 * kItemSlots + 1;
+    static constexpr int kNumBars = 2 * kStages + 2 * kItemSlots + 1 + (NT > 1 ? 1 : 0);
     static constexpr int kEnd = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = 1024 /* alignment slack */ + kEnd;
     static_assert(kQOff % 16 == 0 && kSlotOff % 16 == 0 && kBarOff % 8 == 0, "smem alignment");
@@ -350,6 +359,7 @@ __device__ __forceinline__ int seq_splits(int64_t L, int split_len, int max_spli
 // With per-sequence split counts, `prefix` holds the running sum of S_b
 // (prefix[b] splits before sequence b) and the sequence is found by binary
 // search.
+template <int kCols>
 __device__ __forceinline__ ItemSlot decode_item(const SplitParams& p, int idx, const int32_t* cus,
                                                 const int32_t* prefix) {
     ItemSlot it;
@@ -380,8 +390,8 @@ __device__ __forceinline__ ItemSlot decode_item(const SplitParams& p, int idx, c
         it.kvh = r / Sb;
     }
     it.h0 = it.kvh * p.G;
-    it.c0 = chunk * kHeadsPerCta;
-    it.nh = min(kHeadsPerCta, p.G * p.tq - it.c0);
+    it.c0 = chunk * kCols;
+    it.nh = min(kCols, p.G * p.tq - it.c0);
     int64_t base;
     bool bad;
     const int64_t L = cus != nullptr
@@ -408,12 +418,12 @@ __device__ __forceinline__ int64_t column_row(const SplitParams& p, const ItemSl
 }
 
 // ------------------------------------------------------------ split step
-template <int D, int DT>
+template <int D, int DT, int NT>
 __global__ void __launch_bounds__(kThreads, kMinBlocksPerSm)
 split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
              const __grid_constant__ CUtensorMap tmK16, const __grid_constant__ CUtensorMap tmV16,
              const SplitParams p) {
-    using Sh = Shape<D>;
+    using Sh = Shape<D, NT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -425,6 +435,7 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
     const uint32_t ifull0 = empty0 + 8 * kStages;       // [kItemSlots]
     const uint32_t iempty0 = ifull0 + 8 * kItemSlots;   // [kItemSlots]
     const uint32_t mfull = iempty0 + 8 * kItemSlots;    // an item's per-warp partials written
+    const uint32_t mdone = mfull + 8;                   // two n-tiles: a merge round's rows all read
     // past the fixed layout: cu_seqlens_k [B + 1] (when staged), then prefix[B + 1] (per-sequence mode)
     int32_t* cus = p.stage_cu ? reinterpret_cast<int32_t*>(smem + Sh::kEnd) : nullptr;
     int32_t* prefix = reinterpret_cast<int32_t*>(smem + Sh::kEnd + (p.stage_cu ? kStagedBytes : 0));
@@ -441,6 +452,7 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
             mbar_init(iempty0 + 8 * i, kConsumerWarps);
         }
         mbar_init(mfull, kConsumerWarps);
+        if constexpr (NT > 1) mbar_init(mdone, kConsumerWarps);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == kConsumerWarps && lane == 0 && p.no_kv == 0) {
@@ -522,7 +534,7 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
                     mbar_arrive(ifull0 + 8 * slot);
                     return 0;
                 }
-                item = decode_item(p, idx, cus, prefix);
+                item = decode_item<NT * kHeadsPerCta>(p, idx, cus, prefix);
                 slots[slot] = item;
                 const uint32_t ib = ifull0 + 8 * slot;
                 mbar_arrive_expect_tx(ib, item.nh * D * 2);
@@ -631,6 +643,7 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
     int st = 0;          // ring position of the next tile
     uint32_t ph = 0;     // its phase parity
 
+    uint32_t mz = 0, md = 0;   // two n-tiles: phases used of mfull and mdone
     uint32_t it = 0;
     for (;; ++it) {
         const int slot = it % kItemSlots;
@@ -641,225 +654,491 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
             break;
         }
         const ItemSlot item = slots[slot];
-        // Q^T fragments (B operand, k16 x n8): head g, dims ks*16 + 2*t4 (+1) and +8 (+9).
-        uint32_t qf[D / 16][2];
-        {
-            const bool hv = g < item.nh;
-            const uint32_t qrow = qbuf + slot * Sh::kQBytes + (hv ? g : 0) * D * 2;
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                uint32_t a0, a1;
-                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(a0) : "r"(qrow + (ks * 16 + 2 * t4) * 2));
-                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(a1) : "r"(qrow + (ks * 16 + 8 + 2 * t4) * 2));
-                qf[ks][0] = hv ? a0 : 0u;
-                qf[ks][1] = hv ? a1 : 0u;
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(iempty0 + 8 * slot);
-        if (!item.valid) break;
-
-        // keys (relative to the split start) visible to this thread's two columns
-        int visA = item.nkeys, visB = item.nkeys;
-        if (p.tq > 1) {
-            visA = min(item.nkeys, item.vis0 + (item.c0 + 2 * t4) / p.G);
-            visB = min(item.nkeys, item.vis0 + (item.c0 + 2 * t4 + 1) / p.G);
-        }
-        float acc[D / 16][4];
-#pragma unroll
-        for (int i = 0; i < D / 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-        float m_run[2] = {-INFINITY, -INFINITY};   // heads 2*t4, 2*t4+1 (log2 domain)
-        float l_run[2] = {0.f, 0.f};               // this thread's share of the running sum
-
-        for (int t = 0; t < item.ntiles; ++t) {
-            const uint32_t fb = full0 + 8 * st;
-            if (ok && !mbar_wait_warp(fb, ph, p.wait_limit_ns)) {
-                ok = false;
-                bad_bar = fb;
-                bad_ph = ph;
-                if (lane == 0) flag_error(p.err, DA_DEVERR_TIMEOUT);
-            }
-            const int keys_t = min(kStageKeys, item.nkeys - t * kStageKeys);
-            bool zeroed = false;
-            if (ok && warp * kBoxKeys < keys_t) {
-                const uint32_t kbase = ring + st * Sh::kStageBytes;
-                const uint32_t vbase = kbase + Sh::kTileBytes;
-                const int valid_rows = keys_t - warp * kBoxKeys;
-                if (valid_rows < kBoxKeys) {
-                    // The box's rows past the split end hold other keys (or, in a
-                    // padded cache, anything): their P is 0, but 0 * NaN is not, so
-                    // clear those V rows before the PV product.
-                    const int per_row = Sh::kHalves * 8;   // 16-byte chunks per row
-                    for (int c = lane; c < (kBoxKeys - valid_rows) * per_row; c += 32) {
-                        const int r = valid_rows + c / per_row;
-                        const int hf = (c % per_row) >> 3, ch = c & 7;
-                        const uint32_t addr = vbase + hf * Sh::kSliceBytes + (warp * kBoxKeys + r) * 128 + ch * 16;
-                        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
-                    }
-                    zeroed = true;
-                    __syncwarp();
-                }
-                // S^T[16 keys, 8 heads] = K_tile . Q^T, two independent accumulator chains
-                float sc[4] = {0.f, 0.f, 0.f, 0.f};
-                float sd[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
+        if constexpr (NT == 1) {
+        // ---- one n-tile (up to 8 columns per item)
+            // Q^T fragments (B operand, k16 x n8): head g, dims ks*16 + 2*t4 (+1) and +8 (+9).
+            uint32_t qf[D / 16][2];
+            {
+                const bool hv = g < item.nh;
+                const uint32_t qrow = qbuf + slot * Sh::kQBytes + (hv ? g : 0) * D * 2;
+    #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
-                    const int chunk16 = ks * 2 + kchunk_add;          // 16-byte chunk along D
-                    const uint32_t addr = kbase + (chunk16 >> 3) * Sh::kSliceBytes + krow * 128 +
-                                          (((chunk16 & 7) ^ (krow & 7)) << 4);
-                    uint32_t a[4];
-                    ldsm_x4(addr, a);
-                    if (ks & 1) mma_16816<DT>(sd, a, qf[ks][0], qf[ks][1]);
-                    else mma_16816<DT>(sc, a, qf[ks][0], qf[ks][1]);
+                    uint32_t a0, a1;
+                    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(a0) : "r"(qrow + (ks * 16 + 2 * t4) * 2));
+                    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(a1) : "r"(qrow + (ks * 16 + 8 + 2 * t4) * 2));
+                    qf[ks][0] = hv ? a0 : 0u;
+                    qf[ks][1] = hv ? a1 : 0u;
                 }
-                // scores -> exp2 domain, mask keys past the split end
-                const int key_lo = t * kStageKeys + warp * kBoxKeys + g;   // relative to split start
-                const float x0 = key_lo < visA ? (sc[0] + sd[0]) * p.scale_log2 : -INFINITY;
-                const float x1 = key_lo < visB ? (sc[1] + sd[1]) * p.scale_log2 : -INFINITY;
-                const float x2 = key_lo + 8 < visA ? (sc[2] + sd[2]) * p.scale_log2 : -INFINITY;
-                const float x3 = key_lo + 8 < visB ? (sc[3] + sd[3]) * p.scale_log2 : -INFINITY;
-                float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
-#pragma unroll
-                for (int off = 4; off < 32; off <<= 1) {
-                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-                }
-                const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
-                // a column that has seen no key yet (several query tokens) keeps -inf: use 0 as
-                // its reference so that every weight below is 0 rather than NaN
-                const float ms0 = mn0 == -INFINITY ? 0.f : mn0, ms1 = mn1 == -INFINITY ? 0.f : mn1;
-                const float p0 = fast_exp2(x0 - ms0), p1 = fast_exp2(x1 - ms1);
-                const float p2 = fast_exp2(x2 - ms0), p3 = fast_exp2(x3 - ms1);
-                if (mn0 != m_run[0] || mn1 != m_run[1]) {
-                    const float al0 = fast_exp2(m_run[0] - ms0), al1 = fast_exp2(m_run[1] - ms1);
-                    l_run[0] *= al0;
-                    l_run[1] *= al1;
-#pragma unroll
-                    for (int i = 0; i < D / 16; ++i) {
-                        acc[i][0] *= al0;
-                        acc[i][1] *= al1;
-                        acc[i][2] *= al0;
-                        acc[i][3] *= al1;
-                    }
-                    m_run[0] = mn0;
-                    m_run[1] = mn1;
-                }
-                l_run[0] += p0 + p2;
-                l_run[1] += p1 + p3;
-                // P^T operand (k16 keys x n8 heads) via 8x8 transposes of the score fragment
-                const uint32_t pb0 = movmatrix_trans(pack2<DT>(p0, p1));
-                const uint32_t pb1 = movmatrix_trans(pack2<DT>(p2, p3));
-                // O^T[D, 8] += V_tile^T . P^T
-#pragma unroll
-                for (int i = 0; i < D / 16; ++i) {
-                    const int chunk16 = i * 2 + vchunk_add;
-                    const uint32_t addr = vbase + (chunk16 >> 3) * Sh::kSliceBytes + vrow * 128 +
-                                          (((chunk16 & 7) ^ (vrow & 7)) << 4);
-                    uint32_t a[4];
-                    ldsm_x4_trans(addr, a);
-                    mma_16816<DT>(acc[i], a, pb0, pb1);
-                }
-            }
-            if (zeroed) {
-                // order the generic-proxy stores above before the next TMA write to this stage
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(empty0 + 8 * st);
-            if (++st == kStages) {
-                st = 0;
-                ph ^= 1;
-            }
-        }
+            if (lane == 0) mbar_arrive(iempty0 + 8 * slot);
+            if (!item.valid) break;
 
-        // per-thread partial sums -> per-warp sums (over the 8 key rows g)
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], off);
-            l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], off);
-        }
-
-        // ---------------- merge the four warps' states for this item, in the
-        // ring stage the producer handed over (it loads nothing into it)
-        if (ok && !mbar_wait_warp(full0 + 8 * st, ph, p.wait_limit_ns)) {
-            ok = false;
-            if (lane == 0) flag_error(p.err, DA_DEVERR_TIMEOUT);
-        }
-        float* red_acc = reinterpret_cast<float*>(smem + st * Sh::kStageBytes);   // [warp][8][D+4]
-        float* red_m = red_acc + kConsumerWarps * kHeadsPerCta * Sh::kMergeRow;    // [warp][8]
-        float* red_l = red_m + kConsumerWarps * kHeadsPerCta;                       // [warp][8]
-        if (g == 0) {
-            red_m[warp * kHeadsPerCta + 2 * t4] = m_run[0];
-            red_m[warp * kHeadsPerCta + 2 * t4 + 1] = m_run[1];
-            red_l[warp * kHeadsPerCta + 2 * t4] = l_run[0];
-            red_l[warp * kHeadsPerCta + 2 * t4 + 1] = l_run[1];
-        }
-        {
-            float* h0row = red_acc + (warp * kHeadsPerCta + 2 * t4) * Sh::kMergeRow;
-            float* h1row = h0row + Sh::kMergeRow;
-#pragma unroll
-            for (int i = 0; i < D / 16; ++i) {
-                h0row[i * 16 + g] = acc[i][0];
-                h1row[i * 16 + g] = acc[i][1];
-                h0row[i * 16 + g + 8] = acc[i][2];
-                h1row[i * 16 + g + 8] = acc[i][3];
+            // keys (relative to the split start) visible to this thread's two columns
+            int visA = item.nkeys, visB = item.nkeys;
+            if (p.tq > 1) {
+                visA = min(item.nkeys, item.vis0 + (item.c0 + 2 * t4) / p.G);
+                visB = min(item.nkeys, item.vis0 + (item.c0 + 2 * t4 + 1) / p.G);
             }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(mfull);
-        if (ok && !mbar_wait_warp(mfull, it & 1, p.wait_limit_ns)) {
-            ok = false;
-            if (lane == 0) flag_error(p.err, DA_DEVERR_TIMEOUT);
-        }
-        // Warp w writes heads w and w + 4; a lane owns four consecutive dims, read
-        // from each warp's row as one 16-byte load and stored as one vector. The
-        // passes are predicated rather than skipped, so their latencies overlap.
-        {
-            constexpr int kLanesPerHead = D / 4;
-            constexpr int kHeadsPerPass = 32 / kLanesPerHead;   // 1 at head_dim 128, 2 at 64
-            constexpr int kPasses = (kHeadsPerCta / kConsumerWarps) / kHeadsPerPass;
-            const int d0 = (lane % kLanesPerHead) * 4;
-#pragma unroll
-            for (int pass = 0; pass < kPasses; ++pass) {
-                const int hh = warp + kConsumerWarps * (pass * kHeadsPerPass + lane / kLanesPerHead);
-                const bool live = hh < item.nh;
-                float mw[kConsumerWarps];
-                float M = -INFINITY;
-#pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) {
-                    mw[w] = red_m[w * kHeadsPerCta + hh];
-                    M = fmaxf(M, mw[w]);
+            float acc[D / 16][4];
+    #pragma unroll
+            for (int i = 0; i < D / 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+            float m_run[2] = {-INFINITY, -INFINITY};   // heads 2*t4, 2*t4+1 (log2 domain)
+            float l_run[2] = {0.f, 0.f};               // this thread's share of the running sum
+
+            for (int t = 0; t < item.ntiles; ++t) {
+                const uint32_t fb = full0 + 8 * st;
+                if (ok && !mbar_wait_warp(fb, ph, p.wait_limit_ns)) {
+                    ok = false;
+                    bad_bar = fb;
+                    bad_ph = ph;
+                    if (lane == 0) flag_error(p.err, DA_DEVERR_TIMEOUT);
                 }
-                // a head that saw no key keeps M = -inf: weights 0, output 0, lse -inf
-                const float Ms = M == -INFINITY ? 0.f : M;
-                float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-                float lsum = 0.f;
-#pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) {
-                    const float wt = fast_exp2(mw[w] - Ms);
-                    lsum = fmaf(wt, red_l[w * kHeadsPerCta + hh], lsum);
-                    const float4 a = *reinterpret_cast<const float4*>(
-                        red_acc + (w * kHeadsPerCta + hh) * Sh::kMergeRow + d0);
-                    o.x = fmaf(wt, a.x, o.x);
-                    o.y = fmaf(wt, a.y, o.y);
-                    o.z = fmaf(wt, a.z, o.z);
-                    o.w = fmaf(wt, a.w, o.w);
+                const int keys_t = min(kStageKeys, item.nkeys - t * kStageKeys);
+                bool zeroed = false;
+                if (ok && warp * kBoxKeys < keys_t) {
+                    const uint32_t kbase = ring + st * Sh::kStageBytes;
+                    const uint32_t vbase = kbase + Sh::kTileBytes;
+                    const int valid_rows = keys_t - warp * kBoxKeys;
+                    if (valid_rows < kBoxKeys) {
+                        // The box's rows past the split end hold other keys (or, in a
+                        // padded cache, anything): their P is 0, but 0 * NaN is not, so
+                        // clear those V rows before the PV product.
+                        const int per_row = Sh::kHalves * 8;   // 16-byte chunks per row
+                        for (int c = lane; c < (kBoxKeys - valid_rows) * per_row; c += 32) {
+                            const int r = valid_rows + c / per_row;
+                            const int hf = (c % per_row) >> 3, ch = c & 7;
+                            const uint32_t addr = vbase + hf * Sh::kSliceBytes + (warp * kBoxKeys + r) * 128 + ch * 16;
+                            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+                        }
+                        zeroed = true;
+                        __syncwarp();
+                    }
+                    // S^T[16 keys, 8 heads] = K_tile . Q^T, two independent accumulator chains
+                    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+                    float sd[4] = {0.f, 0.f, 0.f, 0.f};
+    #pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const int chunk16 = ks * 2 + kchunk_add;          // 16-byte chunk along D
+                        const uint32_t addr = kbase + (chunk16 >> 3) * Sh::kSliceBytes + krow * 128 +
+                                              (((chunk16 & 7) ^ (krow & 7)) << 4);
+                        uint32_t a[4];
+                        ldsm_x4(addr, a);
+                        if (ks & 1) mma_16816<DT>(sd, a, qf[ks][0], qf[ks][1]);
+                        else mma_16816<DT>(sc, a, qf[ks][0], qf[ks][1]);
+                    }
+                    // scores -> exp2 domain, mask keys past the split end
+                    const int key_lo = t * kStageKeys + warp * kBoxKeys + g;   // relative to split start
+                    const float x0 = key_lo < visA ? (sc[0] + sd[0]) * p.scale_log2 : -INFINITY;
+                    const float x1 = key_lo < visB ? (sc[1] + sd[1]) * p.scale_log2 : -INFINITY;
+                    const float x2 = key_lo + 8 < visA ? (sc[2] + sd[2]) * p.scale_log2 : -INFINITY;
+                    const float x3 = key_lo + 8 < visB ? (sc[3] + sd[3]) * p.scale_log2 : -INFINITY;
+                    float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+    #pragma unroll
+                    for (int off = 4; off < 32; off <<= 1) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                    }
+                    const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
+                    // a column that has seen no key yet (several query tokens) keeps -inf: use 0 as
+                    // its reference so that every weight below is 0 rather than NaN
+                    const float ms0 = mn0 == -INFINITY ? 0.f : mn0, ms1 = mn1 == -INFINITY ? 0.f : mn1;
+                    const float p0 = fast_exp2(x0 - ms0), p1 = fast_exp2(x1 - ms1);
+                    const float p2 = fast_exp2(x2 - ms0), p3 = fast_exp2(x3 - ms1);
+                    if (mn0 != m_run[0] || mn1 != m_run[1]) {
+                        const float al0 = fast_exp2(m_run[0] - ms0), al1 = fast_exp2(m_run[1] - ms1);
+                        l_run[0] *= al0;
+                        l_run[1] *= al1;
+    #pragma unroll
+                        for (int i = 0; i < D / 16; ++i) {
+                            acc[i][0] *= al0;
+                            acc[i][1] *= al1;
+                            acc[i][2] *= al0;
+                            acc[i][3] *= al1;
+                        }
+                        m_run[0] = mn0;
+                        m_run[1] = mn1;
+                    }
+                    l_run[0] += p0 + p2;
+                    l_run[1] += p1 + p3;
+                    // P^T operand (k16 keys x n8 heads) via 8x8 transposes of the score fragment
+                    const uint32_t pb0 = movmatrix_trans(pack2<DT>(p0, p1));
+                    const uint32_t pb1 = movmatrix_trans(pack2<DT>(p2, p3));
+                    // O^T[D, 8] += V_tile^T . P^T
+    #pragma unroll
+                    for (int i = 0; i < D / 16; ++i) {
+                        const int chunk16 = i * 2 + vchunk_add;
+                        const uint32_t addr = vbase + (chunk16 >> 3) * Sh::kSliceBytes + vrow * 128 +
+                                              (((chunk16 & 7) ^ (vrow & 7)) << 4);
+                        uint32_t a[4];
+                        ldsm_x4_trans(addr, a);
+                        mma_16816<DT>(acc[i], a, pb0, pb1);
+                    }
                 }
-                // lsum >= 1 whenever M is finite (the largest score weighs 1)
-                const float inv = M == -INFINITY ? 0.f : fast_rcp(lsum);
-                o.x *= inv;
-                o.y *= inv;
-                o.z *= inv;
-                o.w *= inv;
-                if (live) {
-                    const int64_t qrow = column_row(p, item, hh);
-                    const int64_t row = qrow * p.S + item.s;
-                    *reinterpret_cast<float4*>(p.opart + row * D + d0) = o;
-                    if (d0 == 0) p.lse[row] = M == -INFINITY ? -INFINITY : (M + fast_log2(lsum)) * kLn2;
-                    // one split: its weight exp(lse_0 - lse) is 1, so o_0 is the answer
-                    if (p.out != nullptr)
-                        *reinterpret_cast<uint2*>(p.out + qrow * D + d0) =
-                            make_uint2(pack2<DT>(o.x, o.y), pack2<DT>(o.z, o.w));
+                if (zeroed) {
+                    // order the generic-proxy stores above before the next TMA write to this stage
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty0 + 8 * st);
+                if (++st == kStages) {
+                    st = 0;
+                    ph ^= 1;
+                }
+            }
+
+            // per-thread partial sums -> per-warp sums (over the 8 key rows g)
+    #pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], off);
+                l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], off);
+            }
+
+            // ---------------- merge the four warps' states for this item, in the
+            // ring stage the producer handed over (it loads nothing into it)
+            if (ok && !mbar_wait_warp(full0 + 8 * st, ph, p.wait_limit_ns)) {
+                ok = false;
+                if (lane == 0) flag_error(p.err, DA_DEVERR_TIMEOUT);
+            }
+            float* red_acc = reinterpret_cast<float*>(smem + st * Sh::kStageBytes);   // [warp][8][D+4]
+            float* red_m = red_acc + kConsumerWarps * kHeadsPerCta * Sh::kMergeRow;    // [warp][8]
+            float* red_l = red_m + kConsumerWarps * kHeadsPerCta;                       // [warp][8]
+            if (g == 0) {
+                red_m[warp * kHeadsPerCta + 2 * t4] = m_run[0];
+                red_m[warp * kHeadsPerCta + 2 * t4 + 1] = m_run[1];
+                red_l[warp * kHeadsPerCta + 2 * t4] = l_run[0];
+                red_l[warp * kHeadsPerCta + 2 * t4 + 1] = l_run[1];
+            }
+            {
+                float* h0row = red_acc + (warp * kHeadsPerCta + 2 * t4) * Sh::kMergeRow;
+                float* h1row = h0row + Sh::kMergeRow;
+    #pragma unroll
+                for (int i = 0; i < D / 16; ++i) {
+                    h0row[i * 16 + g] = acc[i][0];
+                    h1row[i * 16 + g] = acc[i][1];
+                    h0row[i * 16 + g + 8] = acc[i][2];
+                    h1row[i * 16 + g + 8] = acc[i][3];
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(mfull);
+            if (ok && !mbar_wait_warp(mfull, it & 1, p.wait_limit_ns)) {
+                ok = false;
+                if (lane == 0) flag_error(p.err, DA_DEVERR_TIMEOUT);
+            }
+            // Warp w writes heads w and w + 4; a lane owns four consecutive dims, read
+            // from each warp's row as one 16-byte load and stored as one vector. The
+            // passes are predicated rather than skipped, so their latencies overlap.
+            {
+                constexpr int kLanesPerHead = D / 4;
+                constexpr int kHeadsPerPass = 32 / kLanesPerHead;   // 1 at head_dim 128, 2 at 64
+                constexpr int kPasses = (kHeadsPerCta / kConsumerWarps) / kHeadsPerPass;
+                const int d0 = (lane % kLanesPerHead) * 4;
+    #pragma unroll
+                for (int pass = 0; pass < kPasses; ++pass) {
+                    const int hh = warp + kConsumerWarps * (pass * kHeadsPerPass + lane / kLanesPerHead);
+                    const bool live = hh < item.nh;
+                    float mw[kConsumerWarps];
+                    float M = -INFINITY;
+    #pragma unroll
+                    for (int w = 0; w < kConsumerWarps; ++w) {
+                        mw[w] = red_m[w * kHeadsPerCta + hh];
+                        M = fmaxf(M, mw[w]);
+                    }
+                    // a head that saw no key keeps M = -inf: weights 0, output 0, lse -inf
+                    const float Ms = M == -INFINITY ? 0.f : M;
+                    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+                    float lsum = 0.f;
+    #pragma unroll
+                    for (int w = 0; w < kConsumerWarps; ++w) {
+                        const float wt = fast_exp2(mw[w] - Ms);
+                        lsum = fmaf(wt, red_l[w * kHeadsPerCta + hh], lsum);
+                        const float4 a = *reinterpret_cast<const float4*>(
+                            red_acc + (w * kHeadsPerCta + hh) * Sh::kMergeRow + d0);
+                        o.x = fmaf(wt, a.x, o.x);
+                        o.y = fmaf(wt, a.y, o.y);
+                        o.z = fmaf(wt, a.z, o.z);
+                        o.w = fmaf(wt, a.w, o.w);
+                    }
+                    // lsum >= 1 whenever M is finite (the largest score weighs 1)
+                    const float inv = M == -INFINITY ? 0.f : fast_rcp(lsum);
+                    o.x *= inv;
+                    o.y *= inv;
+                    o.z *= inv;
+                    o.w *= inv;
+                    if (live) {
+                        const int64_t qrow = column_row(p, item, hh);
+                        const int64_t row = qrow * p.S + item.s;
+                        *reinterpret_cast<float4*>(p.opart + row * D + d0) = o;
+                        if (d0 == 0) p.lse[row] = M == -INFINITY ? -INFINITY : (M + fast_log2(lsum)) * kLn2;
+                        // one split: its weight exp(lse_0 - lse) is 1, so o_0 is the answer
+                        if (p.out != nullptr)
+                            *reinterpret_cast<uint2*>(p.out + qrow * D + d0) =
+                                make_uint2(pack2<DT>(o.x, o.y), pack2<DT>(o.z, o.w));
+                    }
+                }
+            }
+        } else {
+        // ---- two n-tiles (up to 16 columns per item): each K and V fragment feeds both
+            // Q^T fragments (B operand, k16 x n8) of n-tile n: column 8n + g, dims ks*16 + 2*t4 (+1)
+            // and +8 (+9).
+            uint32_t qf[D / 16][NT][2];
+    #pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                const int col = 8 * n + g;
+                const bool hv = col < item.nh;
+                const uint32_t qrow = qbuf + slot * Sh::kQBytes + (hv ? col : 0) * D * 2;
+    #pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    uint32_t a0, a1;
+                    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(a0) : "r"(qrow + (ks * 16 + 2 * t4) * 2));
+                    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(a1) : "r"(qrow + (ks * 16 + 8 + 2 * t4) * 2));
+                    qf[ks][n][0] = hv ? a0 : 0u;
+                    qf[ks][n][1] = hv ? a1 : 0u;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(iempty0 + 8 * slot);
+            if (!item.valid) break;
+
+            // keys (relative to the split start) visible to this thread's two columns of each n-tile
+            int visA[NT], visB[NT];
+    #pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                visA[n] = visB[n] = item.nkeys;
+                if (p.tq > 1) {
+                    visA[n] = min(item.nkeys, item.vis0 + (item.c0 + 8 * n + 2 * t4) / p.G);
+                    visB[n] = min(item.nkeys, item.vis0 + (item.c0 + 8 * n + 2 * t4 + 1) / p.G);
+                }
+            }
+            float acc[D / 16][NT][4];
+    #pragma unroll
+            for (int i = 0; i < D / 16; ++i)
+    #pragma unroll
+                for (int n = 0; n < NT; ++n) acc[i][n][0] = acc[i][n][1] = acc[i][n][2] = acc[i][n][3] = 0.f;
+            float m_run[NT][2], l_run[NT][2];   // columns 8n + 2*t4 (+1): running max (log2 domain), sum share
+    #pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                m_run[n][0] = m_run[n][1] = -INFINITY;
+                l_run[n][0] = l_run[n][1] = 0.f;
+            }
+
+            for (int t = 0; t < item.ntiles; ++t) {
+                const uint32_t fb = full0 + 8 * st;
+                if (ok && !mbar_wait_warp(fb, ph, p.wait_limit_ns)) {
+                    ok = false;
+                    bad_bar = fb;
+                    bad_ph = ph;
+                    if (lane == 0) flag_error(p.err, DA_DEVERR_TIMEOUT);
+                }
+                const int keys_t = min(kStageKeys, item.nkeys - t * kStageKeys);
+                bool zeroed = false;
+                if (ok && warp * kBoxKeys < keys_t) {
+                    const uint32_t kbase = ring + st * Sh::kStageBytes;
+                    const uint32_t vbase = kbase + Sh::kTileBytes;
+                    const int valid_rows = keys_t - warp * kBoxKeys;
+                    if (valid_rows < kBoxKeys) {
+                        // The box's rows past the split end hold other keys (or, in a
+                        // padded cache, anything): their P is 0, but 0 * NaN is not, so
+                        // clear those V rows before the PV product.
+                        const int per_row = Sh::kHalves * 8;   // 16-byte chunks per row
+                        for (int c = lane; c < (kBoxKeys - valid_rows) * per_row; c += 32) {
+                            const int r = valid_rows + c / per_row;
+                            const int hf = (c % per_row) >> 3, ch = c & 7;
+                            const uint32_t addr = vbase + hf * Sh::kSliceBytes + (warp * kBoxKeys + r) * 128 + ch * 16;
+                            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+                        }
+                        zeroed = true;
+                        __syncwarp();
+                    }
+                    // S^T[16 keys, 8 columns] = K_tile . Q^T per n-tile, two independent accumulator
+                    // chains each; one K fragment feeds every n-tile
+                    float sc[NT][4], sd[NT][4];
+    #pragma unroll
+                    for (int n = 0; n < NT; ++n)
+    #pragma unroll
+                        for (int j = 0; j < 4; ++j) sc[n][j] = sd[n][j] = 0.f;
+    #pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const int chunk16 = ks * 2 + kchunk_add;          // 16-byte chunk along D
+                        const uint32_t addr = kbase + (chunk16 >> 3) * Sh::kSliceBytes + krow * 128 +
+                                              (((chunk16 & 7) ^ (krow & 7)) << 4);
+                        uint32_t a[4];
+                        ldsm_x4(addr, a);
+    #pragma unroll
+                        for (int n = 0; n < NT; ++n) {
+                            if (ks & 1) mma_16816<DT>(sd[n], a, qf[ks][n][0], qf[ks][n][1]);
+                            else mma_16816<DT>(sc[n], a, qf[ks][n][0], qf[ks][n][1]);
+                        }
+                    }
+                    const int key_lo = t * kStageKeys + warp * kBoxKeys + g;   // relative to split start
+                    uint32_t pb0[NT], pb1[NT];
+    #pragma unroll
+                    for (int n = 0; n < NT; ++n) {
+                        // scores -> exp2 domain, mask keys past the split end
+                        const float x0 = key_lo < visA[n] ? (sc[n][0] + sd[n][0]) * p.scale_log2 : -INFINITY;
+                        const float x1 = key_lo < visB[n] ? (sc[n][1] + sd[n][1]) * p.scale_log2 : -INFINITY;
+                        const float x2 = key_lo + 8 < visA[n] ? (sc[n][2] + sd[n][2]) * p.scale_log2 : -INFINITY;
+                        const float x3 = key_lo + 8 < visB[n] ? (sc[n][3] + sd[n][3]) * p.scale_log2 : -INFINITY;
+                        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+    #pragma unroll
+                        for (int off = 4; off < 32; off <<= 1) {
+                            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                        }
+                        const float mn0 = fmaxf(m_run[n][0], mx0), mn1 = fmaxf(m_run[n][1], mx1);
+                        // a column that has seen no key yet (several query tokens) keeps -inf: use 0 as
+                        // its reference so that every weight below is 0 rather than NaN
+                        const float ms0 = mn0 == -INFINITY ? 0.f : mn0, ms1 = mn1 == -INFINITY ? 0.f : mn1;
+                        const float p0 = fast_exp2(x0 - ms0), p1 = fast_exp2(x1 - ms1);
+                        const float p2 = fast_exp2(x2 - ms0), p3 = fast_exp2(x3 - ms1);
+                        if (mn0 != m_run[n][0] || mn1 != m_run[n][1]) {
+                            const float al0 = fast_exp2(m_run[n][0] - ms0), al1 = fast_exp2(m_run[n][1] - ms1);
+                            l_run[n][0] *= al0;
+                            l_run[n][1] *= al1;
+    #pragma unroll
+                            for (int i = 0; i < D / 16; ++i) {
+                                acc[i][n][0] *= al0;
+                                acc[i][n][1] *= al1;
+                                acc[i][n][2] *= al0;
+                                acc[i][n][3] *= al1;
+                            }
+                            m_run[n][0] = mn0;
+                            m_run[n][1] = mn1;
+                        }
+                        l_run[n][0] += p0 + p2;
+                        l_run[n][1] += p1 + p3;
+                        // P^T operand (k16 keys x n8 columns) via 8x8 transposes of the score fragment
+                        pb0[n] = movmatrix_trans(pack2<DT>(p0, p1));
+                        pb1[n] = movmatrix_trans(pack2<DT>(p2, p3));
+                    }
+                    // O^T[D, 8 per n-tile] += V_tile^T . P^T; one V fragment feeds every n-tile
+    #pragma unroll
+                    for (int i = 0; i < D / 16; ++i) {
+                        const int chunk16 = i * 2 + vchunk_add;
+                        const uint32_t addr = vbase + (chunk16 >> 3) * Sh::kSliceBytes + vrow * 128 +
+                                              (((chunk16 & 7) ^ (vrow & 7)) << 4);
+                        uint32_t a[4];
+                        ldsm_x4_trans(addr, a);
+    #pragma unroll
+                        for (int n = 0; n < NT; ++n) mma_16816<DT>(acc[i][n], a, pb0[n], pb1[n]);
+                    }
+                }
+                if (zeroed) {
+                    // order the generic-proxy stores above before the next TMA write to this stage
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty0 + 8 * st);
+                if (++st == kStages) {
+                    st = 0;
+                    ph ^= 1;
+                }
+            }
+
+            // per-thread partial sums -> per-warp sums (over the 8 key rows g)
+    #pragma unroll
+            for (int n = 0; n < NT; ++n)
+    #pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    l_run[n][0] += __shfl_xor_sync(0xffffffffu, l_run[n][0], off);
+                    l_run[n][1] += __shfl_xor_sync(0xffffffffu, l_run[n][1], off);
+                }
+
+            // ---------------- merge the four warps' states for this item, in the
+            // ring stage the producer handed over (it loads nothing into it), one
+            // n-tile (8 columns) per round
+            if (ok && !mbar_wait_warp(full0 + 8 * st, ph, p.wait_limit_ns)) {
+                ok = false;
+                if (lane == 0) flag_error(p.err, DA_DEVERR_TIMEOUT);
+            }
+            float* red_acc = reinterpret_cast<float*>(smem + st * Sh::kStageBytes);   // [warp][8][D+4]
+            float* red_m = red_acc + kConsumerWarps * 8 * Sh::kMergeRow;               // [warp][8]
+            float* red_l = red_m + kConsumerWarps * 8;                                  // [warp][8]
+    #pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                if (n > 0) {
+                    // every warp has read the previous round's rows before they are overwritten
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(mdone);
+                    if (ok && !mbar_wait_warp(mdone, md & 1, p.wait_limit_ns)) {
+                        ok = false;
+                        if (lane == 0) flag_error(p.err, DA_DEVERR_TIMEOUT);
+                    }
+                    ++md;
+                }
+                if (g == 0) {
+                    red_m[warp * 8 + 2 * t4] = m_run[n][0];
+                    red_m[warp * 8 + 2 * t4 + 1] = m_run[n][1];
+                    red_l[warp * 8 + 2 * t4] = l_run[n][0];
+                    red_l[warp * 8 + 2 * t4 + 1] = l_run[n][1];
+                }
+                {
+                    float* h0row = red_acc + (warp * 8 + 2 * t4) * Sh::kMergeRow;
+                    float* h1row = h0row + Sh::kMergeRow;
+    #pragma unroll
+                    for (int i = 0; i < D / 16; ++i) {
+                        h0row[i * 16 + g] = acc[i][n][0];
+                        h1row[i * 16 + g] = acc[i][n][1];
+                        h0row[i * 16 + g + 8] = acc[i][n][2];
+                        h1row[i * 16 + g + 8] = acc[i][n][3];
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(mfull);
+                if (ok && !mbar_wait_warp(mfull, mz & 1, p.wait_limit_ns)) {
+                    ok = false;
+                    if (lane == 0) flag_error(p.err, DA_DEVERR_TIMEOUT);
+                }
+                ++mz;
+                // Warp w writes columns w and w + 4 of the round; a lane owns four consecutive
+                // dims, read from each warp's row as one 16-byte load and stored as one vector.
+                // The passes are predicated rather than skipped, so their latencies overlap.
+                constexpr int kLanesPerHead = D / 4;
+                constexpr int kHeadsPerPass = 32 / kLanesPerHead;   // 1 at head_dim 128, 2 at 64
+                constexpr int kPasses = (8 / kConsumerWarps) / kHeadsPerPass;
+                const int d0 = (lane % kLanesPerHead) * 4;
+    #pragma unroll
+                for (int pass = 0; pass < kPasses; ++pass) {
+                    const int hh = warp + kConsumerWarps * (pass * kHeadsPerPass + lane / kLanesPerHead);
+                    const bool live = 8 * n + hh < item.nh;
+                    float mw[kConsumerWarps];
+                    float M = -INFINITY;
+    #pragma unroll
+                    for (int w = 0; w < kConsumerWarps; ++w) {
+                        mw[w] = red_m[w * 8 + hh];
+                        M = fmaxf(M, mw[w]);
+                    }
+                    // a column that saw no key keeps M = -inf: weights 0, output 0, lse -inf
+                    const float Ms = M == -INFINITY ? 0.f : M;
+                    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+                    float lsum = 0.f;
+    #pragma unroll
+                    for (int w = 0; w < kConsumerWarps; ++w) {
+                        const float wt = fast_exp2(mw[w] - Ms);
+                        lsum = fmaf(wt, red_l[w * 8 + hh], lsum);
+                        const float4 a = *reinterpret_cast<const float4*>(red_acc + (w * 8 + hh) * Sh::kMergeRow + d0);
+                        o.x = fmaf(wt, a.x, o.x);
+                        o.y = fmaf(wt, a.y, o.y);
+                        o.z = fmaf(wt, a.z, o.z);
+                        o.w = fmaf(wt, a.w, o.w);
+                    }
+                    // lsum >= 1 whenever M is finite (the largest score weighs 1)
+                    const float inv = M == -INFINITY ? 0.f : fast_rcp(lsum);
+                    o.x *= inv;
+                    o.y *= inv;
+                    o.z *= inv;
+                    o.w *= inv;
+                    if (live) {
+                        const int64_t qrow = column_row(p, item, 8 * n + hh);
+                        const int64_t row = qrow * p.S + item.s;
+                        *reinterpret_cast<float4*>(p.opart + row * D + d0) = o;
+                        if (d0 == 0) p.lse[row] = M == -INFINITY ? -INFINITY : (M + fast_log2(lsum)) * kLn2;
+                        // one split: its weight exp(lse_0 - lse) is 1, so o_0 is the answer
+                        if (p.out != nullptr)
+                            *reinterpret_cast<uint2*>(p.out + qrow * D + d0) =
+                                make_uint2(pack2<DT>(o.x, o.y), pack2<DT>(o.z, o.w));
+                    }
                 }
             }
         }
@@ -1107,7 +1386,7 @@ da_status check_common(const void* q, const void* k, const void* v, const int32_
     const size_t need = decode_attn_splitkv_workspace_size(B, Hq, D, S);
     if (need == 0) return DA_ERR_INVALID_ARG;
     if (ws_bytes < need) return DA_ERR_WORKSPACE_TOO_SMALL;
-    const int64_t chunks = (Hq / Hkv + kHeadsPerCta - 1) / kHeadsPerCta;
+    const int64_t chunks = item_chunks(Hq / Hkv);
     if (static_cast<int64_t>(B) * Hkv * chunks * S > 0x7fffffffll) return DA_ERR_INVALID_ARG;
     return DA_OK;
 }
@@ -1137,7 +1416,7 @@ constexpr int kMaxVarsplitBatch = 1024;                                   // seq
 constexpr double kLongStreamBytes = 1.5e9;   // K/V bytes above which even batches are split for balance
 
 // `out` is written by the split kernel itself only with one uniform split.
-template <int D, int DT>
+template <int D, int DT, int NT>
 da_status launch_split(const Call& c, void* out, cudaStream_t stream) {
     // 64-key boxes for full stages, 16-key boxes for the ragged end of a split
     alignas(64) CUtensorMap mk, mv, mk16, mv16;
@@ -1171,7 +1450,7 @@ da_status launch_split(const Call& c, void* out, cudaStream_t stream) {
     p.kv_rows = c.kv_rows;
     p.layout = c.lay;
     p.tq = c.tq;
-    p.chunks = (p.G * c.tq + kHeadsPerCta - 1) / kHeadsPerCta;
+    p.chunks = (p.G * c.tq + NT * kHeadsPerCta - 1) / (NT * kHeadsPerCta);
     p.no_kv = c.kv_rows == 0;
     p.n_items = c.B * c.Hkv * p.chunks * c.S;   // per-sequence mode: an upper bound (the kernel counts)
     p.split_len = c.split_len;
@@ -1180,8 +1459,8 @@ da_status launch_split(const Call& c, void* out, cudaStream_t stream) {
     p.wait_limit_ns = kWaitLimitNs;
 
     const bool var = c.split_len != 0;
-    const int smem = Shape<D>::kSmemBytes + (p.stage_cu ? kStagedBytes : 0) + (var ? kStagedBytes : 0);
-    auto kern = split_kernel<D, DT>;
+    const int smem = Shape<D, NT>::kSmemBytes + (p.stage_cu ? kStagedBytes : 0) + (var ? kStagedBytes : 0);
+    auto kern = split_kernel<D, DT, NT>;
     static DeviceCache caches[3];   // by the number of staged [B + 1] arrays
     int grid = 0;
     if (persistent_grid(kern, smem, caches[(p.stage_cu ? 1 : 0) + (var ? 1 : 0)], &grid) != cudaSuccess)
@@ -1233,10 +1512,17 @@ da_status launch_combine(const Call& c, void* out, cudaStream_t stream) {
     return cudaLaunchKernelEx(&cfg, combine_kernel<D, DT>, cp) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
 }
 
+template <int D, int DT>
+da_status launch_split_cols(const Call& c, void* out, cudaStream_t st) {
+    if (item_cols(static_cast<int64_t>(c.Hq / c.Hkv) * c.tq) > kHeadsPerCta)
+        return launch_split<D, DT, 2>(c, out, st);
+    return launch_split<D, DT, 1>(c, out, st);
+}
+
 da_status dispatch_split(const Call& c, void* out, cudaStream_t st) {
     if (c.D == 128)
-        return c.dt == DA_F16 ? launch_split<128, DA_F16>(c, out, st) : launch_split<128, DA_BF16>(c, out, st);
-    return c.dt == DA_F16 ? launch_split<64, DA_F16>(c, out, st) : launch_split<64, DA_BF16>(c, out, st);
+        return c.dt == DA_F16 ? launch_split_cols<128, DA_F16>(c, out, st) : launch_split_cols<128, DA_BF16>(c, out, st);
+    return c.dt == DA_F16 ? launch_split_cols<64, DA_F16>(c, out, st) : launch_split_cols<64, DA_BF16>(c, out, st);
 }
 
 da_status dispatch_combine(const Call& c, void* out, cudaStream_t st) {
@@ -1319,7 +1605,7 @@ int decode_attn_splitkv_num_splits(int B, int Hq, int Hkv, int D, int min_kv, in
             sm_count <= 0)
             sm_count = 148;
     }
-    const int64_t chunks = (Hq / Hkv + kHeadsPerCta - 1) / kHeadsPerCta;
+    const int64_t chunks = item_chunks(Hq / Hkv);
     const int64_t units = static_cast<int64_t>(B) * Hkv * chunks;   // (sequence, KV head, chunk)
     const int64_t slots = static_cast<int64_t>(sm_count) * (D == 128 ? 2 : 4);   // persistent CTAs
     int64_t S;
@@ -1413,7 +1699,7 @@ int decode_attn_splitkv_varsplit_plan(int B, int Hq, int Hkv, int D, int64_t tot
             sm_count <= 0)
             sm_count = 148;
     }
-    const int64_t chunks = (Hq / Hkv + kHeadsPerCta - 1) / kHeadsPerCta;
+    const int64_t chunks = item_chunks(Hq / Hkv);
     const int64_t key_units = total_kv * Hkv * chunks;      // keys to stream, summed over (KV head, chunk)
     const int64_t target = 8 * static_cast<int64_t>(sm_count);   // about four items per resident CTA
     int64_t len = (key_units + target - 1) / std::max<int64_t>(1, target);
@@ -1457,7 +1743,7 @@ da_status decode_attn_splitkv_multiquery(const void* q, const void* k, const voi
     if (workspace_bytes < need) return DA_ERR_WORKSPACE_TOO_SMALL;
     if (!out) return DA_ERR_INVALID_ARG;
     if (!aligned(out, 16)) return DA_ERR_ALIGNMENT;
-    const int64_t chunks = (static_cast<int64_t>(Hq / Hkv) * T_q + kHeadsPerCta - 1) / kHeadsPerCta;
+    const int64_t chunks = item_chunks(static_cast<int64_t>(Hq / Hkv) * T_q);
     if (static_cast<int64_t>(B) * Hkv * chunks * num_splits > 0x7fffffffll) return DA_ERR_INVALID_ARG;
     if (static_cast<int64_t>(B) * T_q * Hq * D > 0x7fffffffll) return DA_ERR_INVALID_ARG;
     return run_decode(make_call(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale, num_splits, 0,
@@ -1541,7 +1827,7 @@ double decode_attn_splitkv_model_us(const int32_t* kv_lens, int B, int Hq, int H
     const double t0 = m[0], t_item = m[1], r_cta = m[2], bw = m[3], t_comb = m[4], bw_comb = m[5], kappa = m[6];
     if (!(r_cta > 0) || !(bw > 0) || !(bw_comb > 0) || !(t_item >= 0) || !(kappa >= 0)) return -1.0;
     const int S = num_splits;
-    const int chunks = (Hq / Hkv * T_q + kHeadsPerCta - 1) / kHeadsPerCta;
+    const int chunks = static_cast<int>(item_chunks(static_cast<int64_t>(Hq / Hkv) * T_q));
     const int slots = sm_count * (D == 128 ? 2 : 4);
     const double key_bytes = 4.0 * D;   // K and V rows of one key and KV head
     // the work items in queue order: the bytes each streams (later chunks of a

@@ -75,7 +75,9 @@ def test_picker_properties(lib, shape):
         S = da.num_splits(B, Hq, Hkv, D, mn, mx, sm)
         assert 1 <= S <= min(mn, da.DA_MAX_SPLITS)
         assert S == da.num_splits(B, Hq, Hkv, D, mn, mx, sm)
-        units = B * Hkv * math.ceil(Hq // Hkv / 8)
+        cols = Hq // Hkv
+        chunks = math.ceil(cols / (16 if cols > 8 else 8))   # 16-column items past 8 columns
+        units = B * Hkv * chunks
         slots = sm * (2 if D == 128 else 4)
         if 2 * mn > mx:
             if 5 * units >= 4 * sm:
@@ -88,7 +90,7 @@ def test_picker_properties(lib, shape):
                 assert S == 1 or mn // S >= 256
         else:
             # eight items per SM, or as many as keep the longest splits near two CTA shares
-            share = (mx + (B - 1) * mn) * Hkv * math.ceil(Hq // Hkv / 8) / slots
+            share = (mx + (B - 1) * mn) * Hkv * chunks / slots
             assert units * (S - 1) < 8 * sm or S == math.ceil(mx / (2 * share))
 
 

@@ -58,6 +58,9 @@ CASES = [
     ("long_single_split", 1, 7, 1, 128, [4096], "f16", LAYOUT_VARLEN, 1, 0),
     ("d64_bhsd_bf16", 3, 8, 2, 64, [77, 1, 64], "bf16", LAYOUT_BHSD, 2, 80),
     ("many_splits", 2, 4, 1, 128, [2000, 1500], "f16", LAYOUT_VARLEN, 100, 0),
+    # more than 8 columns per KV head: 16-column items (two n-tiles), and a second chunk
+    ("group20_two_chunks", 2, 40, 2, 128, [300, 517], "f16", LAYOUT_VARLEN, 3, 0),
+    ("group9_d64_bhsd", 2, 18, 2, 64, [100, 64], "bf16", LAYOUT_BHSD, 2, 128),
 ]
 
 
