@@ -119,7 +119,9 @@ da_status decode_attn_splitkv_workspace_init(void* workspace, size_t workspace_b
  *     with splits of 256 to 1024 keys.
  *   Ragged lengths: about eight items per SM (splits of at least 64 keys),
  *     raised until the longest sequence's splits are at most twice one CTA's
- *     share of a lower bound of the total keys (max_kv + (B-1) * min_kv).
+ *     share of a lower bound of the total keys (max_kv + (B-1) * min_kv); with
+ *     16-column items (G > 8, or G * T_q > 8 when Hq is passed as Hq * T_q for
+ *     several query tokens) four items per SM and four shares.
  * No split is ever empty (num_splits <= min_kv; the TileLang page's scheduling
  * constraint, split kernel docstring). sm_count 0 means: query the current
  * device. Returns a value in [1, DA_MAX_SPLITS]; 1 when min_kv <= 0 or an

@@ -24,7 +24,7 @@ import statistics
 import sys
 
 from . import (alloc_workspace, build, decode_attn_splitkv, decode_attn_splitkv_get_error,
-               decode_attn_splitkv_varsplit, load, model_us, num_splits)
+               decode_attn_splitkv_multiquery, decode_attn_splitkv_varsplit, load, model_us, num_splits)
 
 SPLITS = [1, 2, 3, 4, 5, 6, 8, 10, 12, 16, 19, 24, 32, 38, 48, 64, 76, 96, 128, 192, 256]
 WORKLOADS = [
@@ -73,9 +73,20 @@ def _device_problem(p, dev):
     return up(p.q), up(p.k), up(p.v), torch.from_numpy(p.cu.astype(np.int32)).to(dev)
 
 
+def _workload(name: str):
+    """A named workload; a `_tqN` suffix asks for N query tokens per sequence."""
+    from synth.workloads import materialize, workload
+    if "_tq" not in name:
+        return workload(name)
+    base, tq = name.rsplit("_tq", 1)
+    p = workload(base, data=False)
+    p.tq = int(tq)
+    p.name = name
+    return materialize(p)
+
+
 def sweep(names, reps: int, out_path: str) -> dict:
     import torch
-    from synth.workloads import workload
     build()
     load()
     timer = _Timer(reps)
@@ -83,18 +94,19 @@ def sweep(names, reps: int, out_path: str) -> dict:
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     res = {}
     for name in names:
-        p = workload(name)
+        p = _workload(name)
         q, k, v, cu = _device_problem(p, dev)
         p.k = p.v = None
         out = torch.empty(*p.q.shape, dtype=q.dtype, device=dev)
         splits = [S for S in SPLITS if S <= max(1, min(p.lens))]
-        ws = alloc_workspace(p.B, p.Hq, p.D, max(splits), device=dev, stream=st)
-        row = {"lens": p.lens, "B": p.B, "Hq": p.Hq, "Hkv": p.Hkv, "D": p.D, "sms": sms,
-               "picker": num_splits(p.B, p.Hq, p.Hkv, p.D, min(p.lens), max(p.lens), sms), "t": {}}
+        ws = alloc_workspace(p.B * p.tq, p.Hq, p.D, max(splits), device=dev, stream=st)
+        row = {"lens": p.lens, "B": p.B, "Hq": p.Hq, "Hkv": p.Hkv, "D": p.D, "tq": p.tq, "sms": sms,
+               "picker": num_splits(p.B, p.Hq * p.tq, p.Hkv, p.D, min(p.lens), max(p.lens), sms), "t": {}}
+        entry = decode_attn_splitkv if p.tq == 1 else decode_attn_splitkv_multiquery
         for S in splits:
-            row["t"][str(S)] = round(timer(lambda S=S: decode_attn_splitkv(
+            row["t"][str(S)] = round(timer(lambda S=S: entry(
                 q, k, v, cu, out, ws, num_splits=S, scale=p.scale, layout=p.layout, stream=st)), 2)
-        if 2 * min(p.lens) <= max(p.lens):
+        if p.tq == 1 and 2 * min(p.lens) <= max(p.lens):
             row["var"] = {}
             for sl in (512, 1024, 2048, 4096, 8192):
                 ms = min(1024, -(-max(p.lens) // sl))
@@ -121,7 +133,7 @@ def _log_err(args):
     load()
     e = 0.0
     for r, S, t in pts:
-        p = model_us(r["lens"], r["Hq"], r["Hkv"], r["D"], S, r["sms"], 1, params)
+        p = model_us(r["lens"], r["Hq"], r["Hkv"], r["D"], S, r["sms"], r.get("tq", 1), params)
         if p <= 0:
             return 1e9
         e += (math.log(p) - math.log(t)) ** 2
@@ -160,7 +172,7 @@ def fit(path: str, within: float = 1.3, workers: int = 8) -> dict:
     params = [math.exp(v) for v in best.x]
 
     def err(sel):
-        return np.array([abs(model_us(r["lens"], r["Hq"], r["Hkv"], r["D"], S, r["sms"], 1, params) / t - 1)
+        return np.array([abs(model_us(r["lens"], r["Hq"], r["Hkv"], r["D"], S, r["sms"], r.get("tq", 1), params) / t - 1)
                          for _, r, S, t in sel])
     e, ea = err(pts), err(allpts)
     out = {"params": params, "fitted_calls": len(pts), "measured_calls": len(allpts),

@@ -1612,14 +1612,19 @@ int decode_attn_splitkv_num_splits(int B, int Hq, int Hkv, int D, int min_kv, in
     if (2 * static_cast<int64_t>(min_kv) <= max_kv) {
         // Ragged lengths: about eight items per SM, so the work queue can even
         // out splits of unequal length; splits may be short ...
-        S = (8 * static_cast<int64_t>(sm_count) + units - 1) / units;
+        // (16-column items carry twice the work per key and a two-round merge:
+        // half as many of them, with longer splits, measured best)
+        const bool wide = item_cols(Hq / Hkv) > kHeadsPerCta;
+        const int64_t per_sm = wide ? 4 : 8;
+        const double shares = wide ? 4.0 : 2.0;
+        S = (per_sm * static_cast<int64_t>(sm_count) + units - 1) / units;
         S = std::min<int64_t>(S, std::max<int64_t>(1, min_kv / 64));
-        // ... and the longest sequence's splits at most about twice one CTA's
-        // share of the keys (the share taken from a lower bound of the total),
-        // so that no single split outlasts the rest of the batch.
+        // ... and the longest sequence's splits at most about twice (wide items:
+        // four times) one CTA's share of the keys (the share taken from a lower
+        // bound of the total), so that no single split outlasts the rest of the batch.
         const double total = static_cast<double>(max_kv) + static_cast<double>(B - 1) * min_kv;
         const double share = total * Hkv * chunks / static_cast<double>(slots);
-        S = std::max<int64_t>(S, static_cast<int64_t>(std::ceil(max_kv / (2.0 * share))));
+        S = std::max<int64_t>(S, static_cast<int64_t>(std::ceil(max_kv / (shares * share))));
     } else if (5 * units >= 4 * static_cast<int64_t>(sm_count)) {
         // Even lengths, about one unit per SM or more: one split (no combine)
         // while the stream is short; for a long stream about 1.7 waves of items,

@@ -90,8 +90,11 @@ def test_picker_properties(lib, shape):
                 assert S == 1 or mn // S >= 256
         else:
             # eight items per SM, or as many as keep the longest splits near two CTA shares
+            # (16-column items: four per SM, four shares)
+            wide = cols > 8
             share = (mx + (B - 1) * mn) * Hkv * chunks / slots
-            assert units * (S - 1) < 8 * sm or S == math.ceil(mx / (2 * share))
+            assert (units * (S - 1) < (4 if wide else 8) * sm
+                    or S == math.ceil(mx / ((4 if wide else 2) * share)))
 
 
 def test_picker_choices_on_measured_workloads(lib):
@@ -102,6 +105,9 @@ def test_picker_choices_on_measured_workloads(lib):
     assert da.num_splits(16, 32, 8, 128, 131072, 131072, sm) == 4
     assert da.num_splits(8, 32, 32, 128, 4096, 4096, sm) == 1
     assert 16 <= da.num_splits(16, 32, 8, 128, 512, 131072, sm) <= 24   # one 128K sequence among 512s
+    # several query tokens: Hq passed as Hq * T_q; Qwen heads (28 / 4), lengths 552 .. 8192
+    assert da.num_splits(64, 28 * 2, 4, 128, 552, 8192, sm) == 4        # 14 columns: 16-column items
+    assert da.num_splits(64, 28 * 4, 4, 128, 552, 8192, sm) == 2        # 28 columns: two 16-column items
 
 
 def test_picker_degenerate(lib):
