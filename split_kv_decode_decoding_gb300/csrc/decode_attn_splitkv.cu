@@ -1,18 +1,20 @@
 // Split-KV decode attention (flash-decoding) for GB300 / sm_103a.
 //
 // Split step: a persistent kernel, two CTAs per SM (more at head_dim 64), that
-// takes work items (sequence b, KV head, head chunk, split s) from a queue in
-// the workspace. For each item it computes, for the up-to-8 query heads of the
-// KV head's group that the chunk holds, the normalised partial output o_s and
+// takes work items (sequence b, KV head, column chunk, split s) from a queue in
+// the workspace. The columns of a KV head are its query heads times the query
+// tokens (one token in plain decode). For each item it computes, for the up-to-8
+// (or, when the KV head serves more than 8 columns, up-to-16) columns that the
+// chunk holds, the normalised partial output o_s and
 // lse_s = ln sum_{j in split} exp(s_j), and writes them to the workspace.
-//   * The GQA group (up to 8 query heads) is packed into the N = 8 columns of
-//     m16n8k16 tensor-core products, so every K/V byte is read from HBM once
-//     per group (TileLang decode_attention_splitkv.py, split segment,
-//     cur_kv_head; CS349E lecture 11 04_flash_decoding.py, demo1_exact second
-//     observation). Keys are the M rows: S^T[key, head] = K_tile . Q^T, then
-//     O^T[dim, head] += V_tile^T . P^T; the score fragment turns into the P^T
+//   * The GQA group is packed into the N = 8 columns of m16n8k16 tensor-core
+//     products (two such n-tiles for 16 columns), so every K/V byte is read
+//     from HBM once per group (TileLang decode_attention_splitkv.py, split
+//     segment, cur_kv_head; CS349E lecture 11 04_flash_decoding.py, demo1_exact
+//     second observation). Keys are the M rows: S^T[key, col] = K_tile . Q^T, then
+//     O^T[dim, col] += V_tile^T . P^T; the score fragment turns into the P^T
 //     operand with one movmatrix transpose per 8x8 block, so P stays in
-//     registers.
+//     registers; with two n-tiles each K and V fragment feeds both.
 //   * One producer warp runs ahead of four consumer warps: it takes the next
 //     item from the queue, publishes its descriptor and bulk-copies its Q rows
 //     into shared memory, and streams the item's K and V tiles with TMA
@@ -27,7 +29,7 @@
 //     flash_decode_splitk.py, _splitk_stage1_kernel). At the end of an item
 //     the producer hands the consumers one ring stage instead of a tile, and
 //     the four warps merge their states through it in a fixed order (the
-//     result does not depend on timing).
+//     result does not depend on timing), one n-tile per round.
 //   * Split bounds are proportional: [L*s/S, L*(s+1)/S) in 64-bit integers
 //     (TileLang page, split segment). Keys of a stage past the split end are
 //     masked to -inf before the max, and their V rows are cleared in shared

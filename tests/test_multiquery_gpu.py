@@ -45,6 +45,8 @@ CASES = [
     ("short_seq_more_splits", 2, 3, 4, 1, 64, [2, 50], "f16", LAYOUT_VARLEN, 5, 0),
     ("tq16_g8", 1, 16, 16, 2, 128, [4096], "f16", LAYOUT_VARLEN, 8, 0),
     ("one_split_direct", 3, 2, 8, 2, 64, [1, 2, 3], "bf16", LAYOUT_VARLEN, 1, 0),
+    # 20 columns per KV head: a 16-column item and a 4-column one, over NaN-padded slabs
+    ("bhsd_g4_tq5", 2, 5, 16, 4, 128, [500, 37], "bf16", LAYOUT_BHSD, 3, 512),
 ]
 
 

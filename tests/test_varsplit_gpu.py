@@ -56,6 +56,8 @@ CASES = [
     ("bhsd_mha", 3, 16, 16, 128, [900, 33, 450], "f16", LAYOUT_BHSD, 256, 8, 1000),
     ("d64_group12", 4, 12, 1, 64, [70, 1, 260, 129], "bf16", LAYOUT_VARLEN, 64, 8, 0),
     ("one_split_each", 3, 8, 2, 128, [50, 60, 70], "f16", LAYOUT_VARLEN, 4096, 4, 0),
+    # 16 columns at head_dim 128: two n-tiles, with the per-sequence arrays in shared memory
+    ("group16_d128", 3, 32, 2, 128, [2000, 5, 700], "f16", LAYOUT_VARLEN, 256, 8, 0),
 ]
 
 
