@@ -232,8 +232,10 @@ int decode_attn_splitkv_varsplit_plan(int B, int Hq, int Hkv, int D, int64_t tot
  * out = 0). Splits still cut each sequence's whole range [0, L_b) as in
  * decode_attn_splitkv; a split holding no key a token may see is empty for
  * that token (lse = -inf, weight 0). The (token, head) pairs of one KV head's
- * group are packed together into the tensor-core columns, so with
- * G * T_q <= 8 each K/V byte is still read once. The pages' split kernel has
+ * group are packed together into the tensor-core columns (work items of 8
+ * columns, or of 16 when G * T_q > 8), so with G * T_q <= 16 each K/V byte is
+ * still read and multiplied once; more columns take several items, whose
+ * repeated reads of the same keys come mostly from L2. The pages' split kernel has
  * query blocking only in the official examples it refers to (TileLang page,
  * module docstring item 1); the masking follows its split segment's -inf rule.
  *   q, out         device, [B, T_q, Hq, D] elements of `dtype`, 16-byte aligned
