@@ -50,6 +50,9 @@ def parse():
     ap.add_argument("--varsplit", action="store_true",
                     help="per-sequence split counts (decode_attn_splitkv_varsplit) with its planner")
     ap.add_argument("--split-len", type=int, default=0, help="override the planner's split_len")
+    ap.add_argument("--cuda-core-math", action="store_true",
+                    help="time the split step with its products on CUDA-core fp32 FMAs instead of "
+                         "tensor cores (the comparison arm; uniform splits, one query token, G <= 8)")
     ap.add_argument("--fa2-style", action="store_true",
                     help="comparison: no split and one query head per unit (K/V repeated per "
                          "query head, as FlashAttention-style decode reads them); GB/s still "
@@ -315,8 +318,16 @@ def main():
     out = torch.empty(*p.q.shape, dtype=q.dtype, device=dev)
     ws = da.alloc_workspace(p.B * p.tq, p.Hq, p.D, S, device=dev, stream=stream)
 
+    if args.cuda_core_math and (split_len or p.tq > 1 or p.Hq // p.Hkv > 8):
+        raise SystemExit("--cuda-core-math takes uniform splits, one query token and G <= 8")
+
     def call():
-        if split_len:
+        if args.cuda_core_math:
+            da.decode_attn_splitkv_partial_cuda_core(q, k, v, cu, ws, num_splits=S, scale=p.scale,
+                                                     layout=p.layout, stream=stream)
+            if S > 1:
+                da.decode_attn_splitkv_combine(out, ws, num_splits=S, stream=stream)
+        elif split_len:
             da.decode_attn_splitkv_varsplit(q, k, v, cu, out, ws, split_len=split_len, max_splits=S,
                                             scale=p.scale, layout=p.layout, stream=stream)
         elif p.tq > 1:
@@ -352,8 +363,9 @@ def main():
             return step(ev0, ev1)   # these modes have no split-only entry point: time the call
         flush()
         ev0.record(stream)
-        da.decode_attn_splitkv_partial(q, k, v, cu, ws, num_splits=S, scale=p.scale,
-                                       layout=p.layout, stream=stream)
+        partial = (da.decode_attn_splitkv_partial_cuda_core if args.cuda_core_math
+                   else da.decode_attn_splitkv_partial)
+        partial(q, k, v, cu, ws, num_splits=S, scale=p.scale, layout=p.layout, stream=stream)
         ev1.record(stream)
         da.decode_attn_splitkv_combine(out, ws, num_splits=S, stream=stream)
 
@@ -393,7 +405,7 @@ def main():
 
     # ---- end to end through the public call, host buffers, copies inside each step
     e2e = None
-    if args.e2e_steps > 0:
+    if args.e2e_steps > 0 and not args.cuda_core_math:
         pq, pk, pv, pcu = hq.pin_memory(), hk.pin_memory(), hv.pin_memory(), hcu.pin_memory()
         hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
 
@@ -457,7 +469,7 @@ def main():
     q_bytes = p.B * p.tq * p.Hq * p.D * 2
     alg_bytes = p.kv_bytes + q_bytes + 4 * (p.B + 1) + ws_bytes
     achieved = alg_bytes / (split_mean_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(p.name, S)
+    traffic = None if args.cuda_core_math else recorded_traffic(p.name, S)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_step_ms, 5),
@@ -467,6 +479,8 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": p.dtype, "data": "synthetic (seeded N(0,1), rounded to the input dtype)",
         "config": {**workload_config(p, S),
+                   "products": ("CUDA-core fp32 FMA (comparison arm)" if args.cuda_core_math
+                                else "tensor-core mma.sync m16n8k16"),
                    **({"split_mode": "per-sequence", "split_len": split_len, "max_splits": S}
                       if split_len else {"split_mode": "uniform"})},
         "roofline": {"kernel": ("split_kernel" if not (split_len or p.tq > 1)
@@ -485,7 +499,7 @@ def main():
         "model_us": (round(da.model_us(p.lens, p.Hq, p.Hkv, p.D, S,
                                        torch.cuda.get_device_properties(dev).multi_processor_count,
                                        T_q=p.tq), 1)
-                     if not (split_len or args.fa2_style) else None),
+                     if not (split_len or args.fa2_style or args.cuda_core_math) else None),
         "wall_s_timed_region": round(t_wall, 3),
     }
     if sampler:

@@ -174,6 +174,21 @@ da_status decode_attn_splitkv_partial(const void* q, const void* k, const void* 
                                       size_t workspace_bytes, void* stream);
 
 /*
+ * The split step with its two products (q.k and p.v) on CUDA-core fp32 FMAs
+ * instead of tensor cores: the comparison arm for that design choice (the
+ * pages' kernels use tensor-core GEMMs for a packed group; this measures what
+ * plain FMAs reach on the same pipeline). Same arguments, workspace results
+ * and errors as decode_attn_splitkv_partial, plus DA_ERR_UNSUPPORTED when a KV
+ * head serves more than 8 query heads (Hq / Hkv > 8). The library's own calls
+ * never use it.
+ */
+da_status decode_attn_splitkv_partial_cuda_core(const void* q, const void* k, const void* v,
+                                                const int32_t* cu_seqlens_k, int B, int Hq, int Hkv,
+                                                int D, int kv_rows, da_dtype dtype, da_layout layout,
+                                                float scale, int num_splits, void* workspace,
+                                                size_t workspace_bytes, void* stream);
+
+/*
  * The combine step alone: merges lse_part/o_part from the workspace into
  * out[B, Hq, D]. The workspace must hold a split step's results for the same
  * B, Hq, D and num_splits. Errors as above.

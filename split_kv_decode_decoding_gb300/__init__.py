@@ -33,6 +33,7 @@ EXPORTED = [
     "decode_attn_splitkv_noalloc", "decode_attn_splitkv_varsplit",
     "decode_attn_splitkv_varsplit_plan", "decode_attn_splitkv_multiquery",
     "decode_attn_splitkv_model_us", "decode_attn_splitkv_model_best_splits",
+    "decode_attn_splitkv_partial_cuda_core",
 ]
 
 _lib = None
@@ -71,6 +72,8 @@ def load(path: str = LIB):
     lib.decode_attn_splitkv.restype = I
     lib.decode_attn_splitkv_partial.argtypes = [P, P, P, P, I, I, I, I, I, I, I, F, I, P, SZ, P]
     lib.decode_attn_splitkv_partial.restype = I
+    lib.decode_attn_splitkv_partial_cuda_core.argtypes = [P, P, P, P, I, I, I, I, I, I, I, F, I, P, SZ, P]
+    lib.decode_attn_splitkv_partial_cuda_core.restype = I
     lib.decode_attn_splitkv_combine.argtypes = [I, I, I, I, I, P, P, SZ, P]
     lib.decode_attn_splitkv_combine.restype = I
     lib.decode_attn_splitkv_get_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
@@ -262,6 +265,18 @@ def decode_attn_splitkv_partial(q, k, v, cu_seqlens_k, workspace, *, num_splits:
         _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_k), B, Hq, Hkv, D, kv_rows, _dtype_code(q),
         layout, sc, num_splits, _ptr(workspace), workspace.numel(), _stream(stream))
     _check(st, "decode_attn_splitkv_partial")
+
+
+def decode_attn_splitkv_partial_cuda_core(q, k, v, cu_seqlens_k, workspace, *, num_splits: int,
+                                          scale: float | None = None, layout: int = DA_LAYOUT_VARLEN,
+                                          stream=None):
+    """The split step with CUDA-core FMA products (comparison arm); see the C header."""
+    B, Hq, Hkv, D, kv_rows = _shape_args(q, k, cu_seqlens_k, layout)
+    sc = 1.0 / math.sqrt(D) if scale is None else scale
+    st = load().decode_attn_splitkv_partial_cuda_core(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_k), B, Hq, Hkv, D, kv_rows, _dtype_code(q),
+        layout, sc, num_splits, _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "decode_attn_splitkv_partial_cuda_core")
 
 
 def decode_attn_splitkv_combine(out, workspace, *, num_splits: int, stream=None):

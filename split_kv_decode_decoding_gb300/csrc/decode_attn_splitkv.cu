@@ -274,6 +274,30 @@ __device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4],
     }
 }
 
+// One 16-bit input element to fp32 (exact).
+template <int DT>
+__device__ __forceinline__ float bits_to_f32(uint32_t h) {
+    if constexpr (DT == DA_F16) {
+        float f;
+        asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(static_cast<uint16_t>(h)));
+        return f;
+    } else {
+        return __uint_as_float(h << 16);
+    }
+}
+
+// Eight 16-bit elements (one 16-byte shared-memory chunk) to fp32.
+template <int DT>
+__device__ __forceinline__ void chunk_to_f32(uint32_t addr, float (&f)[8]) {
+    uint32_t w[4];
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(addr));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        f[2 * j] = bits_to_f32<DT>(w[j] & 0xffffu);
+        f[2 * j + 1] = bits_to_f32<DT>(w[j] >> 16);
+    }
+}
+
 // Pack two fp32 values into one register of two 16-bit values (lo = a), RN.
 template <int DT>
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
@@ -420,7 +444,9 @@ __device__ __forceinline__ int64_t column_row(const SplitParams& p, const ItemSl
 }
 
 // ------------------------------------------------------------ split step
-template <int D, int DT, int NT>
+// MATH 0: tensor-core products (the library's path); 1: the same kernel with the
+// products on CUDA-core fp32 FMAs, kept as the comparison arm for that choice.
+template <int D, int DT, int NT, int MATH>
 __global__ void __launch_bounds__(kThreads, kMinBlocksPerSm)
 split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
              const __grid_constant__ CUtensorMap tmK16, const __grid_constant__ CUtensorMap tmV16,
@@ -441,6 +467,9 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
     // past the fixed layout: cu_seqlens_k [B + 1] (when staged), then prefix[B + 1] (per-sequence mode)
     int32_t* cus = p.stage_cu ? reinterpret_cast<int32_t*>(smem + Sh::kEnd) : nullptr;
     int32_t* prefix = reinterpret_cast<int32_t*>(smem + Sh::kEnd + (p.stage_cu ? kStagedBytes : 0));
+    // CUDA-core math only: per consumer warp, softmax weights [16 keys][8 columns] and 8 rescale factors
+    float* fma_p = reinterpret_cast<float*>(smem + Sh::kEnd + (p.stage_cu ? kStagedBytes : 0) +
+                                            (p.split_len != 0 ? kStagedBytes : 0));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -656,7 +685,241 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
             break;
         }
         const ItemSlot item = slots[slot];
-        if constexpr (NT == 1) {
+        if constexpr (MATH == 1) {
+        // ---- CUDA-core math (comparison arm): fp32 FMA dot products and PV for the
+        // item's live columns, over the same pipeline and merge as the tensor-core path
+            static_assert(NT == 1, "CUDA-core math handles items of up to 8 columns");
+            constexpr int kDpl = D / 32;               // dims per lane in the PV product
+            if (!item.valid) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(iempty0 + 8 * slot);
+                break;
+            }
+            const uint32_t qrows = qbuf + slot * Sh::kQBytes;    // Q rows [column][D] of this item
+            float* pw = fma_p + warp * 17 * 8;                   // [16 keys][8 columns], then [8]
+            const int c0 = 2 * t4, c1 = 2 * t4 + 1;              // this thread's score columns
+            const bool live0 = c0 < item.nh, live1 = c1 < item.nh;
+            int visA = item.nkeys, visB = item.nkeys;
+            if (p.tq > 1) {
+                visA = min(item.nkeys, item.vis0 + (item.c0 + c0) / p.G);
+                visB = min(item.nkeys, item.vis0 + (item.c0 + c1) / p.G);
+            }
+            float acc[8][kDpl];                                  // [column][dim kDpl * lane + j]
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+#pragma unroll
+                for (int j = 0; j < kDpl; ++j) acc[c][j] = 0.f;
+            float m_run[2] = {-INFINITY, -INFINITY};
+            float l_run[2] = {0.f, 0.f};
+            for (int t = 0; t < item.ntiles; ++t) {
+                const uint32_t fb = full0 + 8 * st;
+                if (ok && !mbar_wait_warp(fb, ph, p.wait_limit_ns)) {
+                    ok = false;
+                    bad_bar = fb;
+                    bad_ph = ph;
+                    if (lane == 0) flag_error(p.err, DA_DEVERR_TIMEOUT);
+                }
+                const int keys_t = min(kStageKeys, item.nkeys - t * kStageKeys);
+                bool zeroed = false;
+                if (ok && warp * kBoxKeys < keys_t) {
+                    const uint32_t kbase = ring + st * Sh::kStageBytes;
+                    const uint32_t vbase = kbase + Sh::kTileBytes;
+                    const int valid_rows = keys_t - warp * kBoxKeys;
+                    if (valid_rows < kBoxKeys) {
+                        const int per_row = Sh::kHalves * 8;
+                        for (int c = lane; c < (kBoxKeys - valid_rows) * per_row; c += 32) {
+                            const int r = valid_rows + c / per_row;
+                            const int hf = (c % per_row) >> 3, ch = c & 7;
+                            const uint32_t addr = vbase + hf * Sh::kSliceBytes + (warp * kBoxKeys + r) * 128 + ch * 16;
+                            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+                        }
+                        zeroed = true;
+                        __syncwarp();
+                    }
+                    // scores of keys g and g + 8 of this warp's 16 against columns c0, c1
+                    const int r0 = warp * kBoxKeys + g, r1 = r0 + 8;
+                    float s00 = 0.f, s01 = 0.f, s10 = 0.f, s11 = 0.f;
+#pragma unroll 4
+                    for (int ch = 0; ch < D / 8; ++ch) {
+                        const int hf = ch >> 3, cc = ch & 7;
+                        float k0[8], k1[8];
+                        chunk_to_f32<DT>(kbase + hf * Sh::kSliceBytes + r0 * 128 + ((cc ^ (r0 & 7)) << 4), k0);
+                        chunk_to_f32<DT>(kbase + hf * Sh::kSliceBytes + r1 * 128 + ((cc ^ (r1 & 7)) << 4), k1);
+                        if (live0) {
+                            float q[8];
+                            chunk_to_f32<DT>(qrows + c0 * D * 2 + ch * 16, q);
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                s00 = fmaf(q[j], k0[j], s00);
+                                s10 = fmaf(q[j], k1[j], s10);
+                            }
+                        }
+                        if (live1) {
+                            float q[8];
+                            chunk_to_f32<DT>(qrows + c1 * D * 2 + ch * 16, q);
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                s01 = fmaf(q[j], k0[j], s01);
+                                s11 = fmaf(q[j], k1[j], s11);
+                            }
+                        }
+                    }
+                    const int key_lo = t * kStageKeys + warp * kBoxKeys + g;
+                    const float x0 = key_lo < visA ? s00 * p.scale_log2 : -INFINITY;
+                    const float x1 = key_lo < visB ? s01 * p.scale_log2 : -INFINITY;
+                    const float x2 = key_lo + 8 < visA ? s10 * p.scale_log2 : -INFINITY;
+                    const float x3 = key_lo + 8 < visB ? s11 * p.scale_log2 : -INFINITY;
+                    float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+                    for (int off = 4; off < 32; off <<= 1) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                    }
+                    const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
+                    const float ms0 = mn0 == -INFINITY ? 0.f : mn0, ms1 = mn1 == -INFINITY ? 0.f : mn1;
+                    const float p0 = fast_exp2(x0 - ms0), p1 = fast_exp2(x1 - ms1);
+                    const float p2 = fast_exp2(x2 - ms0), p3 = fast_exp2(x3 - ms1);
+                    const bool moved = mn0 != m_run[0] || mn1 != m_run[1];
+                    const float al0 = moved ? fast_exp2(m_run[0] - ms0) : 1.f;
+                    const float al1 = moved ? fast_exp2(m_run[1] - ms1) : 1.f;
+                    l_run[0] = l_run[0] * al0 + p0 + p2;
+                    l_run[1] = l_run[1] * al1 + p1 + p3;
+                    m_run[0] = mn0;
+                    m_run[1] = mn1;
+                    // every lane's PV needs the weights of all 16 keys and 8 columns: through shared memory
+                    pw[g * 8 + c0] = p0;
+                    pw[g * 8 + c1] = p1;
+                    pw[(g + 8) * 8 + c0] = p2;
+                    pw[(g + 8) * 8 + c1] = p3;
+                    if (g == 0) {
+                        pw[16 * 8 + c0] = al0;
+                        pw[16 * 8 + c1] = al1;
+                    }
+                    __syncwarp();
+                    if (__any_sync(0xffffffffu, moved)) {
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const float a = pw[16 * 8 + c];
+#pragma unroll
+                            for (int j = 0; j < kDpl; ++j) acc[c][j] *= a;
+                        }
+                    }
+                    // O[column, dims kDpl * lane ..] += p[key, column] * V[key, dims], one key at a time
+                    const int nk = min(kBoxKeys, valid_rows);
+                    const int d0 = kDpl * lane;
+                    const int ch = d0 >> 3;                                // 16-byte chunk of the row
+                    for (int kk = 0; kk < nk; ++kk) {
+                        const int r = warp * kBoxKeys + kk;
+                        const uint32_t vaddr = vbase + (ch >> 3) * Sh::kSliceBytes + r * 128 +
+                                               (((ch & 7) ^ (r & 7)) << 4) + (d0 & 7) * 2;
+                        float v[kDpl];
+                        if constexpr (kDpl == 4) {
+                            uint32_t w0, w1;
+                            asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(w0), "=r"(w1) : "r"(vaddr));
+                            v[0] = bits_to_f32<DT>(w0 & 0xffffu);
+                            v[1] = bits_to_f32<DT>(w0 >> 16);
+                            v[2] = bits_to_f32<DT>(w1 & 0xffffu);
+                            v[3] = bits_to_f32<DT>(w1 >> 16);
+                        } else {
+                            uint32_t w0;
+                            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w0) : "r"(vaddr));
+                            v[0] = bits_to_f32<DT>(w0 & 0xffffu);
+                            v[1] = bits_to_f32<DT>(w0 >> 16);
+                        }
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            if (c < item.nh) {
+                                const float pc = pw[kk * 8 + c];
+#pragma unroll
+                                for (int j = 0; j < kDpl; ++j) acc[c][j] = fmaf(pc, v[j], acc[c][j]);
+                            }
+                        }
+                    }
+                    __syncwarp();   // the weights are read before the next stage rewrites them
+                }
+                if (zeroed) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty0 + 8 * st);
+                if (++st == kStages) {
+                    st = 0;
+                    ph ^= 1;
+                }
+            }
+            // the item's Q rows are no longer read: release its descriptor slot
+            __syncwarp();
+            if (lane == 0) mbar_arrive(iempty0 + 8 * slot);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], off);
+                l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], off);
+            }
+            if (ok && !mbar_wait_warp(full0 + 8 * st, ph, p.wait_limit_ns)) {
+                ok = false;
+                if (lane == 0) flag_error(p.err, DA_DEVERR_TIMEOUT);
+            }
+            float* red_acc = reinterpret_cast<float*>(smem + st * Sh::kStageBytes);   // [warp][8][D+4]
+            float* red_m = red_acc + kConsumerWarps * 8 * Sh::kMergeRow;               // [warp][8]
+            float* red_l = red_m + kConsumerWarps * 8;                                  // [warp][8]
+            if (g == 0) {
+                red_m[warp * 8 + c0] = m_run[0];
+                red_m[warp * 8 + c1] = m_run[1];
+                red_l[warp * 8 + c0] = l_run[0];
+                red_l[warp * 8 + c1] = l_run[1];
+            }
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+#pragma unroll
+                for (int j = 0; j < kDpl; ++j) red_acc[(warp * 8 + c) * Sh::kMergeRow + kDpl * lane + j] = acc[c][j];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(mfull);
+            if (ok && !mbar_wait_warp(mfull, it & 1, p.wait_limit_ns)) {
+                ok = false;
+                if (lane == 0) flag_error(p.err, DA_DEVERR_TIMEOUT);
+            }
+            constexpr int kLanesPerHead = D / 4;
+            constexpr int kHeadsPerPass = 32 / kLanesPerHead;
+            constexpr int kPasses = (8 / kConsumerWarps) / kHeadsPerPass;
+            const int d4 = (lane % kLanesPerHead) * 4;
+#pragma unroll
+            for (int pass = 0; pass < kPasses; ++pass) {
+                const int hh = warp + kConsumerWarps * (pass * kHeadsPerPass + lane / kLanesPerHead);
+                const bool live = hh < item.nh;
+                float mw[kConsumerWarps];
+                float M = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) {
+                    mw[w] = red_m[w * 8 + hh];
+                    M = fmaxf(M, mw[w]);
+                }
+                const float Ms = M == -INFINITY ? 0.f : M;
+                float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+                float lsum = 0.f;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) {
+                    const float wt = fast_exp2(mw[w] - Ms);
+                    lsum = fmaf(wt, red_l[w * 8 + hh], lsum);
+                    const float4 a = *reinterpret_cast<const float4*>(red_acc + (w * 8 + hh) * Sh::kMergeRow + d4);
+                    o.x = fmaf(wt, a.x, o.x);
+                    o.y = fmaf(wt, a.y, o.y);
+                    o.z = fmaf(wt, a.z, o.z);
+                    o.w = fmaf(wt, a.w, o.w);
+                }
+                const float inv = M == -INFINITY ? 0.f : fast_rcp(lsum);
+                o.x *= inv;
+                o.y *= inv;
+                o.z *= inv;
+                o.w *= inv;
+                if (live) {
+                    const int64_t qrow = column_row(p, item, hh);
+                    const int64_t row = qrow * p.S + item.s;
+                    *reinterpret_cast<float4*>(p.opart + row * D + d4) = o;
+                    if (d4 == 0) p.lse[row] = M == -INFINITY ? -INFINITY : (M + fast_log2(lsum)) * kLn2;
+                    if (p.out != nullptr)
+                        *reinterpret_cast<uint2*>(p.out + qrow * D + d4) =
+                            make_uint2(pack2<DT>(o.x, o.y), pack2<DT>(o.z, o.w));
+                }
+            }
+        } else if constexpr (NT == 1) {
         // ---- one n-tile (up to 8 columns per item)
             // Q^T fragments (B operand, k16 x n8): head g, dims ks*16 + 2*t4 (+1) and +8 (+9).
             uint32_t qf[D / 16][2];
@@ -1411,6 +1674,7 @@ struct Call {
     int S;           // splits per sequence, or the cap of S_b in per-sequence mode
     int split_len;   // 0: S splits for every sequence; else per-sequence S_b
     int tq;          // query tokens per sequence
+    int math;        // 0: tensor-core products; 1: CUDA-core FMAs (comparison arm)
     void* ws;
 };
 
@@ -1418,7 +1682,7 @@ constexpr int kMaxVarsplitBatch = 1024;                                   // seq
 constexpr double kLongStreamBytes = 1.5e9;   // K/V bytes above which even batches are split for balance
 
 // `out` is written by the split kernel itself only with one uniform split.
-template <int D, int DT, int NT>
+template <int D, int DT, int NT, int MATH>
 da_status launch_split(const Call& c, void* out, cudaStream_t stream) {
     // 64-key boxes for full stages, 16-key boxes for the ragged end of a split
     alignas(64) CUtensorMap mk, mv, mk16, mv16;
@@ -1461,8 +1725,9 @@ da_status launch_split(const Call& c, void* out, cudaStream_t stream) {
     p.wait_limit_ns = kWaitLimitNs;
 
     const bool var = c.split_len != 0;
-    const int smem = Shape<D, NT>::kSmemBytes + (p.stage_cu ? kStagedBytes : 0) + (var ? kStagedBytes : 0);
-    auto kern = split_kernel<D, DT, NT>;
+    const int smem = Shape<D, NT>::kSmemBytes + (p.stage_cu ? kStagedBytes : 0) + (var ? kStagedBytes : 0) +
+                     (MATH == 1 ? kConsumerWarps * 17 * 8 * 4 : 0);
+    auto kern = split_kernel<D, DT, NT, MATH>;
     static DeviceCache caches[3];   // by the number of staged [B + 1] arrays
     int grid = 0;
     if (persistent_grid(kern, smem, caches[(p.stage_cu ? 1 : 0) + (var ? 1 : 0)], &grid) != cudaSuccess)
@@ -1516,9 +1781,10 @@ da_status launch_combine(const Call& c, void* out, cudaStream_t stream) {
 
 template <int D, int DT>
 da_status launch_split_cols(const Call& c, void* out, cudaStream_t st) {
-    if (item_cols(static_cast<int64_t>(c.Hq / c.Hkv) * c.tq) > kHeadsPerCta)
-        return launch_split<D, DT, 2>(c, out, st);
-    return launch_split<D, DT, 1>(c, out, st);
+    const bool wide = item_cols(static_cast<int64_t>(c.Hq / c.Hkv) * c.tq) > kHeadsPerCta;
+    if (c.math == 1) return wide ? DA_ERR_UNSUPPORTED : launch_split<D, DT, 1, 1>(c, out, st);
+    if (wide) return launch_split<D, DT, 2, 0>(c, out, st);
+    return launch_split<D, DT, 1, 0>(c, out, st);
 }
 
 da_status dispatch_split(const Call& c, void* out, cudaStream_t st) {
@@ -1544,6 +1810,7 @@ Call make_call(const void* q, const void* k, const void* v, const int32_t* cu, i
                int kv_rows, da_dtype dt, da_layout lay, float scale, int S, int split_len, void* ws, int tq = 1) {
     Call c;
     c.tq = tq;
+    c.math = 0;
     c.q = q;
     c.k = k;
     c.v = v;
@@ -1660,6 +1927,21 @@ da_status decode_attn_splitkv_partial(const void* q, const void* k, const void* 
     return dispatch_split(make_call(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale,
                                     num_splits, 0, workspace),
                           nullptr, static_cast<cudaStream_t>(stream));
+}
+
+da_status decode_attn_splitkv_partial_cuda_core(const void* q, const void* k, const void* v,
+                                                const int32_t* cu_seqlens_k, int B, int Hq, int Hkv, int D,
+                                                int kv_rows, da_dtype dtype, da_layout layout, float scale,
+                                                int num_splits, void* workspace, size_t workspace_bytes,
+                                                void* stream) {
+    da_status st = check_common(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale,
+                                num_splits, workspace, workspace_bytes);
+    if (st != DA_OK) return st;
+    if (Hq / Hkv > kHeadsPerCta) return DA_ERR_UNSUPPORTED;
+    Call c = make_call(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale, num_splits, 0,
+                       workspace);
+    c.math = 1;
+    return dispatch_split(c, nullptr, static_cast<cudaStream_t>(stream));
 }
 
 da_status decode_attn_splitkv_combine(int B, int Hq, int D, int num_splits, da_dtype dtype, void* out,
