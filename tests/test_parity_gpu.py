@@ -201,6 +201,13 @@ def test_large_batch_reads_cu_from_global_memory():
     check_full(p, 2)
 
 
+def test_maximum_split_count_on_a_long_sequence():
+    """num_splits = DA_MAX_SPLITS on 131072 keys: 128-key splits, and a combine over 1024
+    partials per row (the combine kernel's widest reduction)."""
+    p = custom("maxS", 1, 8, 2, 128, [131072], "bf16", LAYOUT_VARLEN, da.DA_MAX_SPLITS, seed=22)
+    check_full(p, da.DA_MAX_SPLITS)
+
+
 def test_empty_cache_without_kv_buffers():
     """kv_rows = 0: every sequence is empty, K/V may be NULL; out = 0, every lse = -inf."""
     B, Hq, D, S = 3, 8, 128, 2
