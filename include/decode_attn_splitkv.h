@@ -339,8 +339,10 @@ da_status decode_attn_splitkv_noalloc(const void* q, const void* k, const void* 
  * largest item's bytes (kappa charges the last item for unequal CTA rates);
  * W_ws = B*T_q*Hq*S*(D+1)*4 workspace bytes combined.
  *   kv_lens   host, int32 [B] sequence lengths (negative counts as 0)
- *   params    host, double[7] {t0 us, t_item us, r_cta B/us, bw B/us, t_comb us,
- *             bw_comb B/us, kappa}, or NULL for the built-in GB300 calibration
+ *   params    host, double[8] {t0 us, t_item us, r_cta B/us, bw B/us, t_comb us,
+ *             bw_comb B/us, kappa, r_cta2 B/us}, or NULL for the built-in GB300
+ *             calibration; r_cta2 replaces r_cta for items of 16 columns
+ *             (G * T_q > 8), which carry twice the products per key
  * Returns the predicted time, or a negative value if an argument is out of range.
  */
 double decode_attn_splitkv_model_us(const int32_t* kv_lens, int B, int Hq, int Hkv, int D, int T_q,

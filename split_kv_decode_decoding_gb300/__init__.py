@@ -147,13 +147,13 @@ def split_range(L: int, S: int, s: int) -> tuple:
 
 def model_us(lens, Hq: int, Hkv: int, D: int, num_splits: int, sm_count: int, T_q: int = 1,
              params=None) -> float:
-    """Predicted µs of one call (the GB300 time model; params: 7 values as in the C header,
+    """Predicted µs of one call (the GB300 time model; params: 8 values as in the C header,
     None = the built-in calibration)."""
     import numpy as np
     ln = np.ascontiguousarray(lens, dtype=np.int32)
     pa = None if params is None else np.ascontiguousarray(params, dtype=np.float64)
-    if pa is not None and pa.size != 7:
-        raise ValueError("model_us takes 7 parameters")
+    if pa is not None and pa.size != 8:
+        raise ValueError("model_us takes 8 parameters")
     return load().decode_attn_splitkv_model_us(ln.ctypes.data, ln.size, Hq, Hkv, D, T_q, num_splits,
                                                sm_count, None if pa is None else pa.ctypes.data)
 

@@ -1,11 +1,12 @@
 """Calibrate the library's GB300 time model and the split-count picker on this GPU.
 
-    python -m split_kv_decode_decoding_gb300.calibrate sweep --out sweep.json [--workloads a,b]
+    python -m split_kv_decode_decoding_gb300.calibrate sweep --out sweep.json [--workloads a,b | --multiquery]
         call time against split count for the named workloads (GPU): L2 flushed before
         every call (a write of twice the L2 size, then a read of another such buffer),
-        CUDA events on the launching stream, median of --reps calls
-    python -m split_kv_decode_decoding_gb300.calibrate fit sweep.json
-        least-squares fit (in log time) of the 7 model parameters of
+        CUDA events on the launching stream, median of --reps calls; --multiquery sweeps
+        the workloads with 2 or 4 new tokens per sequence
+    python -m split_kv_decode_decoding_gb300.calibrate fit sweep.json [more.json ...]
+        least-squares fit (in log time) of the 8 model parameters of
         decode_attn_splitkv_model_us to the calls within 30 % of their workload's
         fastest split count (CPU); prints the parameters and the errors
     python -m split_kv_decode_decoding_gb300.calibrate fa2 --out fa2.json
@@ -32,6 +33,10 @@ WORKLOADS = [
     "codellama_B4_S16384", "codellama_B1_S65536", "codellama_B1_S131072", "llama_S1024_B1", "llama_S1024_B16",
     "llama_S8192_B1", "llama_S8192_B16", "llama_S32768_B1", "llama_S32768_B16", "llama_S131072_B1",
     "llama_S131072_B16", "llama_skewed"]
+# several new tokens per sequence (decode_attn_splitkv_multiquery), 8- and 16-column items
+MULTIQUERY_WORKLOADS = [
+    "qwen_varlen_tq2", "qwen_varlen_tq4", "llama_S8192_B16_tq2", "llama_S8192_B16_tq4", "llama_S32768_B16_tq2",
+    "llama_S32768_B16_tq4", "llama_S131072_B1_tq4", "codellama_B16_S4096_tq2", "llama_S8192_B1_tq4"]
 
 
 class _Timer:
@@ -140,13 +145,15 @@ def _log_err(args):
     return e
 
 
-def fit(path: str, within: float = 1.3, workers: int = 8) -> dict:
+def fit(paths, within: float = 1.3, workers: int = 8) -> dict:
     import multiprocessing as mp
 
     import numpy as np
     from scipy.optimize import minimize
     load()
-    d = json.load(open(path))
+    d = {}
+    for path in ([paths] if isinstance(paths, str) else paths):
+        d.update(json.load(open(path)))
     pts, allpts = [], []
     for name, r in d.items():
         best = min(r["t"].values())
@@ -161,7 +168,7 @@ def fit(path: str, within: float = 1.3, workers: int = 8) -> dict:
         params = [math.exp(v) for v in x]
         return sum(pool.map(_log_err, [(params, c) for c in chunks]))
 
-    x = [math.log(v) for v in (13.73, 0.2623, 72540, 7.459e6, 0.07119, 1.083e6, 0.04376)]
+    x = [math.log(v) for v in (13.73, 0.2623, 72540, 7.459e6, 0.07119, 1.083e6, 0.04376, 50000)]
     best = None
     for _ in range(3):
         res = minimize(loss, x if best is None else best.x, method="Nelder-Mead",
@@ -219,16 +226,17 @@ def main(argv=None) -> None:
     a = sub.add_parser("sweep")
     a.add_argument("--out", required=True)
     a.add_argument("--workloads", default=",".join(WORKLOADS))
+    a.add_argument("--multiquery", action="store_true")
     a.add_argument("--reps", type=int, default=25)
     b = sub.add_parser("fit")
-    b.add_argument("sweep_json")
+    b.add_argument("sweep_json", nargs="+")
     b.add_argument("--within", type=float, default=1.3)
     c = sub.add_parser("fa2")
     c.add_argument("--out", required=True)
     c.add_argument("--reps", type=int, default=40)
     args = ap.parse_args(argv)
     if args.cmd == "sweep":
-        sweep(args.workloads.split(","), args.reps, args.out)
+        sweep(MULTIQUERY_WORKLOADS if args.multiquery else args.workloads.split(","), args.reps, args.out)
     elif args.cmd == "fit":
         fit(args.sweep_json, args.within)
     else:

@@ -2092,20 +2092,23 @@ const char* decode_attn_splitkv_status_string(da_status status) {
 // where makespan is a processor-sharing run of the work items, in queue order,
 // over the persistent CTAs: each CTA spends t_item before an item and then
 // streams its bytes (each split's key count rounded up to the 16-key TMA box)
-// at min(r_cta, bw / streaming CTAs); kappa charges the last item for the CTAs'
-// unequal rates, and W_ws is the workspace bytes the combine reads. Fitted (least
-// squares in log time) on one GB300 to the 203 calls, of 357 measured (17
-// workloads of the CodeLlama, Llama, Qwen and MHA shapes x split counts 1 to
-// 256, L2 flushed, CUDA-event median per call), that lie within 30 % of their
-// workload's fastest split count: median error 2.6 %, 90th percentile 6.1 %.
-static const double kModelGb300[7] = {
-    /* t0 us      */ 13.73,
-    /* t_item us  */ 0.2623,
-    /* r_cta B/us */ 72540,
-    /* bw B/us    */ 7.459e+06,
-    /* t_comb us  */ 0.07119,
-    /* bw_comb    */ 1.083e+06,
-    /* kappa      */ 0.04376};
+// at min(r_cta, bw / streaming CTAs), r_cta being one CTA's rate for 8-column
+// items and r_cta2 for 16-column ones; kappa charges the last item for the
+// CTAs' unequal rates, and W_ws is the workspace bytes the combine reads.
+// Fitted (least squares in log time) on one GB300 to the 309 calls, of 546
+// measured (17 single-token workloads of the CodeLlama, Llama, Qwen and MHA
+// shapes and 9 of them with 2 or 4 new tokens x split counts 1 to 256, L2
+// flushed, CUDA-event median per call), that lie within 30 % of their
+// workload's fastest split count: median error 3.1 %, 90th percentile 11.8 %.
+static const double kModelGb300[8] = {
+    /* t0 us       */ 12.34,
+    /* t_item us   */ 0.06824,
+    /* r_cta B/us  */ 76500,
+    /* bw B/us     */ 7.655e+06,
+    /* t_comb us   */ 2.450,
+    /* bw_comb     */ 7.553e+05,
+    /* kappa       */ 0.05017,
+    /* r_cta2 B/us */ 45140};
 
 double decode_attn_splitkv_model_us(const int32_t* kv_lens, int B, int Hq, int Hkv, int D, int T_q, int num_splits,
                                     int sm_count, const double* params) {
@@ -2113,7 +2116,10 @@ double decode_attn_splitkv_model_us(const int32_t* kv_lens, int B, int Hq, int H
         num_splits < 1 || num_splits > DA_MAX_SPLITS || sm_count < 1)
         return -1.0;
     const double* m = params ? params : kModelGb300;
-    const double t0 = m[0], t_item = m[1], r_cta = m[2], bw = m[3], t_comb = m[4], bw_comb = m[5], kappa = m[6];
+    const double t0 = m[0], t_item = m[1], bw = m[3], t_comb = m[4], bw_comb = m[5], kappa = m[6];
+    // one CTA's streaming cap: 16-column items carry twice the products per key
+    const bool wide = item_cols(static_cast<int64_t>(Hq / Hkv) * T_q) > kHeadsPerCta;
+    const double r_cta = wide ? m[7] : m[2];
     if (!(r_cta > 0) || !(bw > 0) || !(bw_comb > 0) || !(t_item >= 0) || !(kappa >= 0)) return -1.0;
     const int S = num_splits;
     const int chunks = static_cast<int>(item_chunks(static_cast<int64_t>(Hq / Hkv) * T_q));

@@ -239,7 +239,7 @@ def test_time_model_formula_by_hand(lib):
     4 us, so the makespan is 5 us. The last-item term is 0.5 * 262144 / (1e6 / 2) =
     0.262144 us; workspace 1*1*1*2*129*4 = 1032 B. T = 5 + 5 + 0.262144 + 2 + 0.001032.
     """
-    params = [5.0, 1.0, 65536.0, 1e6, 2.0, 1e6, 0.5]
+    params = [5.0, 1.0, 65536.0, 1e6, 2.0, 1e6, 0.5, 32768.0]
     t = da.model_us([1000], 1, 1, 128, 2, 152, params=params)
     assert abs(t - (5 + 5 + 0.262144 + 2 + 0.001032)) < 1e-9
     # one split: no combine term, one 1008-key item (1000 rounded up): 1 + 1008*512/65536,
@@ -249,7 +249,7 @@ def test_time_model_formula_by_hand(lib):
     # bandwidth-bound: four items streaming together share bw = 1e5 B/us (25000 each,
     # below r_cta): 1 + 262144 / 25000 us; last-item term 0.5 * 262144 / 25000; the
     # combine reads 2*1*2*129*4 = 2064 B
-    params_bw = [5.0, 1.0, 65536.0, 1e5, 2.0, 1e6, 0.5]
+    params_bw = [5.0, 1.0, 65536.0, 1e5, 2.0, 1e6, 0.5, 32768.0]
     t4 = da.model_us([1000, 1000], 1, 1, 128, 2, 152, params=params_bw)
     assert abs(t4 - (5 + 1 + 262144 / 25000 + 0.5 * 262144 / 25000 + 2 + 0.002064)) < 1e-9
 
