@@ -215,6 +215,27 @@ def cpu_oracle_sample(p, budget_s: float = 12.0, steps=None):
     return n, nrows, cores
 
 
+def cpu_oracle_one_thread(p, budget_s: float = 4.0):
+    """The float64 oracle on one thread over (b, h) rows of the workload: returns (GB/s, desc)."""
+    import numpy as np
+
+    import oracle
+    orc = oracle.default()
+    rows_b = np.repeat(np.arange(p.B), p.Hq).astype(np.int32)
+    rows_h = np.tile(np.arange(p.Hq), p.B).astype(np.int32)
+    nrows = rows_b.size
+    t0 = time.perf_counter()
+    orc.attention_rows(p, rows_b[:1], rows_h[:1], nthreads=1)
+    per_row = max(time.perf_counter() - t0, 1e-6)
+    n = max(1, min(nrows, int(budget_s / per_row)))
+    sel = np.linspace(0, nrows - 1, n).astype(np.int64)
+    t0 = time.perf_counter()
+    orc.attention_rows(p, rows_b[sel], rows_h[sel], nthreads=1)
+    dt = time.perf_counter() - t0
+    gbs = p.kv_bytes * (n / nrows) / dt / 1e9
+    return gbs, f"{n} of {nrows} (b, h) rows, float64, 1 thread, {dt:.2f} s wall"
+
+
 def run_reference(args, p, ws_, rank):
     """--impl reference: the float64 oracle alone, each step a bounded sample of rows."""
     import numpy as np
@@ -395,6 +416,19 @@ def main():
             sampler.__exit__(None, None, None)
         if world > 1:
             torch.distributed.barrier()
+    # back-to-back calls, no flush between them (after the timed region, not part of it):
+    # what a decode loop sees; the inputs stay in HBM only when they exceed the L2
+    n_b2b = min(args.steps, 200)
+    with torch.cuda.stream(stream):
+        b0 = torch.cuda.Event(enable_timing=True)
+        b1 = torch.cuda.Event(enable_timing=True)
+        flush()
+        b0.record(stream)
+        for _ in range(n_b2b):
+            call()
+        b1.record(stream)
+        torch.cuda.synchronize(dev)
+    b2b_ms = b0.elapsed_time(b1) / n_b2b
     if da.decode_attn_splitkv_get_error(ws, stream=stream) != 0:
         raise RuntimeError("device error flag set during the timed steps")
     step_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(args.steps)]
@@ -494,6 +528,10 @@ def main():
                      "launches_timed": k_split,
                      **({"combine_us_mean_derived": round((mean_step_ms - split_mean_ms) * 1e3, 2)}
                         if per_call == 2 and not (split_len or p.tq > 1) else {})},
+        "back_to_back": {"us_per_call": round(b2b_ms * 1e3, 2),
+                         "value": round(world * kv_bytes_gqa / (b2b_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+                         "calls": n_b2b, "inputs_exceed_l2": p.kv_bytes > l2,
+                         "note": "calls back to back without an L2 flush, after the timed region"},
         "e2e": e2e,
         "gpu_launches": per_call * args.steps + per_split_step * k_split,
         "model_us": (round(da.model_us(p.lens, p.Hq, p.Hkv, p.D, S,
@@ -506,8 +544,10 @@ def main():
         line["clocks"] = sampler.summary()
     if not args.no_cpu_baseline and world == 1:
         gbs, cores, desc, _ = cpu_oracle_sample(p)
+        gbs1, desc1 = cpu_oracle_one_thread(p)
         line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores,
-                                "kind": "oracle", "sample": desc}
+                                "kind": "oracle", "sample": desc,
+                                "one_thread": {"value": round(gbs1, 4), "unit": "GB/s", "sample": desc1}}
     print(json.dumps(line), flush=True)
 
 
