@@ -74,6 +74,7 @@ constexpr int kStages = 3;          // pipeline depth (two CTAs per SM at head_d
 constexpr int kPrefetchStages = 4;  // BHSD: first stages pulled into L2 while cu_seqlens_k is read
 constexpr int kMinBlocksPerSm = 2;
 constexpr int kItemSlots = 2;       // item descriptors the producer may run ahead
+constexpr float kLazyRescale = 8.f; // 16-column items: headroom (log2) before the running max moves
 constexpr size_t kHeaderBytes = 256;
 constexpr size_t kWorkCounterOff = 64;   // header: uint32 work-queue head
 constexpr size_t kDoneCounterOff = 128;  // header: uint32 count of CTAs finished
@@ -1245,19 +1246,23 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
                         const float x1 = key_lo < visB[n] ? (sc[n][1] + sd[n][1]) * p.scale_log2 : -INFINITY;
                         const float x2 = key_lo + 8 < visA[n] ? (sc[n][2] + sd[n][2]) * p.scale_log2 : -INFINITY;
                         const float x3 = key_lo + 8 < visB[n] ? (sc[n][3] + sd[n][3]) * p.scale_log2 : -INFINITY;
+                        // Lazy reference: a column's running max m_run moves only when some score
+                        // of the warp's box exceeds it by more than kLazyRescale (log2 units), so
+                        // the shuffle reduction and the accumulator rescale run on a few boxes
+                        // per item; the weights stay below 2^kLazyRescale, well inside the fp16
+                        // and bf16 range, and every sum below shares the same reference.
                         float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+                        if (__any_sync(0xffffffffu, mx0 > m_run[n][0] + kLazyRescale ||
+                                                        mx1 > m_run[n][1] + kLazyRescale)) {
     #pragma unroll
-                        for (int off = 4; off < 32; off <<= 1) {
-                            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-                        }
-                        const float mn0 = fmaxf(m_run[n][0], mx0), mn1 = fmaxf(m_run[n][1], mx1);
-                        // a column that has seen no key yet (several query tokens) keeps -inf: use 0 as
-                        // its reference so that every weight below is 0 rather than NaN
-                        const float ms0 = mn0 == -INFINITY ? 0.f : mn0, ms1 = mn1 == -INFINITY ? 0.f : mn1;
-                        const float p0 = fast_exp2(x0 - ms0), p1 = fast_exp2(x1 - ms1);
-                        const float p2 = fast_exp2(x2 - ms0), p3 = fast_exp2(x3 - ms1);
-                        if (mn0 != m_run[n][0] || mn1 != m_run[n][1]) {
+                            for (int off = 4; off < 32; off <<= 1) {
+                                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                            }
+                            const float mn0 = fmaxf(m_run[n][0], mx0), mn1 = fmaxf(m_run[n][1], mx1);
+                            // a column that has seen no key yet (several query tokens) keeps -inf:
+                            // 0 stands in as its reference so that no weight below is NaN
+                            const float ms0 = mn0 == -INFINITY ? 0.f : mn0, ms1 = mn1 == -INFINITY ? 0.f : mn1;
                             const float al0 = fast_exp2(m_run[n][0] - ms0), al1 = fast_exp2(m_run[n][1] - ms1);
                             l_run[n][0] *= al0;
                             l_run[n][1] *= al1;
@@ -1271,6 +1276,10 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
                             m_run[n][0] = mn0;
                             m_run[n][1] = mn1;
                         }
+                        const float ms0 = m_run[n][0] == -INFINITY ? 0.f : m_run[n][0];
+                        const float ms1 = m_run[n][1] == -INFINITY ? 0.f : m_run[n][1];
+                        const float p0 = fast_exp2(x0 - ms0), p1 = fast_exp2(x1 - ms1);
+                        const float p2 = fast_exp2(x2 - ms0), p3 = fast_exp2(x3 - ms1);
                         l_run[n][0] += p0 + p2;
                         l_run[n][1] += p1 + p3;
                         // P^T operand (k16 keys x n8 columns) via 8x8 transposes of the score fragment
