@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--cuda-core-math", action="store_true",
                     help="time the split step with its products on CUDA-core fp32 FMAs instead of "
                          "tensor cores (the comparison arm; uniform splits, one query token, G <= 8)")
+    ap.add_argument("--tmem-math", action="store_true",
+                    help="run the tcgen05 / tensor-memory comparison arm (G * T_q > 8, G <= 32)")
     ap.add_argument("--fa2-style", action="store_true",
                     help="comparison: no split and one query head per unit (K/V repeated per "
                          "query head, as FlashAttention-style decode reads them); GB/s still "
@@ -341,9 +343,17 @@ def main():
 
     if args.cuda_core_math and (split_len or p.tq > 1 or p.Hq // p.Hkv > 8):
         raise SystemExit("--cuda-core-math takes uniform splits, one query token and G <= 8")
+    if args.tmem_math and (split_len or args.cuda_core_math or (p.Hq // p.Hkv) * p.tq <= 8
+                           or p.Hq // p.Hkv > 32):
+        raise SystemExit("--tmem-math takes uniform splits and G * T_q > 8 with G <= 32")
+    q4 = q.view(p.B, p.tq, p.Hq, p.D)
+    out4 = out.view(p.B, p.tq, p.Hq, p.D)
 
     def call():
-        if args.cuda_core_math:
+        if args.tmem_math:
+            da.decode_attn_splitkv_multiquery_tmem(q4, k, v, cu, out4, ws, num_splits=S, scale=p.scale,
+                                                   layout=p.layout, stream=stream)
+        elif args.cuda_core_math:
             da.decode_attn_splitkv_partial_cuda_core(q, k, v, cu, ws, num_splits=S, scale=p.scale,
                                                      layout=p.layout, stream=stream)
             if S > 1:
@@ -380,7 +390,7 @@ def main():
 
     def split_step(ev0, ev1):
         # the split kernel alone, for its roofline; the combine follows untimed
-        if split_len or p.tq > 1:
+        if split_len or p.tq > 1 or args.tmem_math:
             return step(ev0, ev1)   # these modes have no split-only entry point: time the call
         flush()
         ev0.record(stream)
@@ -439,7 +449,7 @@ def main():
 
     # ---- end to end through the public call, host buffers, copies inside each step
     e2e = None
-    if args.e2e_steps > 0 and not args.cuda_core_math:
+    if args.e2e_steps > 0 and not (args.cuda_core_math or args.tmem_math):
         pq, pk, pv, pcu = hq.pin_memory(), hk.pin_memory(), hv.pin_memory(), hcu.pin_memory()
         hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
 
@@ -497,13 +507,13 @@ def main():
         return
     peak, peak_kind = measured_peaks()
     per_call = 1 if (S == 1 and not split_len) else 2          # one split writes the output itself
-    per_split_step = per_call if (split_len or p.tq > 1) else 2
+    per_split_step = per_call if (split_len or p.tq > 1 or args.tmem_math) else 2
     split_mean_ms = sum(split_ms) / len(split_ms)
     ws_bytes = p.B * p.tq * p.Hq * S * (p.D + 1) * 4
     q_bytes = p.B * p.tq * p.Hq * p.D * 2
     alg_bytes = p.kv_bytes + q_bytes + 4 * (p.B + 1) + ws_bytes
     achieved = alg_bytes / (split_mean_ms * 1e-3) / 1e9
-    traffic = None if args.cuda_core_math else recorded_traffic(p.name, S)
+    traffic = None if (args.cuda_core_math or args.tmem_math) else recorded_traffic(p.name, S)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_step_ms, 5),
@@ -514,10 +524,12 @@ def main():
         "dtype": p.dtype, "data": "synthetic (seeded N(0,1), rounded to the input dtype)",
         "config": {**workload_config(p, S),
                    "products": ("CUDA-core fp32 FMA (comparison arm)" if args.cuda_core_math
+                                else "tcgen05 with tensor memory (comparison arm)" if args.tmem_math
                                 else "tensor-core mma.sync m16n8k16"),
                    **({"split_mode": "per-sequence", "split_len": split_len, "max_splits": S}
                       if split_len else {"split_mode": "uniform"})},
-        "roofline": {"kernel": ("split_kernel" if not (split_len or p.tq > 1)
+        "roofline": {"kernel": ("split_kernel_tc+combine_kernel" if args.tmem_math
+                                else "split_kernel" if not (split_len or p.tq > 1)
                                 else "split_kernel+combine_kernel"),
                      "bound": "hbm", "achieved": round(achieved, 2),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
@@ -527,7 +539,7 @@ def main():
                      "launch_us_mean": round(split_mean_ms * 1e3, 2),
                      "launches_timed": k_split,
                      **({"combine_us_mean_derived": round((mean_step_ms - split_mean_ms) * 1e3, 2)}
-                        if per_call == 2 and not (split_len or p.tq > 1) else {})},
+                        if per_call == 2 and not (split_len or p.tq > 1 or args.tmem_math) else {})},
         "back_to_back": {"us_per_call": round(b2b_ms * 1e3, 2),
                          "value": round(world * kv_bytes_gqa / (b2b_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
                          "calls": n_b2b, "inputs_exceed_l2": p.kv_bytes > l2,
@@ -537,7 +549,7 @@ def main():
         "model_us": (round(da.model_us(p.lens, p.Hq, p.Hkv, p.D, S,
                                        torch.cuda.get_device_properties(dev).multi_processor_count,
                                        T_q=p.tq), 1)
-                     if not (split_len or args.fa2_style or args.cuda_core_math) else None),
+                     if not (split_len or args.fa2_style or args.cuda_core_math or args.tmem_math) else None),
         "wall_s_timed_region": round(t_wall, 3),
     }
     if sampler:

@@ -267,6 +267,26 @@ da_status decode_attn_splitkv_multiquery(const void* q, const void* k, const voi
                                          void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Comparison arm for the product choice on Blackwell: decode_attn_splitkv_multiquery
+ * with the split step on the tcgen05 tensor cores and the accumulators in tensor
+ * memory, for G * T_q > 8 and G <= 32 (else DA_ERR_UNSUPPORTED). Per 64-key stage
+ * S = Q K^T and O += P V run as tcgen05.mma with M = 128 rows: the item's packed
+ * columns (up to 32, whole query tokens of one KV head's group), laid into all four
+ * 32-row quarters so that four warps, one per SM sub-partition, each take 16 of the
+ * stage's keys; P goes back to tensor memory as the A operand of the PV product.
+ * Same arguments, results and errors as decode_attn_splitkv_multiquery; the outputs
+ * agree with it to fp16/bf16 rounding (the order of the sums differs). It measures
+ * slower than the mma.sync path on every shape tried: with M fixed at 128 the
+ * products of a stage cost about as much tensor time as the stage takes to stream,
+ * whatever the column count.
+ */
+da_status decode_attn_splitkv_multiquery_tmem(const void* q, const void* k, const void* v,
+                                              const int32_t* cu_seqlens_k, int B, int T_q, int Hq,
+                                              int Hkv, int D, int kv_rows, da_dtype dtype,
+                                              da_layout layout, float scale, int num_splits, void* out,
+                                              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Read and clear the device error word of `workspace` (DA_DEVERR_* bits).
  * Synchronises `stream` first. Errors: DA_ERR_INVALID_ARG, DA_ERR_CUDA.
  */

@@ -33,7 +33,7 @@ EXPORTED = [
     "decode_attn_splitkv_noalloc", "decode_attn_splitkv_varsplit",
     "decode_attn_splitkv_varsplit_plan", "decode_attn_splitkv_multiquery",
     "decode_attn_splitkv_model_us", "decode_attn_splitkv_model_best_splits",
-    "decode_attn_splitkv_partial_cuda_core",
+    "decode_attn_splitkv_partial_cuda_core", "decode_attn_splitkv_multiquery_tmem",
 ]
 
 _lib = None
@@ -90,6 +90,9 @@ def load(path: str = LIB):
     lib.decode_attn_splitkv_multiquery.argtypes = [P, P, P, P, I, I, I, I, I, I, I, I, F, I, P, P,
                                                    SZ, P]
     lib.decode_attn_splitkv_multiquery.restype = I
+    lib.decode_attn_splitkv_multiquery_tmem.argtypes = [P, P, P, P, I, I, I, I, I, I, I, I, F, I, P, P,
+                                                        SZ, P]
+    lib.decode_attn_splitkv_multiquery_tmem.restype = I
     lib.decode_attn_splitkv_model_us.argtypes = [P, I, I, I, I, I, I, I, P]
     lib.decode_attn_splitkv_model_us.restype = ctypes.c_double
     lib.decode_attn_splitkv_model_best_splits.argtypes = [P, I, I, I, I, I, I,
@@ -239,21 +242,35 @@ def decode_attn_splitkv_varsplit(q, k, v, cu_seqlens_k, out, workspace, *, split
     return out
 
 
-def decode_attn_splitkv_multiquery(q, k, v, cu_seqlens_k, out, workspace, *, num_splits: int,
-                                   scale: float | None = None, layout: int = DA_LAYOUT_VARLEN,
-                                   stream=None):
-    """Several query tokens per sequence: q and out are [B, T_q, Hq, D]; see the C header."""
+def _multiquery(name, q, k, v, cu_seqlens_k, out, workspace, num_splits, scale, layout, stream):
     B, T, Hq, D = q.shape
     if layout == DA_LAYOUT_VARLEN:
         kv_rows, Hkv = k.shape[0], k.shape[1]
     else:
         Hkv, kv_rows = k.shape[1], k.shape[2]
     sc = 1.0 / math.sqrt(D) if scale is None else scale
-    st = load().decode_attn_splitkv_multiquery(
+    st = getattr(load(), name)(
         _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_k), B, T, Hq, Hkv, D, kv_rows, _dtype_code(q),
         layout, sc, num_splits, _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
-    _check(st, "decode_attn_splitkv_multiquery")
+    _check(st, name)
     return out
+
+
+def decode_attn_splitkv_multiquery(q, k, v, cu_seqlens_k, out, workspace, *, num_splits: int,
+                                   scale: float | None = None, layout: int = DA_LAYOUT_VARLEN,
+                                   stream=None):
+    """Several query tokens per sequence: q and out are [B, T_q, Hq, D]; see the C header."""
+    return _multiquery("decode_attn_splitkv_multiquery", q, k, v, cu_seqlens_k, out, workspace, num_splits,
+                       scale, layout, stream)
+
+
+def decode_attn_splitkv_multiquery_tmem(q, k, v, cu_seqlens_k, out, workspace, *, num_splits: int,
+                                        scale: float | None = None, layout: int = DA_LAYOUT_VARLEN,
+                                        stream=None):
+    """The tcgen05 / tensor-memory comparison arm of decode_attn_splitkv_multiquery (G * T_q > 8,
+    G <= 32); see the C header."""
+    return _multiquery("decode_attn_splitkv_multiquery_tmem", q, k, v, cu_seqlens_k, out, workspace,
+                       num_splits, scale, layout, stream)
 
 
 def decode_attn_splitkv_partial(q, k, v, cu_seqlens_k, workspace, *, num_splits: int,

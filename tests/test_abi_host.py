@@ -31,7 +31,7 @@ def header_functions():
 
 def test_exports_every_declared_symbol(lib):
     names = header_functions()
-    assert len(names) == 19
+    assert len(names) == 20
     assert sorted(names) == sorted(da.EXPORTED)
     for n in names:
         assert hasattr(lib, n), n
@@ -226,6 +226,23 @@ def test_multiquery_host_checks(lib):
     assert call(S=0) == da.DA_ERR_INVALID_ARG
     assert call(q=FAKE + 4) == da.DA_ERR_ALIGNMENT
     need = da.workspace_size(2 * 2, 4, 64, 4)
+    assert call(ws_bytes=need - 1) == da.DA_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_multiquery_tmem_host_checks(lib):
+    """The tcgen05 arm takes G * T_q > 8 with G <= 32 only; the checks launch nothing."""
+    v = ctypes.c_void_p
+
+    def call(T=4, Hq=8, Hkv=2, S=2, ws_bytes=1 << 22):
+        return lib.decode_attn_splitkv_multiquery_tmem(v(FAKE), v(FAKE + 0x100000), v(FAKE + 0x200000),
+                                                       v(FAKE + 0x300000), 2, T, Hq, Hkv, 64, 237, 0, 0,
+                                                       0.125, S, v(FAKE + 0x400000), v(FAKE + 0x500000),
+                                                       ws_bytes, None)
+    assert call(T=2) == da.DA_ERR_UNSUPPORTED              # G * T_q = 8: one n-tile, not this arm
+    assert call(T=1, Hq=66, Hkv=1) == da.DA_ERR_UNSUPPORTED   # G = 66 > 32
+    assert call(T=0) == da.DA_ERR_INVALID_ARG
+    assert call(S=0) == da.DA_ERR_INVALID_ARG
+    need = da.workspace_size(2 * 4, 8, 64, 2)
     assert call(ws_bytes=need - 1) == da.DA_ERR_WORKSPACE_TOO_SMALL
 
 

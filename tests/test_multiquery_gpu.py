@@ -138,3 +138,38 @@ def test_multiquery_cuda_graph_replay():
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, eager)
+
+
+@pytest.mark.parametrize("layout", [LAYOUT_VARLEN, LAYOUT_BHSD], ids=["varlen", "bhsd"])
+def test_multiquery_ramping_scores(layout):
+    """16-column items whose scores climb by about 0.07 (log2 units) per key: the running
+    reference of the rising columns moves every couple of stages and the weights between
+    moves reach 2^8; the other columns see falling scores and never move after the first box."""
+    B, tq, Hq, Hkv, D, lens, S = 2, 2, 16, 2, 128, [1500, 700], 3
+    p = custom("ramp", B, Hq, Hkv, D, lens, "f16", layout, S, seed=17, kv_rows=1536, tq=tq)
+    q = np.zeros((B, tq, Hq, D), np.float32)
+    q[:, :, 0::2, :] = 0.25
+    q[:, :, 1::2, :] = -0.25
+    q[:, 1, :, :] *= 0.5                      # the second token climbs at half the rate
+    p.q = q.astype(np.float16).view(np.uint16).reshape(p.q.shape)
+    kf = np.zeros(p.k.shape, np.float32)
+    for b, L in enumerate(lens):
+        ramp = (np.arange(L) / 60.0).astype(np.float32)   # scale * q.k_j = 2.83 * j / 60 at 0.25
+        if layout == LAYOUT_BHSD:
+            kf[b, :, :L, :] = ramp[None, :, None]
+        else:
+            kf[p.cu[b]:p.cu[b] + L, :, :] = ramp[:, None, None]
+    p.k = kf.astype(np.float16).view(np.uint16)
+    if layout == LAYOUT_BHSD:
+        for b, L in enumerate(lens):
+            p.k[b, :, L:, :] = 0x7E00
+            p.v[b, :, L:, :] = 0x7E00
+    out, lse, opart, err = run_mq(p, tq, S)
+    assert err == 0
+    orc = oracle.default()
+    ref, _ = orc.attention_mq(p, tq)
+    ref_op, ref_lse = orc.split_partials_mq(p, tq, S)
+    assert out_excess(out, ref, p.dtype) <= OUT_TOL
+    assert np.array_equal(np.isneginf(lse), np.isneginf(ref_lse)), "empty-split pattern differs"
+    assert max_abs(lse, ref_lse) <= LSE_TOL
+    assert max_abs(opart, ref_op) <= opart_tol(p)
