@@ -2876,20 +2876,20 @@ const char* decode_attn_splitkv_status_string(da_status status) {
 // at min(r_cta, bw / streaming CTAs), r_cta being one CTA's rate for 8-column
 // items and r_cta2 for 16-column ones; kappa charges the last item for the
 // CTAs' unequal rates, and W_ws is the workspace bytes the combine reads.
-// Fitted (least squares in log time) on one GB300 to the 309 calls, of 546
+// Fitted (least squares in log time) on one GB300 to the 310 calls, of 546
 // measured (17 single-token workloads of the CodeLlama, Llama, Qwen and MHA
 // shapes and 9 of them with 2 or 4 new tokens x split counts 1 to 256, L2
 // flushed, CUDA-event median per call), that lie within 30 % of their
-// workload's fastest split count: median error 3.1 %, 90th percentile 11.8 %.
+// workload's fastest split count: median error 2.9 %, 90th percentile 10.8 %.
 static const double kModelGb300[8] = {
-    /* t0 us       */ 12.34,
-    /* t_item us   */ 0.06824,
-    /* r_cta B/us  */ 76500,
-    /* bw B/us     */ 7.655e+06,
-    /* t_comb us   */ 2.450,
-    /* bw_comb     */ 7.553e+05,
-    /* kappa       */ 0.05017,
-    /* r_cta2 B/us */ 45140};
+    /* t0 us       */ 12.24,
+    /* t_item us   */ 0.1241,
+    /* r_cta B/us  */ 76340,
+    /* bw B/us     */ 7.592e+06,
+    /* t_comb us   */ 2.462,
+    /* bw_comb     */ 8.561e+05,
+    /* kappa       */ 0.05135,
+    /* r_cta2 B/us */ 52610};
 
 double decode_attn_splitkv_model_us(const int32_t* kv_lens, int B, int Hq, int Hkv, int D, int T_q, int num_splits,
                                     int sm_count, const double* params) {
