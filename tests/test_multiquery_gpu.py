@@ -111,6 +111,34 @@ def test_multiquery_long_context_sampled():
     assert out_excess(out[rb, rt, rh], ref, p.dtype) <= OUT_TOL
 
 
+@pytest.mark.parametrize("name,tq", [("qwen_varlen", 4), ("llama_S8192_B16", 4)])
+@pytest.mark.parametrize("arm", ["mma_sync", "tmem"])
+def test_multiquery_named_workloads_sampled(name, tq, arm):
+    """Full-size workloads with several query tokens, the picker's split count (as the benchmark
+    times them), sampled (sequence, token, head) rows; both the default path and the tcgen05 arm."""
+    from synth.workloads import materialize, workload
+    p = workload(name, data=False)
+    p.tq = tq
+    materialize(p)
+    S = da.num_splits(p.B, p.Hq * tq, p.Hkv, p.D, min(p.lens), max(p.lens))
+    fn = da.decode_attn_splitkv_multiquery if arm == "mma_sync" else da.decode_attn_splitkv_multiquery_tmem
+    q, k, v, cu = to_device(p)
+    q = q.view(p.B, tq, p.Hq, p.D)
+    ws = da.alloc_workspace(p.B * tq, p.Hq, p.D, S)
+    out = torch.empty(p.B, tq, p.Hq, p.D, dtype=torch_dtype(p), device="cuda")
+    fn(q, k, v, cu, out, ws, num_splits=S, scale=p.scale, layout=p.layout)
+    assert da.decode_attn_splitkv_get_error(ws) == 0
+    out = out.to(torch.float64).cpu().numpy()
+    assert np.isfinite(out).all()
+    rng = np.random.default_rng(5)
+    n = 24
+    rb = np.concatenate([[0, p.B - 1], rng.integers(0, p.B, n)]).astype(np.int32)
+    rt = np.concatenate([[0, tq - 1], rng.integers(0, tq, n)]).astype(np.int32)
+    rh = np.concatenate([[0, p.Hq - 1], rng.integers(0, p.Hq, n)]).astype(np.int32)
+    ref, _ = oracle.default().attention_rows_mq(p, tq, rb, rt, rh)
+    assert out_excess(out[rb, rt, rh], ref, p.dtype) <= OUT_TOL
+
+
 def test_multiquery_d64_bhsd_bf16():
     p = custom("mq64", 3, 12, 3, 64, [40, 3, 200], "bf16", LAYOUT_BHSD, 3, seed=41, kv_rows=210, tq=3)
     for b, L in enumerate(p.lens):
