@@ -26,10 +26,13 @@
 //   * Online softmax in the exp2 domain (scale * log2 e folded into the
 //     scores), with running max, running sum and accumulator per consumer warp
 //     in fp32 registers (TileLang page, split segment online softmax; MiniInfer
-//     flash_decode_splitk.py, _splitk_stage1_kernel). At the end of an item
-//     the producer hands the consumers one ring stage instead of a tile, and
-//     the four warps merge their states through it in a fixed order (the
-//     result does not depend on timing), one n-tile per round.
+//     flash_decode_splitk.py, _splitk_stage1_kernel). The accumulator is
+//     rescaled only when the running max moves; in 16-column items the
+//     reference lags, moving only when a score passes it by more than 8 (log2
+//     units) as one warp vote decides, so the weights stay below 2^8. At the
+//     end of an item the producer hands the consumers one ring stage instead
+//     of a tile, and the four warps merge their states through it in a fixed
+//     order (the result does not depend on timing), one n-tile per round.
 //   * Split bounds are proportional: [L*s/S, L*(s+1)/S) in 64-bit integers
 //     (TileLang page, split segment). Keys of a stage past the split end are
 //     masked to -inf before the max, and their V rows are cleared in shared
@@ -41,6 +44,10 @@
 // the weight indexed by head row; MiniInfer _splitk_reduce_kernel).
 // The two kernels are chained with programmatic dependent launch. With a single
 // split the split kernel writes the output itself and no combine is launched.
+// split_kernel_tc runs the same split step on the tcgen05 tensor cores with the
+// accumulators in tensor memory, for items of 9 to 32 columns; it is a
+// comparison arm (decode_attn_splitkv_multiquery_tmem) that the library's own
+// calls never use.
 //
 // Every mbarrier wait is bounded in time; on expiry the kernel sets
 // DA_DEVERR_TIMEOUT in the workspace error word and winds down instead of
