@@ -34,7 +34,10 @@ if ROOT not in sys.path:
 
 METRIC = "decode-attn µs/call and KV-read HBM GB/s (% of GB300 peak)"
 DEFAULT_WORKLOAD = "mha_bhsd"
-CU_SRC = os.path.join(ROOT, "split_kv_decode_decoding_gb300", "csrc", "decode_attn_splitkv.cu")
+# the sources the library's own kernels are compiled from (recorded ncu traffic is current only
+# while these are unchanged)
+CU_SRCS = [os.path.join(ROOT, "split_kv_decode_decoding_gb300", "csrc", n)
+           for n in ("decode_attn_splitkv.cu", "split_common.cuh", "geometry.h")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 FALLBACK_HBM_GBS = 6800.0
 
@@ -100,8 +103,11 @@ def measured_peaks():
 
 
 def kernel_sha() -> str:
-    with open(CU_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for path in CU_SRCS:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def recorded_traffic(workload: str, S: int):

@@ -1,20 +1,25 @@
-"""Compile the CUDA library for sm_103a, in tree (no cmake, one translation unit)."""
+"""Compile the CUDA library for sm_103a, in tree (no cmake): three translation units
+compiled in parallel, then linked into one shared library."""
 from __future__ import annotations
 
+import glob
 import os
 import shutil
 import subprocess
+from concurrent.futures import ThreadPoolExecutor
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SRC = os.path.join(PKG, "csrc", "decode_attn_splitkv.cu")
+CSRC = os.path.join(PKG, "csrc")
+SOURCES = [os.path.join(CSRC, n) for n in
+           ("decode_attn_splitkv.cu", "comparison_arms.cu", "time_model.cpp")]
 HEADER = os.path.join(ROOT, "include", "decode_attn_splitkv.h")
 LIB = os.path.join(PKG, "_build", "libdecode_attn_splitkv.so")
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-O3", "-lineinfo", "-std=c++17",
-    "-Xcompiler", "-fPIC", "-shared",
+    "-Xcompiler", "-fPIC",
     "--expt-relaxed-constexpr",
 ]
 
@@ -26,15 +31,36 @@ def nvcc() -> str:
     return cand
 
 
+def inputs() -> list:
+    """Every file the library is built from (sources and headers)."""
+    return SOURCES + [HEADER] + sorted(glob.glob(os.path.join(CSRC, "*.h")) +
+                                       glob.glob(os.path.join(CSRC, "*.cuh")))
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(os.path.dirname(LIB), exist_ok=True)
-    newest = max(os.path.getmtime(SRC), os.path.getmtime(HEADER))
+    newest = max(os.path.getmtime(f) for f in inputs())
     if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= newest:
         return LIB
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *NVCC_FLAGS, "-I", os.path.join(ROOT, "include"), "-o", tmp, SRC]
-    if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
+    tag = f".tmp{os.getpid()}"
+    objs = [os.path.join(os.path.dirname(LIB), os.path.basename(s) + tag + ".o") for s in SOURCES]
+
+    def compile_one(src_obj):
+        src, obj = src_obj
+        cmd = [nvcc(), *NVCC_FLAGS, "-I", os.path.join(ROOT, "include"), "-c", "-o", obj, src]
+        if verbose and src.endswith(".cu"):
+            cmd.insert(1, "-Xptxas=-v")
+        subprocess.run(cmd, check=True)
+
+    try:
+        with ThreadPoolExecutor(len(SOURCES)) as ex:
+            list(ex.map(compile_one, zip(SOURCES, objs)))
+        tmp = LIB + tag
+        subprocess.run([nvcc(), "-gencode", "arch=compute_103a,code=sm_103a", "-shared",
+                        "-Xcompiler", "-fPIC", "-o", tmp, *objs], check=True)
+        os.replace(tmp, LIB)
+    finally:
+        for o in objs:
+            if os.path.exists(o):
+                os.remove(o)
     return LIB
