@@ -345,6 +345,25 @@ def pin_rows_match_full(o):
     assert np.array_equal(out, full[rb, rh]) and np.array_equal(lse, full_lse[rb, rh])
 
 
+def pin_rows_mq_match_full(o):
+    """The row selector for several query tokens (the checker of the full-size multi-token GPU
+    tests) equals the whole-problem function at the same (b, t, h), bit for bit, in both
+    layouts, for tokens after the first and for a token that sees no key."""
+    for layout in (LAYOUT_VARLEN, LAYOUT_BHSD):
+        tq = 4
+        p = custom("rowsmq", 3, 4, 2, 64, [30, 5, 2], "bf16", layout=layout, seed=62, tq=tq,
+                   kv_rows=32 if layout == LAYOUT_BHSD else 0)
+        full, full_lse = o.attention_mq(p, tq)
+        rb = np.array([0, 2, 1, 0, 1, 2, 0, 2], dtype=np.int32)
+        rt = np.array([3, 1, 2, 1, 3, 0, 2, 3], dtype=np.int32)
+        rh = np.array([0, 3, 1, 2, 2, 1, 3, 0], dtype=np.int32)
+        out, lse = o.attention_rows_mq(p, tq, rb, rt, rh)
+        assert np.array_equal(out, full[rb, rt, rh]), layout
+        assert np.array_equal(lse, full_lse[rb, rt, rh]), layout
+        # token 0 of the two-key sequence sees no key (position 2 - 4 + 0 < 0): out 0, lse -inf
+        assert not out[5].any() and lse[5] == -math.inf
+
+
 def read_count_golden():
     rows = []
     with open(os.path.join(GOLDEN, "split_counts.txt")) as f:
@@ -496,6 +515,7 @@ ALL_PINS = [
     pin_constant_v, pin_gqa_packing, pin_hand_example, pin_q_zero_closed_form,
     pin_one_hot_dominance, pin_library_cross_check, pin_bhsd_matches_varlen,
     pin_empty_splits_and_sequences, pin_threads_deterministic, pin_rows_match_full,
+    pin_rows_mq_match_full,
     pin_split_counts_golden, pin_varsplit_merge_invariance,
     pin_mq_causal_counts_golden, pin_mq_tq1_equals_single, pin_mq_token_equals_truncated_single,
     pin_mq_split_invariance, pin_mq_library_cross_check,

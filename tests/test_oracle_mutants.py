@@ -40,6 +40,12 @@ MUTANTS = {
     "split_ignores_causal_limit": ("if (hi > vis) hi = vis;", "if (false) hi = vis;"),
     "query_token_ignored": ("(((int64_t)b * p.tq + t) * p.Hq + h) * p.D",
                             "(((int64_t)b * p.tq) * p.Hq + h) * p.D"),
+    # the row selector for several query tokens: the token index dropped, or token and head
+    # swapped (the pin's shapes keep the swapped indices in range)
+    "rows_mq_token_dropped": ("attend_row(p, rows_b[i], rows_t[i], rows_h[i], out + i * D, lse + i);",
+                              "attend_row(p, rows_b[i], 0, rows_h[i], out + i * D, lse + i);"),
+    "rows_mq_token_head_swapped": ("attend_row(p, rows_b[i], rows_t[i], rows_h[i], out + i * D, lse + i);",
+                                   "attend_row(p, rows_b[i], rows_h[i], rows_t[i], out + i * D, lse + i);"),
     "merge_skips_last_split": ("for (int s = 0; s < S; ++s) {\n            if (ls[s] == kNegInf) continue;",
                                "for (int s = 0; s + 1 < S; ++s) {\n            if (ls[s] == kNegInf) continue;"),
 }
