@@ -57,8 +57,12 @@ typedef enum {
     DA_ERR_ALIGNMENT = 3,           /* a pointer is not aligned as documented */
     DA_ERR_WORKSPACE_TOO_SMALL = 4, /* workspace_bytes < decode_attn_splitkv_workspace_size() */
     DA_ERR_CUDA = 5,                /* a CUDA runtime or driver call failed */
-    DA_ERR_SCRATCH_LIMIT = 6        /* decode_attn_splitkv_noalloc: the problem needs more scratch
+    DA_ERR_SCRATCH_LIMIT = 6,       /* decode_attn_splitkv_noalloc: the problem needs more scratch
                                        than DA_NOALLOC_SCRATCH_BYTES */
+    DA_ERR_DEVICE_TIMEOUT = 7       /* returned by the error readers (decode_attn_splitkv_get_error,
+                                       decode_attn_splitkv_noalloc_get_error) when a pipeline wait
+                                       of an earlier call on the device timed out
+                                       (DA_DEVERR_TIMEOUT): that call's outputs are invalid */
 } da_status;
 
 typedef enum { DA_F16 = 0, DA_BF16 = 1 } da_dtype;
@@ -67,6 +71,7 @@ typedef enum {
     /* K, V: [kv_rows, Hkv, D] row-major; sequence b owns rows
        cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1 (kv_rows = total_kv). */
     DA_LAYOUT_VARLEN = 0,
+    DA_LAYOUT_VARLEN_THD = DA_LAYOUT_VARLEN,   /* the same layout: tokens x heads x dim */
     /* K, V: [B, Hkv, kv_rows, D] row-major; sequence b owns positions
        0 .. L_b-1 of its own [kv_rows, D] slab per KV head (kv_rows is the
        per-sequence capacity; L_b still comes from cu_seqlens_k). */
@@ -287,8 +292,14 @@ da_status decode_attn_splitkv_multiquery_tmem(const void* q, const void* k, cons
                                               void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * Read and clear the device error word of `workspace` (DA_DEVERR_* bits).
- * Synchronises `stream` first. Errors: DA_ERR_INVALID_ARG, DA_ERR_CUDA.
+ * Read and clear the device error word of `workspace`: *device_error_bits gets
+ * its DA_DEVERR_* bits (the word can hold more than one, so they are returned
+ * apart from the status). Synchronises `stream` first.
+ * Returns DA_ERR_DEVICE_TIMEOUT when DA_DEVERR_TIMEOUT is among the bits (the
+ * outputs of the call that set it are invalid; initialise the workspace again
+ * before reusing it), else DA_OK; a DA_DEVERR_SEQLENS bit alone is reported
+ * through the bits with DA_OK (the bad sequences were computed as empty).
+ * Errors: DA_ERR_INVALID_ARG, DA_ERR_ALIGNMENT, DA_ERR_CUDA (bits then untouched).
  */
 da_status decode_attn_splitkv_get_error(void* workspace, uint32_t* device_error_bits,
                                         void* stream);
@@ -325,23 +336,39 @@ da_status decode_attn_splitkv_selftest_timeout(void* workspace, size_t workspace
  *   - Problems whose workspace_size(B, Hq, D, num_splits) exceeds
  *     DA_NOALLOC_SCRATCH_BYTES are refused with DA_ERR_SCRATCH_LIMIT and
  *     nothing is enqueued. (For example B=64, Hq=28, D=128 fits up to 9 splits.)
+ *   - The argument checks run on the host before anything touches a device,
+ *     so a refused call (DA_ERR_INVALID_ARG, DA_ERR_ALIGNMENT, DA_ERR_UNSUPPORTED,
+ *     DA_ERR_SCRATCH_LIMIT) makes no CUDA call at all.
  *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current and caches it; make
- *     that first call before any stream capture on the device.
+ *     (cudaGetSymbolAddress) with that device current and caches it together
+ *     with the id of the CUDA context it belongs to; make that first call
+ *     before any stream capture on the device. A later call in another context
+ *     of the same device (after cudaDeviceReset, which destroys the context and
+ *     the array with it) finds a different id and looks the address up again.
  *   - All calls share the one array, which keeps the previous call's
  *     contents; each call clears the part that must start at zero (the error
- *     word) and overwrites the rest before reading it. Calls that can overlap
- *     on the GPU (different streams without ordering between them, or
- *     several host threads) race on the array and corrupt each other's
- *     results: serialise them.
- *   - Device-side error bits (DA_DEVERR_*) of these calls are not reported;
- *     use decode_attn_splitkv with a workspace to diagnose them.
+ *     word and the work-queue counters) and overwrites the rest before reading
+ *     it. Calls that can overlap on the GPU (different streams without ordering
+ *     between them, or several host threads) race on the array and corrupt
+ *     each other's results: serialise them.
+ *   - Device-side error bits (DA_DEVERR_*) of the last call on a device land in
+ *     the array's error word: read them with decode_attn_splitkv_noalloc_get_error.
  * Errors: those of decode_attn_splitkv, plus DA_ERR_SCRATCH_LIMIT.
  */
 da_status decode_attn_splitkv_noalloc(const void* q, const void* k, const void* v,
                                       const int32_t* cu_seqlens_k, int B, int Hq, int Hkv,
                                       int D, int kv_rows, da_dtype dtype, da_layout layout,
                                       float scale, int num_splits, void* out, void* stream);
+
+/*
+ * decode_attn_splitkv_get_error for decode_attn_splitkv_noalloc: read and clear
+ * the error word of the built-in scratch array of the current device, after
+ * synchronising `stream` (the stream of the noalloc call to diagnose). Like that
+ * entry point it has no counterpart on the pages and allocates nothing.
+ * Returns DA_ERR_DEVICE_TIMEOUT when DA_DEVERR_TIMEOUT is set, else DA_OK, with
+ * the bits in *device_error_bits; DA_ERR_INVALID_ARG (NULL) or DA_ERR_CUDA.
+ */
+da_status decode_attn_splitkv_noalloc_get_error(uint32_t* device_error_bits, void* stream);
 
 /*
  * Time model of one decode_attn_splitkv (or _multiquery) call on GB300, in

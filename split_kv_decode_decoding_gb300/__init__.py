@@ -15,9 +15,10 @@ import os
 from .build import LIB, build
 
 DA_OK, DA_ERR_INVALID_ARG, DA_ERR_UNSUPPORTED, DA_ERR_ALIGNMENT = 0, 1, 2, 3
-DA_ERR_WORKSPACE_TOO_SMALL, DA_ERR_CUDA, DA_ERR_SCRATCH_LIMIT = 4, 5, 6
+DA_ERR_WORKSPACE_TOO_SMALL, DA_ERR_CUDA, DA_ERR_SCRATCH_LIMIT, DA_ERR_DEVICE_TIMEOUT = 4, 5, 6, 7
 DA_F16, DA_BF16 = 0, 1
 DA_LAYOUT_VARLEN, DA_LAYOUT_BHSD = 0, 1
+DA_LAYOUT_VARLEN_THD = DA_LAYOUT_VARLEN
 DA_DEVERR_SEQLENS, DA_DEVERR_TIMEOUT = 0x1, 0x2
 DA_MAX_SPLITS = 1024
 DA_NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
@@ -34,6 +35,7 @@ EXPORTED = [
     "decode_attn_splitkv_varsplit_plan", "decode_attn_splitkv_multiquery",
     "decode_attn_splitkv_model_us", "decode_attn_splitkv_model_best_splits",
     "decode_attn_splitkv_partial_cuda_core", "decode_attn_splitkv_multiquery_tmem",
+    "decode_attn_splitkv_noalloc_get_error",
 ]
 
 _lib = None
@@ -82,6 +84,8 @@ def load(path: str = LIB):
     lib.decode_attn_splitkv_selftest_timeout.restype = I
     lib.decode_attn_splitkv_noalloc.argtypes = [P, P, P, P, I, I, I, I, I, I, I, F, I, P, P]
     lib.decode_attn_splitkv_noalloc.restype = I
+    lib.decode_attn_splitkv_noalloc_get_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), P]
+    lib.decode_attn_splitkv_noalloc_get_error.restype = I
     lib.decode_attn_splitkv_varsplit.argtypes = [P, P, P, P, I, I, I, I, I, I, I, F, I, I, P, P, SZ, P]
     lib.decode_attn_splitkv_varsplit.restype = I
     lib.decode_attn_splitkv_varsplit_plan.argtypes = [I, I, I, I, I64, I, I, ctypes.POINTER(I),
@@ -305,10 +309,23 @@ def decode_attn_splitkv_combine(out, workspace, *, num_splits: int, stream=None)
 
 
 def decode_attn_splitkv_get_error(workspace, stream=None) -> int:
+    """Read and clear the workspace's device error word: the DA_DEVERR_* bits (0 if none).
+
+    A time-out (the C call's DA_ERR_DEVICE_TIMEOUT) is reported through the bits too,
+    not raised, so that the caller can tell it from a failed read."""
     bits = ctypes.c_uint32(0)
-    _check(load().decode_attn_splitkv_get_error(_ptr(workspace), ctypes.byref(bits),
-                                                _stream(stream)),
-           "decode_attn_splitkv_get_error")
+    st = load().decode_attn_splitkv_get_error(_ptr(workspace), ctypes.byref(bits), _stream(stream))
+    if st != DA_ERR_DEVICE_TIMEOUT:
+        _check(st, "decode_attn_splitkv_get_error")
+    return bits.value
+
+
+def decode_attn_splitkv_noalloc_get_error(stream=None) -> int:
+    """decode_attn_splitkv_get_error for decode_attn_splitkv_noalloc's built-in scratch array."""
+    bits = ctypes.c_uint32(0)
+    st = load().decode_attn_splitkv_noalloc_get_error(ctypes.byref(bits), _stream(stream))
+    if st != DA_ERR_DEVICE_TIMEOUT:
+        _check(st, "decode_attn_splitkv_noalloc_get_error")
     return bits.value
 
 

@@ -920,7 +920,7 @@ da_status decode_attn_splitkv_get_error(void* workspace, uint32_t* device_error_
     if (cudaStreamSynchronize(s) != cudaSuccess) return DA_ERR_CUDA;
     *device_error_bits = bits;
     if (cudaMemsetAsync(workspace, 0, sizeof(uint32_t), s) != cudaSuccess) return DA_ERR_CUDA;
-    return DA_OK;
+    return (bits & DA_DEVERR_TIMEOUT) ? DA_ERR_DEVICE_TIMEOUT : DA_OK;
 }
 
 da_status decode_attn_splitkv_selftest_timeout(void* workspace, size_t workspace_bytes,
@@ -949,6 +949,9 @@ const char* decode_attn_splitkv_status_string(da_status status) {
         case DA_ERR_SCRATCH_LIMIT:
             return "DA_ERR_SCRATCH_LIMIT: the problem needs more scratch than the library's "
                    "8 MiB built-in array (use decode_attn_splitkv with a workspace)";
+        case DA_ERR_DEVICE_TIMEOUT:
+            return "DA_ERR_DEVICE_TIMEOUT: a pipeline wait on the device timed out; that call's "
+                   "outputs are invalid";
     }
     return "unknown da_status";
 }
@@ -961,48 +964,85 @@ const char* decode_attn_splitkv_status_string(da_status status) {
 namespace da_impl {
 
 __device__ __align__(256) uint8_t g_noalloc_scratch[DA_NOALLOC_SCRATCH_BYTES];
+static_assert(static_cast<uint64_t>(DA_NOALLOC_SCRATCH_BYTES) / 4 <= 0x7fffffffull,
+              "every o_part index of a problem that fits the scratch stays within int32");
 
+constexpr int kMaxDevices = 128;
 std::mutex g_noalloc_mu;
-void* g_noalloc_addr[128] = {};   // device address of g_noalloc_scratch, per device ordinal
+void* g_noalloc_addr[kMaxDevices] = {};                 // device address of the array, per device ordinal
+unsigned long long g_noalloc_ctx[kMaxDevices] = {};     // id of the context that address belongs to
+
+// Id of the calling thread's current CUDA context (0 if none is current yet).
+unsigned long long current_context_id() {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, []() {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
 
 // In host code g_noalloc_scratch names a host-side shadow, not device memory:
-// the device address comes from cudaGetSymbolAddress, looked up once per
-// device with that device current.
+// the device address comes from cudaGetSymbolAddress, looked up with the device
+// current, once per device and context (a context made after cudaDeviceReset
+// holds a fresh copy of the array at a possibly different address).
 da_status noalloc_scratch(void** addr) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return DA_ERR_CUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DA_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (g_noalloc_addr[dev] == nullptr) {
+    const unsigned long long ctx = current_context_id();
+    if (g_noalloc_addr[dev] == nullptr || ctx == 0 || ctx != g_noalloc_ctx[dev]) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return DA_ERR_CUDA;
         g_noalloc_addr[dev] = p;
+        // the lookup made the context current if none was: record the one it used
+        g_noalloc_ctx[dev] = current_context_id();
     }
     *addr = g_noalloc_addr[dev];
     return DA_OK;
 }
 
-}  // namespace
+}  // namespace da_impl
 
 extern "C" da_status decode_attn_splitkv_noalloc(const void* q, const void* k, const void* v,
                                                  const int32_t* cu_seqlens_k, int B, int Hq, int Hkv,
                                                  int D, int kv_rows, da_dtype dtype, da_layout layout,
                                                  float scale, int num_splits, void* out, void* stream) {
+    // every host check first: a refused call makes no CUDA call
     const size_t need = decode_attn_splitkv_workspace_size(B, Hq, D, num_splits);
     if (need > DA_NOALLOC_SCRATCH_BYTES) return DA_ERR_SCRATCH_LIMIT;
-    void* ws = nullptr;
-    if (need > 0) {
-        // only sizes that pass the workspace arithmetic reach the device lookup
-        da_status st = noalloc_scratch(&ws);
-        if (st != DA_OK) return st;
-    }
-    da_status st = check_common(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale,
-                                num_splits, ws, DA_NOALLOC_SCRATCH_BYTES);
+    da_status st = check_args(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale, num_splits);
     if (st != DA_OK) return st;
     if (!out) return DA_ERR_INVALID_ARG;
     if (!aligned(out, 16)) return DA_ERR_ALIGNMENT;
+    if (static_cast<int64_t>(B) * Hq * D > 0x7fffffffll) return DA_ERR_INVALID_ARG;
+    void* ws = nullptr;
+    st = noalloc_scratch(&ws);
+    if (st != DA_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(ws, 0, kHeaderBytes, s) != cudaSuccess) return DA_ERR_CUDA;
     return run_decode(make_call(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale, num_splits, 0,
                                 ws),
                       out, s);
+}
+
+extern "C" da_status decode_attn_splitkv_noalloc_get_error(uint32_t* device_error_bits, void* stream) {
+    if (!device_error_bits) return DA_ERR_INVALID_ARG;
+    void* ws = nullptr;
+    const da_status st = noalloc_scratch(&ws);
+    if (st != DA_OK) return st;
+    return decode_attn_splitkv_get_error(ws, device_error_bits, stream);
 }

@@ -794,24 +794,34 @@ cudaError_t persistent_grid(K kernel, int threads, int smem, DeviceCache& cache,
     return cudaSuccess;
 }
 
-inline da_status check_common(const void* q, const void* k, const void* v, const int32_t* cu, int B, int Hq,
-                       int Hkv, int D, int kv_rows, int dt, int lay, float scale, int S,
-                       const void* ws, size_t ws_bytes) {
+// Host checks of a decode call's arguments other than the workspace.
+inline da_status check_args(const void* q, const void* k, const void* v, const int32_t* cu, int B, int Hq,
+                            int Hkv, int D, int kv_rows, int dt, int lay, float scale, int S) {
     if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || kv_rows < 0) return DA_ERR_INVALID_ARG;
     if (S < 1 || S > DA_MAX_SPLITS) return DA_ERR_INVALID_ARG;
     if (!std::isfinite(scale)) return DA_ERR_INVALID_ARG;
     if (dt != DA_F16 && dt != DA_BF16) return DA_ERR_INVALID_ARG;
     if (lay != DA_LAYOUT_VARLEN && lay != DA_LAYOUT_BHSD) return DA_ERR_INVALID_ARG;
     if (D != 64 && D != 128) return DA_ERR_UNSUPPORTED;
-    if (!q || !cu || !ws) return DA_ERR_INVALID_ARG;
+    if (!q || !cu) return DA_ERR_INVALID_ARG;
     if (kv_rows > 0 && (!k || !v)) return DA_ERR_INVALID_ARG;
-    if (!aligned(q, 16) || !aligned(cu, 4) || !aligned(ws, 256)) return DA_ERR_ALIGNMENT;
+    if (!aligned(q, 16) || !aligned(cu, 4)) return DA_ERR_ALIGNMENT;
     if (kv_rows > 0 && (!aligned(k, 16) || !aligned(v, 16))) return DA_ERR_ALIGNMENT;
-    const size_t need = decode_attn_splitkv_workspace_size(B, Hq, D, S);
-    if (need == 0) return DA_ERR_INVALID_ARG;
-    if (ws_bytes < need) return DA_ERR_WORKSPACE_TOO_SMALL;
+    if (decode_attn_splitkv_workspace_size(B, Hq, D, S) == 0) return DA_ERR_INVALID_ARG;
     const int64_t chunks = item_chunks(Hq / Hkv);
     if (static_cast<int64_t>(B) * Hkv * chunks * S > 0x7fffffffll) return DA_ERR_INVALID_ARG;
+    return DA_OK;
+}
+
+// check_args, then the caller's workspace: present, 256-byte aligned, large enough.
+inline da_status check_common(const void* q, const void* k, const void* v, const int32_t* cu, int B, int Hq,
+                              int Hkv, int D, int kv_rows, int dt, int lay, float scale, int S,
+                              const void* ws, size_t ws_bytes) {
+    const da_status st = check_args(q, k, v, cu, B, Hq, Hkv, D, kv_rows, dt, lay, scale, S);
+    if (st != DA_OK) return st;
+    if (!ws) return DA_ERR_INVALID_ARG;
+    if (!aligned(ws, 256)) return DA_ERR_ALIGNMENT;
+    if (ws_bytes < decode_attn_splitkv_workspace_size(B, Hq, D, S)) return DA_ERR_WORKSPACE_TOO_SMALL;
     return DA_OK;
 }
 

@@ -31,17 +31,29 @@ def header_functions():
 
 def test_exports_every_declared_symbol(lib):
     names = header_functions()
-    assert len(names) == 20
+    assert len(names) == 21
     assert sorted(names) == sorted(da.EXPORTED)
     for n in names:
         assert hasattr(lib, n), n
 
 
 def test_status_strings(lib):
-    for code in range(7):
+    for code in range(8):
         s = da.status_string(code)
         assert s and s != "unknown da_status"
     assert da.status_string(99) == "unknown da_status"
+
+
+def test_device_timeout_status_and_layout_alias(lib):
+    """The status the error readers return for a timed-out wait, and the varlen layout's
+    second name, as the header declares them."""
+    text = open(HEADER).read()
+    assert re.search(r"DA_ERR_DEVICE_TIMEOUT\s*=\s*7", text)
+    assert re.search(r"DA_LAYOUT_VARLEN_THD\s*=\s*DA_LAYOUT_VARLEN", text)
+    assert da.DA_ERR_DEVICE_TIMEOUT == 7 and da.DA_LAYOUT_VARLEN_THD == da.DA_LAYOUT_VARLEN == 0
+    assert da.status_string(da.DA_ERR_DEVICE_TIMEOUT).startswith("DA_ERR_DEVICE_TIMEOUT")
+    v = ctypes.c_void_p
+    assert lib.decode_attn_splitkv_noalloc_get_error(None, None) == da.DA_ERR_INVALID_ARG
 
 
 def test_workspace_layout(lib):
@@ -281,3 +293,32 @@ def test_time_model_properties(lib):
     assert 8 <= S <= 256 and t > 0
     assert da.model_us([100], 4, 3, 128, 1, 152) < 0          # Hq % Hkv != 0
     assert da.model_best_splits([5, 3], 4, 1, 128, 152)[0] <= 3
+
+
+def call_noalloc(lib, **kw):
+    a = dict(q=FAKE, k=FAKE + 0x100000, v=FAKE + 0x200000, cu=FAKE + 0x300000, B=2, Hq=4, Hkv=1,
+             D=64, kv_rows=237, dt=0, lay=0, scale=0.125, S=4, out=FAKE + 0x400000, stream=None)
+    a.update(kw)
+    v = ctypes.c_void_p
+    return lib.decode_attn_splitkv_noalloc(v(a["q"]), v(a["k"]), v(a["v"]), v(a["cu"]), a["B"], a["Hq"],
+                                           a["Hkv"], a["D"], a["kv_rows"], a["dt"], a["lay"], a["scale"],
+                                           a["S"], v(a["out"]), v(a["stream"]))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=64, Hq=28, Hkv=4, D=128, S=16), da.DA_ERR_SCRATCH_LIMIT),   # 14.9 MB of scratch
+    (dict(B=4096, Hq=64, Hkv=8, D=128, S=1), da.DA_ERR_SCRATCH_LIMIT),
+    (dict(B=0), da.DA_ERR_INVALID_ARG),
+    (dict(S=0), da.DA_ERR_INVALID_ARG),
+    (dict(Hq=6, Hkv=4), da.DA_ERR_INVALID_ARG),
+    (dict(D=96), da.DA_ERR_UNSUPPORTED),
+    (dict(q=0), da.DA_ERR_INVALID_ARG),
+    (dict(out=0), da.DA_ERR_INVALID_ARG),
+    (dict(q=FAKE + 8), da.DA_ERR_ALIGNMENT),
+    (dict(cu=FAKE + 0x300002), da.DA_ERR_ALIGNMENT),
+    (dict(out=FAKE + 0x400008), da.DA_ERR_ALIGNMENT),
+])
+def test_noalloc_host_checks(lib, kw, code):
+    """The no-allocation entry point refuses bad arguments on the host, before it looks up
+    its scratch array on a device (there is none here: a lookup would fail with DA_ERR_CUDA)."""
+    assert call_noalloc(lib, **kw) == code

@@ -148,6 +148,18 @@ def test_timeout_path_sets_flag_and_device_survives():
     da.decode_attn_splitkv_selftest_timeout(ws, 20_000)
     assert da.decode_attn_splitkv_get_error(ws) == da.DA_DEVERR_TIMEOUT
     assert da.decode_attn_splitkv_get_error(ws) == 0
+    # the C reader returns DA_ERR_DEVICE_TIMEOUT for a timed-out wait, DA_OK otherwise
+    import ctypes
+    lib = da.load()
+    bits = ctypes.c_uint32(0)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    da.decode_attn_splitkv_selftest_timeout(ws, 20_000)
+    assert lib.decode_attn_splitkv_get_error(ctypes.c_void_p(ws.data_ptr()), ctypes.byref(bits),
+                                             stream) == da.DA_ERR_DEVICE_TIMEOUT
+    assert bits.value == da.DA_DEVERR_TIMEOUT
+    assert lib.decode_attn_splitkv_get_error(ctypes.c_void_p(ws.data_ptr()), ctypes.byref(bits),
+                                             stream) == da.DA_OK
+    assert bits.value == 0
     check_full(workload("tiny"), 4)
 
 

@@ -11,8 +11,9 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import split_kv_decode_decoding_gb300 as da
-from gpu_util import OUT_TOL, to_device, torch_dtype
+from gpu_util import OUT_TOL, out_excess, to_device, torch_dtype
 from synth.workloads import LAYOUT_BHSD, LAYOUT_VARLEN, custom
 
 pytestmark = pytest.mark.gpu
@@ -56,6 +57,51 @@ def test_noalloc_matches_workspace_call_on_two_calls_in_a_row():
     da.decode_attn_splitkv_noalloc(*ta, again, num_splits=6, scale=a.scale, layout=a.layout)
     torch.cuda.synchronize()
     assert (again.double() - ref_a.double()).abs().max().item() <= OUT_TOL
+    # and against the float64 oracle directly
+    for p, got in ((a, again), (b, out_b)):
+        ref, _ = oracle.default().attention(p)
+        assert out_excess(got.double().cpu().numpy(), ref, p.dtype) <= OUT_TOL
+    assert da.decode_attn_splitkv_noalloc_get_error() == 0
+
+
+@pytest.mark.parametrize("case", [
+    # head_dim 64 (four CTAs per SM, two heads per merge pass), several splits
+    ("na_d64", 3, 12, 2, 64, [300, 17, 1024], "bf16", LAYOUT_VARLEN, 5, 0),
+    # one split: the split kernel writes the output itself and no combine runs
+    ("na_one_split", 4, 32, 8, 128, [512, 3, 2000, 64], "f16", LAYOUT_VARLEN, 1, 0),
+    ("na_one_split_d64_bhsd", 2, 8, 8, 64, [100, 37], "f16", LAYOUT_BHSD, 1, 128),
+], ids=lambda c: c[0])
+def test_noalloc_head_dim_64_and_single_split(case):
+    name, B, Hq, Hkv, D, lens, dtype, layout, S, kv_rows = case
+    p = custom(name, B, Hq, Hkv, D, lens, dtype, layout, S, seed=len(name), kv_rows=kv_rows)
+    t = to_device(p)
+    ref_ws = with_workspace(p, S, t)
+    out = torch.full_like(ref_ws, float("nan"))
+    da.decode_attn_splitkv_noalloc(*t, out, num_splits=S, scale=p.scale, layout=p.layout)
+    torch.cuda.synchronize()
+    assert (out.double() - ref_ws.double()).abs().max().item() <= OUT_TOL
+    ref, _ = oracle.default().attention(p)
+    assert out_excess(out.double().cpu().numpy(), ref, p.dtype) <= OUT_TOL
+    assert da.decode_attn_splitkv_noalloc_get_error() == 0
+
+
+def test_noalloc_reports_device_errors_through_its_reader():
+    """A cu_seqlens_k entry past the end of K/V sets DA_DEVERR_SEQLENS in the scratch array's
+    error word; the reader returns it once, and the next good call starts clean."""
+    p = custom("na_badcu", 3, 8, 2, 128, [50, 60, 70], "f16", LAYOUT_VARLEN, 2, seed=9)
+    q, k, v, cu = to_device(p)
+    bad = cu.clone()
+    bad[3] = p.total_kv + 1000
+    out = torch.empty(p.B, p.Hq, p.D, dtype=torch.float16, device="cuda")
+    da.decode_attn_splitkv_noalloc(q, k, v, bad, out, num_splits=2, scale=p.scale)
+    assert da.decode_attn_splitkv_noalloc_get_error() == da.DA_DEVERR_SEQLENS
+    assert da.decode_attn_splitkv_noalloc_get_error() == 0
+    ref, _ = oracle.default().attention(p)
+    got = out.double().cpu().numpy()
+    assert out_excess(got[:2], ref[:2], p.dtype) <= OUT_TOL and not got[2].any()
+    da.decode_attn_splitkv_noalloc(q, k, v, cu, out, num_splits=2, scale=p.scale)
+    assert da.decode_attn_splitkv_noalloc_get_error() == 0
+    assert out_excess(out.double().cpu().numpy(), ref, p.dtype) <= OUT_TOL
 
 
 def test_noalloc_refuses_problems_beyond_its_scratch():
