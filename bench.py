@@ -33,13 +33,14 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "decode-attn µs/call and KV-read HBM GB/s (% of GB300 peak)"
-DEFAULT_WORKLOAD = "mha_bhsd"
+DEFAULT_WORKLOAD = "llama_S131072_B16"
 # the sources the library's own kernels are compiled from (recorded ncu traffic is current only
 # while these are unchanged)
 CU_SRCS = [os.path.join(ROOT, "split_kv_decode_decoding_gb300", "csrc", n)
            for n in ("decode_attn_splitkv.cu", "split_common.cuh", "geometry.h")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0   # GB300 HBM3e, nominal
 
 
 def parse():
@@ -70,6 +71,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-flush", action="store_true", help="do not flush L2 between steps")
+    ap.add_argument("--clock-sampler", type=int, default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--clock-interval-ms", type=float, default=2.0, help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -111,49 +114,127 @@ def kernel_sha() -> str:
 
 
 def recorded_traffic(workload: str, S: int):
-    """DRAM bytes per split-kernel launch from a committed ncu capture, if it is current."""
+    """DRAM bytes per split-kernel launch from a committed ncu capture, if it is current:
+    (bytes, source). An entry captured on a smaller case may name larger workloads of the
+    same shape and split count in "scale_to" with the factor of units (keys) they process."""
     try:
         with open(TRAFFIC_FILE) as f:
             d = json.load(f)
     except (OSError, ValueError):
-        return None
+        return None, None
+    sha = kernel_sha()
     for e in d.get("entries", []):
-        if e.get("kernel_sha") == kernel_sha() and e.get("workload") == workload and e.get("num_splits") == S:
-            return float(e["dram_bytes_per_launch"])
-    return None
+        if e.get("kernel_sha") == sha and e.get("workload") == workload and e.get("num_splits") == S:
+            return float(e["dram_bytes_per_launch"]), "ncu capture of this workload"
+    for e in d.get("entries", []):
+        f = e.get("scale_to", {}).get(workload)
+        if e.get("kernel_sha") == sha and e.get("num_splits") == S and f:
+            return (float(e["dram_bytes_per_launch"]) * float(f),
+                    f"ncu capture of {e['workload']} scaled x{f} by the keys processed")
+    return None, None
+
+
+# NVML clock-event reason bits (nvml.h, nvmlClocksEventReason*): read-only sampling
+NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
+def nvml_sampler_main(index: int, interval_ms: float) -> int:
+    """Child process: print 'sm_mhz,max_mhz,reasons' every interval_ms until stdin closes.
+
+    Reads the SM clock, its maximum and the clock-event reasons through NVML
+    (libnvidia-ml, read-only queries); prints 'ready' once the first sample is taken."""
+    import ctypes
+    import select
+    try:
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+    except OSError:
+        print("unavailable", flush=True)
+        return 0
+    if nv.nvmlInit_v2() != 0:
+        print("unavailable", flush=True)
+        return 0
+    h = ctypes.c_void_p()
+    if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(h)) != 0:
+        print("unavailable", flush=True)
+        return 0
+    reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+        getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+    clk, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+    first = True
+    while True:
+        ok = (nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and      # NVML_CLOCK_SM
+              nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 and
+              reasons_fn(h, ctypes.byref(rs)) == 0)
+        if ok:
+            print(f"{clk.value},{mx.value},{rs.value}", flush=True)
+        if first:
+            print("ready", flush=True)
+            first = False
+        r, _, _ = select.select([sys.stdin], [], [], interval_ms / 1000.0)
+        if r and not sys.stdin.readline():
+            break
+    nv.nvmlShutdown()
+    return 0
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    """SM clock and clock-event reasons sampled every 2 ms while the timed region runs, by a
+    child process through NVML (the region of one bench run can be tens of milliseconds, too
+    short for nvidia-smi's loop); nvidia-smi's 100 ms loop when NVML cannot be loaded."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, interval_ms: float = 2.0):
         self.index = index
+        self.interval_ms = interval_ms
         self.proc = None
+        self.kind = None
+        self.lines = []
 
     def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                [sys.executable, os.path.abspath(__file__), "--clock-sampler", str(self.index),
+                 "--clock-interval-ms", str(self.interval_ms)],
+                stdin=subprocess.PIPE, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            head = []
+            while True:
+                ln = self.proc.stdout.readline()
+                if not ln or ln.strip() in ("ready", "unavailable"):
+                    break
+                head.append(ln)
+            if ln.strip() == "ready":
+                self.kind = "nvml"
+                self.lines = head
+                return self
+            self.proc.wait(timeout=5)
+        except (OSError, subprocess.TimeoutExpired):
+            pass
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
                  "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.kind = "nvidia-smi"
         except OSError:
             self.proc = None
         return self
 
     def __exit__(self, *exc):
-        self.lines = []
         if self.proc is not None:
-            self.proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                if self.kind == "nvml":
+                    out, _ = self.proc.communicate(input="", timeout=10)
+                else:
+                    self.proc.terminate()
+                    out, _ = self.proc.communicate(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
                 out, _ = self.proc.communicate()
-            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+            self.lines += [ln for ln in out.splitlines() if ln.strip()]
         return False
 
     def summary(self):
@@ -161,20 +242,23 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
-                continue
             try:
-                sm.append(float(f[1]))
-                smax.append(float(f[2]))
+                if self.kind == "nvml" and len(f) == 3:
+                    sm.append(float(f[0]))
+                    smax.append(float(f[1]))
+                    bits = int(f[2])
+                    reasons.update(n for b, n in NVML_REASONS.items() if bits & b)
+                elif self.kind == "nvidia-smi" and len(f) >= 9:
+                    sm.append(float(f[1]))
+                    smax.append(float(f[2]))
+                    reasons.update(n for n, v in zip(names, f[5:9]) if v.lower() == "active")
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "source": self.kind}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "source": self.kind,
+                "interval_ms": self.interval_ms if self.kind == "nvml" else 100}
 
 
 def problem_tensors(p, device):
@@ -287,11 +371,14 @@ def workload_config(p, S):
             "layout": "bhsd" if p.layout == 1 else "varlen", "in_dtype": p.dtype,
             "query_tokens": p.tq,
             "num_splits": S, "kv_bytes": p.kv_bytes,
-            "l2": "flushed between steps (write then read of 2x L2 size)"}
+            "l2": "flushed between steps (write then read of 2x L2 size)"
+                  + ("; the K/V inputs also exceed L2" if p.kv_bytes > 129e6 else "")}
 
 
 def main():
     args = parse()
+    if args.clock_sampler is not None:
+        raise SystemExit(nvml_sampler_main(args.clock_sampler, args.clock_interval_ms))
     world, rank, local = dist_env()
     from synth.workloads import materialize, workload
     if args.tq > 1:
@@ -519,13 +606,15 @@ def main():
     q_bytes = p.B * p.tq * p.Hq * p.D * 2
     alg_bytes = p.kv_bytes + q_bytes + 4 * (p.B + 1) + ws_bytes
     achieved = alg_bytes / (split_mean_ms * 1e-3) / 1e9
-    traffic = None if (args.cuda_core_math or args.tmem_math) else recorded_traffic(p.name, S)
+    traffic, traffic_src = (None, None) if (args.cuda_core_math or args.tmem_math) else \
+        recorded_traffic(p.name, S)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_step_ms, 5),
         "us_per_call": round(mean_step_ms * 1e3, 2),
         "us_per_call_median": round(statistics.median(step_ms) * 1e3, 2),
         "pct_of_hbm_peak": round(100.0 * value / world / peak, 2),
+        "pct_of_nominal_8tbs": round(100.0 * value / world / NOMINAL_HBM_GBS, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": p.dtype, "data": "synthetic (seeded N(0,1), rounded to the input dtype)",
         "config": {**workload_config(p, S),
@@ -541,7 +630,8 @@ def main():
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "traffic": traffic, "alg_bytes_per_launch": alg_bytes,
+                     "traffic": traffic, "traffic_source": traffic_src,
+                     "alg_bytes_per_launch": alg_bytes,
                      "launch_us_mean": round(split_mean_ms * 1e3, 2),
                      "launches_timed": k_split,
                      **({"combine_us_mean_derived": round((mean_step_ms - split_mean_ms) * 1e3, 2)}

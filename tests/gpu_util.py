@@ -21,8 +21,22 @@ def opart_tol(p) -> float:
     u * max|v|; fp32 accumulation and the exp2 approximation add far less.
     """
     u = 2.0 ** -11 if p.dtype == "f16" else 2.0 ** -8
-    vmax = float(np.abs(_decode(p.v, p.dtype)[np.isfinite(_decode(p.v, p.dtype))]).max()) if p.v.size else 1.0
-    return u * vmax + 1e-5
+    return u * max_abs_finite(p.v, p.dtype) + 1e-5
+
+
+def max_abs_finite(bits, dtype: str) -> float:
+    """Largest |x| over the finite binary16/bfloat16 values among `bits` (uint16 patterns),
+    without widening the whole array: with the sign bit cleared, the bit patterns of finite
+    values order like their magnitudes, and Inf/NaN patterns sit above the largest finite one."""
+    if bits.size == 0:
+        return 1.0
+    inf_bits = 0x7C00 if dtype == "f16" else 0x7F80
+    mag = np.bitwise_and(np.asarray(bits, dtype=np.uint16).reshape(-1), 0x7FFF)
+    finite = mag[mag < inf_bits]
+    if finite.size == 0:
+        return 1.0
+    top = np.array([finite.max()], dtype=np.uint16)
+    return float(_decode(top, dtype)[0])
 
 
 def _decode(bits, dtype):

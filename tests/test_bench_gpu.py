@@ -33,21 +33,25 @@ def test_default_line_has_the_contract_fields():
         assert key in d, key
     assert d["n_gpus"] == 1 and d["steps"] == 20 and d["warmup"] == 3
     assert d["unit"] == "GB/s" and d["higher_is_better"] is True and d["scaling"] == "weak"
-    assert d["config"]["workload"] == "mha_bhsd" and "flush" in d["config"]["l2"]
+    # the largest single-GPU workload: Llama-3.1-8B heads, 16 sequences of 131072 keys, bf16
+    assert d["config"]["workload"] == "llama_S131072_B16" and "flush" in d["config"]["l2"]
+    assert d["dtype"] == "bf16"
     assert 1000.0 < d["value"] < 12000.0                       # KV GB/s on one GB300
+    assert abs(d["pct_of_nominal_8tbs"] - 100.0 * d["value"] / 8000.0) < 0.01
     r = d["roofline"]
     assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] > 0
     assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-3 and 0.1 < r["frac"] < 1.5
-    assert r["alg_bytes_per_launch"] >= 2 * 8 * 32 * 4096 * 128 * 2   # at least the K/V bytes
+    kv = 2 * 16 * 8 * 131072 * 128 * 2
+    assert r["alg_bytes_per_launch"] >= kv                     # at least the K/V bytes
     if r["traffic"] is not None:                                # recorded for this kernel source
         assert 0.9 * r["alg_bytes_per_launch"] < r["traffic"] < 1.2 * r["alg_bytes_per_launch"]
     e = d["e2e"]
     assert e["unit"] == "GB/s" and 0 < e["value"] < d["value"]
-    assert e["h2d_bytes_per_step"] >= 2 * 8 * 32 * 4096 * 128 * 2 and e["d2h_bytes_per_step"] == 8 * 32 * 128 * 2
+    assert e["h2d_bytes_per_step"] >= kv and e["d2h_bytes_per_step"] == 16 * 32 * 128 * 2
     assert d["gpu_launches"] > 0
-    # a timed region this short can end between two clock samples (200 ms apart)
+    # NVML samples every 2 ms: even a short timed region has clock samples
     k = d["clocks"]
-    assert (k["sm_mhz"] is not None and k["sm_mhz"] > 0) or k["reasons"] == ["no samples"]
+    assert k["source"] == "nvml" and k["samples"] >= 3 and k["sm_mhz"] > 0 and k["sm_max_mhz"] > 0
     c = d["cpu_baseline"]
     assert c["kind"] == "oracle" and c["cores"] >= 1 and c["value"] > 0 and c["one_thread"]["value"] > 0
     assert d["back_to_back"]["inputs_exceed_l2"] is True and d["back_to_back"]["value"] > 0

@@ -44,6 +44,7 @@ def test_max_over_ranks_without_process_group():
 
 def test_clock_summary_parsing():
     c = bench.ClockSampler(0)
+    c.kind = "nvidia-smi"
     c.lines = [
         "0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
         "0, 1980, 2070, 1350.0, 0x4, Not Active, Not Active, Not Active, Active",
@@ -55,16 +56,43 @@ def test_clock_summary_parsing():
     assert c.summary()["reasons"] == ["no samples"]
 
 
+def test_nvml_clock_summary_parsing():
+    """The NVML child prints 'sm_mhz,max_mhz,reason bits'; bit 0x4 is the software power cap,
+    0x8 the hardware slowdown (nvml.h clock-event reasons); idle (0x1) is not a slowdown."""
+    c = bench.ClockSampler(0)
+    c.kind = "nvml"
+    c.lines = ["2070,2070,0", "1995,2070,4", "2070,2070,1", "1500,2070,12"]
+    s = c.summary()
+    assert s["samples"] == 4 and s["sm_mhz"] == 2032.5 and s["sm_max_mhz"] == 2070
+    assert s["reasons"] == ["hw_slowdown", "sw_power_cap"] and s["source"] == "nvml"
+
+
+def test_clock_sampler_without_a_gpu_returns_no_samples_or_a_summary():
+    """Here (no GPU, no NVML) the child reports it is unavailable and the sampler falls back;
+    whatever it gets, it never raises and never blocks."""
+    with bench.ClockSampler(0, interval_ms=1.0) as c:
+        pass
+    s = c.summary()
+    assert "reasons" in s
+
+
 def test_recorded_traffic_needs_current_kernel(tmp_path, monkeypatch):
     f = tmp_path / "t.json"
     f.write_text('{"entries": [{"kernel_sha": "%s", "workload": "w", "num_splits": 3, '
                  '"dram_bytes_per_launch": 123.0}]}' % bench.kernel_sha())
     monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
-    assert bench.recorded_traffic("w", 3) == 123.0
-    assert bench.recorded_traffic("w", 4) is None
+    assert bench.recorded_traffic("w", 3)[0] == 123.0
+    assert bench.recorded_traffic("w", 4) == (None, None)
     f.write_text('{"entries": [{"kernel_sha": "old", "workload": "w", "num_splits": 3, '
                  '"dram_bytes_per_launch": 1.0}]}')
-    assert bench.recorded_traffic("w", 3) is None
+    assert bench.recorded_traffic("w", 3) == (None, None)
+    # a capture on a smaller case stands for a larger one of the same shape, scaled
+    f.write_text('{"entries": [{"kernel_sha": "%s", "workload": "small", "num_splits": 4, '
+                 '"dram_bytes_per_launch": 100.0, "scale_to": {"big": 4.0}}]}' % bench.kernel_sha())
+    b, src = bench.recorded_traffic("big", 4)
+    assert b == 400.0 and "small" in src and "x4.0" in src
+    assert bench.recorded_traffic("big", 3) == (None, None)
+    assert bench.recorded_traffic("small", 4)[0] == 100.0
 
 
 def test_reference_arm_prints_one_json_line():

@@ -95,31 +95,46 @@ def test_multiquery_one_token_matches_single_query_bit_for_bit():
     assert np.array_equal(a, out.to(torch.float64).cpu().numpy())
 
 
-def test_multiquery_long_context_sampled():
-    """Llama heads, 16 sequences of 32768 keys, two query tokens each (speculative decoding)."""
+def test_multiquery_long_context_every_element():
+    """Llama heads, 16 sequences of 32768 keys, two query tokens each (speculative decoding), at
+    the picker's split count: every output row and every per-split partial against the oracle."""
     tq = 2
     p = custom("llama_S32768_B16_tq2", 16, 32, 8, 128, [32768] * 16, "bf16", LAYOUT_VARLEN, None,
                seed=0, tq=tq)
     S = da.num_splits(p.B, p.Hq * tq, p.Hkv, p.D, 32768, 32768)
     out, lse, opart, err = run_mq(p, tq, S)
     assert err == 0
-    rng = np.random.default_rng(2)
-    rb = rng.integers(0, p.B, 16).astype(np.int32)
-    rt = rng.integers(0, tq, 16).astype(np.int32)
-    rh = rng.integers(0, p.Hq, 16).astype(np.int32)
-    ref, _ = oracle.default().attention_rows_mq(p, tq, rb, rt, rh)
-    assert out_excess(out[rb, rt, rh], ref, p.dtype) <= OUT_TOL
+    orc = oracle.default()
+    ref, _ = orc.attention_mq(p, tq)
+    assert out_excess(out, ref, p.dtype) <= OUT_TOL
+    ref_op, ref_lse = orc.split_partials_mq(p, tq, S)
+    assert np.array_equal(np.isneginf(lse), np.isneginf(ref_lse))
+    assert max_abs(lse, ref_lse) <= LSE_TOL
+    assert max_abs(opart, ref_op) <= opart_tol(p)
+
+
+_MQ_REF = {}
+
+
+def _mq_reference(name, tq):
+    """The workload with tq query tokens and the oracle's output for it (shared by both arms)."""
+    from synth.workloads import materialize, workload
+    if (name, tq) not in _MQ_REF:
+        p = workload(name, data=False)
+        p.tq = tq
+        materialize(p)
+        ref, _ = oracle.default().attention_mq(p, tq)
+        _MQ_REF[(name, tq)] = (p, ref)
+    return _MQ_REF[(name, tq)]
 
 
 @pytest.mark.parametrize("name,tq", [("qwen_varlen", 4), ("llama_S8192_B16", 4)])
 @pytest.mark.parametrize("arm", ["mma_sync", "tmem"])
-def test_multiquery_named_workloads_sampled(name, tq, arm):
+def test_multiquery_named_workloads_every_row(name, tq, arm):
     """Full-size workloads with several query tokens, the picker's split count (as the benchmark
-    times them), sampled (sequence, token, head) rows; both the default path and the tcgen05 arm."""
-    from synth.workloads import materialize, workload
-    p = workload(name, data=False)
-    p.tq = tq
-    materialize(p)
+    times them): every (sequence, token, head) row against the oracle, on both the default path
+    and the tcgen05 arm; on the default path every per-split partial as well."""
+    p, ref = _mq_reference(name, tq)
     S = da.num_splits(p.B, p.Hq * tq, p.Hkv, p.D, min(p.lens), max(p.lens))
     fn = da.decode_attn_splitkv_multiquery if arm == "mma_sync" else da.decode_attn_splitkv_multiquery_tmem
     q, k, v, cu = to_device(p)
@@ -130,13 +145,15 @@ def test_multiquery_named_workloads_sampled(name, tq, arm):
     assert da.decode_attn_splitkv_get_error(ws) == 0
     out = out.to(torch.float64).cpu().numpy()
     assert np.isfinite(out).all()
-    rng = np.random.default_rng(5)
-    n = 24
-    rb = np.concatenate([[0, p.B - 1], rng.integers(0, p.B, n)]).astype(np.int32)
-    rt = np.concatenate([[0, tq - 1], rng.integers(0, tq, n)]).astype(np.int32)
-    rh = np.concatenate([[0, p.Hq - 1], rng.integers(0, p.Hq, n)]).astype(np.int32)
-    ref, _ = oracle.default().attention_rows_mq(p, tq, rb, rt, rh)
-    assert out_excess(out[rb, rt, rh], ref, p.dtype) <= OUT_TOL
+    assert out_excess(out, ref, p.dtype) <= OUT_TOL
+    if arm == "mma_sync":
+        lse, opart = da.workspace_views(ws, p.B * tq, p.Hq, p.D, S)
+        lse = lse.to(torch.float64).cpu().numpy().reshape(p.B, tq, p.Hq, S)
+        opart = opart.to(torch.float64).cpu().numpy().reshape(p.B, tq, p.Hq, S, p.D)
+        ref_op, ref_lse = oracle.default().split_partials_mq(p, tq, S)
+        assert np.array_equal(np.isneginf(lse), np.isneginf(ref_lse))
+        assert max_abs(lse, ref_lse) <= LSE_TOL
+        assert max_abs(opart, ref_op) <= opart_tol(p)
 
 
 def test_multiquery_d64_bhsd_bf16():

@@ -111,24 +111,114 @@ def test_split_bounds_bit_exact_q_zero(S):
 
 
 @pytest.mark.parametrize("name", [n for n in all_workload_names() if n != "tiny"])
-def test_named_workloads_sampled(name):
-    """Full-size workloads in the launch configuration the benchmark uses, sampled rows."""
+def test_named_workloads_every_element(name):
+    """Full-size workloads in the launch configuration the benchmark uses (the picker's split
+    count): every output row against the plain definition, and every per-split lse_s and o_s
+    against the oracle's split partials at that split count."""
     p = workload(name)
     S = p.num_splits or da.num_splits(p.B, p.Hq, p.Hkv, p.D, min(p.lens), max(p.lens))
     out, lse, opart, err = run(p, S)
     assert err == 0
-    assert np.isfinite(out).all() and np.isfinite(lse).all() and np.isfinite(opart).all()
-    rng = np.random.default_rng(0)
-    n = 24
-    rb = np.concatenate([[0, p.B - 1], rng.integers(0, p.B, n)]).astype(np.int32)
-    rh = np.concatenate([[0, p.Hq - 1], rng.integers(0, p.Hq, n)]).astype(np.int32)
-    ref, ref_lse = oracle.default().attention_rows(p, rb, rh)
-    e = max_abs(out[rb, rh], ref)
+    orc = oracle.default()
+    ref, ref_lse = orc.attention(p)
+    e = max_abs(out, ref)
     assert e <= OUT_TOL, f"{name}: out max|d| {e}"
-    # every split's log-sum-exp merges back to the row's total (property at any size)
-    m = lse[rb, rh].max(axis=1, keepdims=True)
-    tot = m[:, 0] + np.log(np.exp(lse[rb, rh] - m).sum(axis=1))
+    ref_op, ref_lp = orc.split_partials(p, S)
+    assert np.array_equal(np.isneginf(lse), np.isneginf(ref_lp)), "empty-split pattern differs"
+    e_lse = max_abs(lse, ref_lp)
+    assert e_lse <= LSE_TOL, f"{name}: lse_part max|d| {e_lse}"
+    e_op = max_abs(opart, ref_op)
+    assert e_op <= opart_tol(p), f"{name}: o_part max|d| {e_op} > {opart_tol(p)}"
+    # the per-split log-sum-exps merge back to the row's total
+    m = lse.max(axis=2, keepdims=True)
+    tot = m[..., 0] + np.log(np.exp(lse - m).sum(axis=2))
     assert np.abs(tot - ref_lse).max() <= LSE_TOL
+
+
+def _set_bits(p, name, values):
+    """Round float values to the problem's dtype and store them as p.<name> bit patterns."""
+    t = torch.from_numpy(np.ascontiguousarray(values, dtype=np.float32)).to(torch_dtype(p))
+    setattr(p, name, t.view(torch.int16).numpy().view(np.uint16).reshape(getattr(p, name).shape))
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("layout", [LAYOUT_VARLEN, LAYOUT_BHSD], ids=["varlen", "bhsd"])
+def test_single_token_ramping_scores(dtype, layout):
+    """8-column items (one query token, G = 4) whose scores climb key after key: head 0 of
+    each group by 0.068 and head 2 by 0.136 (log2 units) per key, so the running max moves on
+    almost every 16-key box, in every warp and stage, and the accumulator is rescaled each time;
+    heads 1 and 3 see falling scores and keep the first box's max. Every element of the output
+    and of the per-split partials is checked."""
+    B, Hq, Hkv, D, lens, S = 2, 8, 2, 128, [1500, 700], 3
+    p = custom("ramp1", B, Hq, Hkv, D, lens, dtype, layout, S, seed=31, kv_rows=1536)
+    q = np.zeros((B, Hq, D), np.float32)
+    q[:, 0::4, :] = 0.25
+    q[:, 1::4, :] = -0.25
+    q[:, 2::4, :] = 0.5
+    q[:, 3::4, :] = -0.5
+    _set_bits(p, "q", q)
+    kf = np.zeros(p.k.shape, np.float32)
+    for b, L in enumerate(lens):
+        ramp = (np.arange(L) / 60.0).astype(np.float32)   # scale * q.k_j = 2.83 * j / 60 at 0.25
+        if layout == LAYOUT_BHSD:
+            kf[b, :, :L, :] = ramp[None, :, None]
+        else:
+            kf[p.cu[b]:p.cu[b] + L, :, :] = ramp[:, None, None]
+    _set_bits(p, "k", kf)
+    if layout == LAYOUT_BHSD:
+        for b, L in enumerate(lens):
+            p.k[b, :, L:, :] = 0x7E00 if dtype == "f16" else 0x7FC0
+            p.v[b, :, L:, :] = 0x7E00 if dtype == "f16" else 0x7FC0
+    check_full(p, S)
+
+
+def _fp32_ulp(x):
+    a = np.abs(np.asarray(x, dtype=np.float64))
+    return np.ldexp(1.0, (np.floor(np.log2(np.where(a > 0, a, 1.0))) - 23).astype(int))
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("layout", [LAYOUT_VARLEN, LAYOUT_BHSD], ids=["varlen", "bhsd"])
+def test_single_token_one_key_dominates(dtype, layout):
+    """One key scores more than 1000 above every other key of its sequence, late in a split
+    (key 990 of [500, 1000), in the last stage's third warp): the heads that see it must return
+    its value row, the others the ordinary softmax. The GPU twin of the oracle's one-hot pin.
+
+    The split holding that key has lse_s near 1000, where one fp32 ulp is 2^-13: its bound is
+    1e-4 plus 8 ulps of |lse| (the fp32 rounding of the score, of scale * log2 e folded into one
+    constant, of the log2-domain sum and of the product by ln 2); every other value keeps the
+    fixed bounds."""
+    B, Hq, Hkv, D, lens, S = 2, 8, 2, 128, [1500, 700], 3
+    p = custom("dom1", B, Hq, Hkv, D, lens, dtype, layout, S, seed=32, kv_rows=1536, k_std=0.25)
+    q = np.zeros((B, Hq, D), np.float32)
+    q[:, 0::2, :] = 4.0           # even heads: the planted key scores 4 * 23 * 128 / sqrt(128) = 1041
+    q[:, 1::2, :] = -0.125        # odd heads: it scores -32, far below their usual keys
+    _set_bits(p, "q", q)
+    j = 990
+    if layout == LAYOUT_BHSD:
+        p.k[0, :, j, :] = 0x4DC0 if dtype == "f16" else 0x41B8   # 23.0
+    else:
+        p.k[p.cu[0] + j, :, :] = 0x4DC0 if dtype == "f16" else 0x41B8
+    if layout == LAYOUT_BHSD:
+        for b, L in enumerate(lens):
+            p.k[b, :, L:, :] = 0x7E00 if dtype == "f16" else 0x7FC0
+            p.v[b, :, L:, :] = 0x7E00 if dtype == "f16" else 0x7FC0
+    out, lse, opart, err = run(p, S)
+    assert err == 0
+    orc = oracle.default()
+    ref, _ = orc.attention(p)
+    ref_op, ref_lp = orc.split_partials(p, S)
+    assert out_excess(out, ref, p.dtype) <= OUT_TOL
+    # the even heads of sequence 0 return the planted key's value row
+    from gpu_util import _decode
+    vrow = _decode(p.v[0, :, j, :] if layout == LAYOUT_BHSD else p.v[p.cu[0] + j], dtype)   # [Hkv, D]
+    for h in range(0, Hq, 2):
+        assert np.abs(out[0, h] - vrow[h // (Hq // Hkv)]).max() <= OUT_TOL
+    tol = LSE_TOL + 8 * _fp32_ulp(ref_lp)
+    assert np.array_equal(np.isneginf(lse), np.isneginf(ref_lp))
+    d = np.where(np.isneginf(ref_lp), 0.0, np.abs(lse - ref_lp))
+    assert (d <= tol).all(), float((d - tol).max())
+    assert max_abs(opart, ref_op) <= opart_tol(p)
 
 
 def test_bad_seqlens_flagged_and_contained():
