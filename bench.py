@@ -71,6 +71,13 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-flush", action="store_true", help="do not flush L2 between steps")
+    ap.add_argument("--read-probe", default="",
+                    help="instead of the decode call, time the read-ceiling probe (a bare bulk-copy "
+                         "stream through shared memory) over these buffer sizes in bytes, comma "
+                         "separated, with the same flush and event pair; prints one JSON line")
+    ap.add_argument("--probe-ctas-per-sm", type=int, default=2)
+    ap.add_argument("--probe-chunk", type=int, default=16384)
+    ap.add_argument("--probe-stages", type=int, default=4)
     ap.add_argument("--clock-sampler", type=int, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--clock-interval-ms", type=float, default=2.0, help=argparse.SUPPRESS)
     return ap.parse_args()
@@ -375,10 +382,64 @@ def workload_config(p, S):
                   + ("; the K/V inputs also exceed L2" if p.kv_bytes > 129e6 else "")}
 
 
+def run_read_probe(args):
+    """Time the read-ceiling probe over buffers of the given sizes: L2 flushed before each
+    launch exactly as for the decode call, CUDA events around the launch alone."""
+    import ctypes
+
+    import torch
+
+    from split_kv_decode_decoding_gb300.build import build_probe
+    lib = ctypes.CDLL(build_probe())
+    lib.read_probe.argtypes = [ctypes.c_void_p, ctypes.c_ulonglong, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                               ctypes.c_void_p, ctypes.c_void_p]
+    lib.read_probe.restype = ctypes.c_int
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_w = torch.empty(max(2 * l2, 64 << 20), dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(max(2 * l2, 64 << 20) // 4, dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    rows = []
+    for nbytes in [int(x) for x in args.read_probe.split(",") if x]:
+        nbytes -= nbytes % 16
+        buf = torch.ones(nbytes // 2, dtype=torch.float16, device=dev)
+        times = []
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup + args.steps):
+                flush_w.fill_(1)
+                flush_r.sum()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                rc = lib.read_probe(ctypes.c_void_p(buf.data_ptr()), nbytes, args.probe_ctas_per_sm,
+                                    args.probe_chunk, args.probe_stages, ctypes.c_void_p(err.data_ptr()),
+                                    ctypes.c_void_p(stream.cuda_stream))
+                if rc != 0:
+                    raise RuntimeError(f"read_probe returned {rc}")
+                e1.record(stream)
+                if i >= args.warmup:
+                    times.append((e0, e1))
+            torch.cuda.synchronize(dev)
+        if int(err.item()) != 0:
+            raise RuntimeError("read_probe: a wait timed out")
+        us = sorted(a.elapsed_time(b) * 1e3 for a, b in times)
+        med = statistics.median(us)
+        rows.append({"bytes": nbytes, "us_median": round(med, 2), "us_min": round(us[0], 2),
+                     "GBps_median": round(nbytes / (med * 1e-6) / 1e9, 1)})
+        del buf
+    print(json.dumps({"probe": "read_ceiling", "ctas_per_sm": args.probe_ctas_per_sm,
+                      "chunk_bytes": args.probe_chunk, "stages": args.probe_stages, "steps": args.steps,
+                      "l2": "flushed before each launch (write then read of 2x L2 size)", "rows": rows}),
+          flush=True)
+
+
 def main():
     args = parse()
     if args.clock_sampler is not None:
         raise SystemExit(nvml_sampler_main(args.clock_sampler, args.clock_interval_ms))
+    if args.read_probe:
+        return run_read_probe(args)
     world, rank, local = dist_env()
     from synth.workloads import materialize, workload
     if args.tq > 1:

@@ -223,6 +223,9 @@ da_status decode_attn_splitkv_combine(int B, int Hq, int D, int num_splits, da_d
  *   workspace      >= decode_attn_splitkv_workspace_size(B, Hq, D, max_splits);
  *                  lse_part/o_part use max_splits as the split stride, and
  *                  entries s >= S_b of a row are left untouched
+ * The rows of a sequence with S_b = 1 are written by the split step itself (its
+ * one split's weight is exactly 1); the combine step merges only the others, and
+ * is not launched when max_splits = 1.
  * Other arguments, results and errors as decode_attn_splitkv.
  */
 da_status decode_attn_splitkv_varsplit(const void* q, const void* k, const void* v,

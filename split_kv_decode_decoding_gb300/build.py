@@ -15,6 +15,9 @@ SOURCES = [os.path.join(CSRC, n) for n in
            ("decode_attn_splitkv.cu", "comparison_arms.cu", "time_model.cpp")]
 HEADER = os.path.join(ROOT, "include", "decode_attn_splitkv.h")
 LIB = os.path.join(PKG, "_build", "libdecode_attn_splitkv.so")
+# the read-ceiling probe the benchmark times beside the decode call (not part of the library)
+PROBE_SRC = os.path.join(CSRC, "read_probe.cu")
+PROBE_LIB = os.path.join(PKG, "_build", "libread_probe.so")
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
@@ -35,6 +38,17 @@ def inputs() -> list:
     """Every file the library is built from (sources and headers)."""
     return SOURCES + [HEADER] + sorted(glob.glob(os.path.join(CSRC, "*.h")) +
                                        glob.glob(os.path.join(CSRC, "*.cuh")))
+
+
+def build_probe(force: bool = False) -> str:
+    """Compile the read-ceiling probe into its own small library."""
+    os.makedirs(os.path.dirname(PROBE_LIB), exist_ok=True)
+    if not force and os.path.exists(PROBE_LIB) and os.path.getmtime(PROBE_LIB) >= os.path.getmtime(PROBE_SRC):
+        return PROBE_LIB
+    tmp = PROBE_LIB + f".tmp{os.getpid()}"
+    subprocess.run([nvcc(), *NVCC_FLAGS, "-shared", "-o", tmp, PROBE_SRC], check=True)
+    os.replace(tmp, PROBE_LIB)
+    return PROBE_LIB
 
 
 def build(force: bool = False, verbose: bool = False) -> str:

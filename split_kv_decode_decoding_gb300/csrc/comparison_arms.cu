@@ -104,7 +104,7 @@ split_kernel_fma(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     constexpr int NT = 1;
     using Sh = Shape<D, NT>;
     extern __shared__ uint8_t smem_raw[];
-    const SplitLayout sl = split_layout<D, NT>(smem_raw, p);
+    const SplitLayout sl = split_layout<D, NT, kStages>(smem_raw, p);
     uint8_t* smem = sl.smem;
     ItemSlot* slots = sl.slots;
     const uint32_t ring = sl.ring, qbuf = sl.qbuf, full0 = sl.full0, empty0 = sl.empty0;
@@ -112,9 +112,9 @@ split_kernel_fma(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     // per consumer warp: softmax weights [16 keys][8 columns] and 8 rescale factors
     float* fma_p = reinterpret_cast<float*>(sl.extra);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    split_setup<NT>(sl, p, &tmK, &tmV, &tmK16, &tmV16);
+    split_setup<NT, kStages>(sl, p, &tmK, &tmV, &tmK16, &tmV16);
     if (warp == kConsumerWarps) {
-        split_producer<D, NT>(sl, p, &tmK, &tmV, &tmK16, &tmV16);
+        split_producer<D, NT, kStages>(sl, p, &tmK, &tmV, &tmK16, &tmV16);
         return;
     }
 

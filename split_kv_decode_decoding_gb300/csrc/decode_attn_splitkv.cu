@@ -61,22 +61,22 @@ constexpr int kMaxVarsplitBatch = 1024;       // sequences, per-sequence mode
 constexpr double kLongStreamBytes = 1.5e9;    // K/V bytes above which even batches are split for balance
 
 // ------------------------------------------------------------ split step
-template <int D, int DT, int NT>
+template <int D, int DT, int NT, int ST>
 __global__ void __launch_bounds__(kThreads, kMinBlocksPerSm)
 split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
              const __grid_constant__ CUtensorMap tmK16, const __grid_constant__ CUtensorMap tmV16,
              const SplitParams p) {
-    using Sh = Shape<D, NT>;
+    using Sh = Shape<D, NT, ST>;
     extern __shared__ uint8_t smem_raw[];
-    const SplitLayout sl = split_layout<D, NT>(smem_raw, p);
+    const SplitLayout sl = split_layout<D, NT, ST>(smem_raw, p);
     uint8_t* smem = sl.smem;
     ItemSlot* slots = sl.slots;
     const uint32_t ring = sl.ring, qbuf = sl.qbuf, full0 = sl.full0, empty0 = sl.empty0;
     const uint32_t ifull0 = sl.ifull0, iempty0 = sl.iempty0, mfull = sl.mfull, mdone = sl.mdone;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    split_setup<NT>(sl, p, &tmK, &tmV, &tmK16, &tmV16);
+    split_setup<NT, ST>(sl, p, &tmK, &tmV, &tmK16, &tmV16);
     if (warp == kConsumerWarps) {
-        split_producer<D, NT>(sl, p, &tmK, &tmV, &tmK16, &tmV16);
+        split_producer<D, NT, ST>(sl, p, &tmK, &tmV, &tmK16, &tmV16);
         return;
     }
 
@@ -230,7 +230,7 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty0 + 8 * st);
-                if (++st == kStages) {
+                if (++st == Sh::kStages) {
                     st = 0;
                     ph ^= 1;
                 }
@@ -436,7 +436,7 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty0 + 8 * st);
-                if (++st == kStages) {
+                if (++st == Sh::kStages) {
                     st = 0;
                     ph ^= 1;
                 }
@@ -504,7 +504,7 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * st);
-        if (++st == kStages) {
+        if (++st == Sh::kStages) {
             st = 0;
             ph ^= 1;
         }
@@ -563,6 +563,8 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams cp) {
         bool bad;
         Srow = seq_splits(checked_len(cp.cu, row / cp.Hq, cp.layout, cp.kv_rows, cp.no_kv, &base, &bad),
                           cp.split_len, S);
+        // a sequence with one split: the split step wrote its rows
+        if (Srow == 1) return;
     }
     const int DC = D / dchunks;
     const int lps = DC / 4;               // lanes per split row
@@ -641,18 +643,23 @@ __global__ void selftest_timeout_kernel(uint32_t* err, unsigned long long limit_
 }
 
 // ------------------------------------------------------------ host side
-template <int D, int DT, int NT>
+template <int D, int DT, int NT, int ST>
 da_status launch_split(const Call& c, void* out, cudaStream_t stream) {
     SplitLaunch a;
-    if (!prepare_split<D, NT>(c, out, a)) return DA_ERR_CUDA;
+    if (!prepare_split<D, NT, ST>(c, out, a)) return DA_ERR_CUDA;
     static DeviceCache caches[3];
-    return launch_persistent(split_kernel<D, DT, NT>, a, caches[a.cache_idx], stream);
+    return launch_persistent(split_kernel<D, DT, NT, ST>, a, caches[a.cache_idx], stream);
 }
 
-// dims per combine warp: enough warps to cover the GPU, at least 8 dims each
-int combine_dchunks(int rows, int D, int S) {
+
+// dims per combine warp: enough warps to cover the GPU, at least 8 dims each. With
+// per-sequence split counts the rows of one-split sequences return at once and the
+// others may hold up to S splits, so the slices narrow with S alone: a lane then
+// keeps every split of its slice in flight in a few loads.
+int combine_dchunks(int rows, int D, int S, bool per_sequence) {
     int dchunks = 1;
-    while (D / dchunks > 8 && static_cast<int64_t>(rows) * dchunks < 2048 && S > 4 * dchunks) dchunks *= 2;
+    while (D / dchunks > 8 && (per_sequence || static_cast<int64_t>(rows) * dchunks < 2048) && S > 4 * dchunks)
+        dchunks *= 2;
     return dchunks;
 }
 
@@ -666,7 +673,7 @@ da_status launch_combine(const Call& c, void* out, cudaStream_t stream) {
     cp.cu = c.cu;
     cp.rows = c.B * c.tq * c.Hq;
     cp.S = c.S;
-    cp.dchunks = combine_dchunks(cp.rows, D, c.S);
+    cp.dchunks = combine_dchunks(cp.rows, D, c.S, c.split_len != 0);
     cp.Hq = c.Hq * c.tq;   // rows per sequence
     cp.split_len = c.split_len;
     cp.layout = c.lay;
@@ -687,8 +694,8 @@ da_status launch_combine(const Call& c, void* out, cudaStream_t stream) {
 template <int D, int DT>
 da_status launch_split_cols(const Call& c, void* out, cudaStream_t st) {
     const bool wide = item_cols(static_cast<int64_t>(c.Hq / c.Hkv) * c.tq) > kHeadsPerCta;
-    if (wide) return launch_split<D, DT, 2>(c, out, st);
-    return launch_split<D, DT, 1>(c, out, st);
+    if (wide) return launch_split<D, DT, 2, kStages>(c, out, st);
+    return launch_split<D, DT, 1, kStages>(c, out, st);
 }
 
 da_status dispatch_split(const Call& c, void* out, cudaStream_t st) {
@@ -703,10 +710,11 @@ da_status dispatch_combine(const Call& c, void* out, cudaStream_t st) {
     return c.dt == DA_F16 ? launch_combine<64, DA_F16>(c, out, st) : launch_combine<64, DA_BF16>(c, out, st);
 }
 
-// Split step, then the combine step unless a single uniform split already wrote `out`.
+// Split step, then the combine step unless every sequence has a single split
+// (S = 1, or a per-sequence cap of 1): the split step then wrote all of `out`.
 da_status run_decode(const Call& c, void* out, cudaStream_t st) {
     da_status r = dispatch_split(c, out, st);
-    if (r != DA_OK || (c.S == 1 && c.split_len == 0)) return r;
+    if (r != DA_OK || c.S == 1) return r;
     return dispatch_combine(c, out, st);
 }
 

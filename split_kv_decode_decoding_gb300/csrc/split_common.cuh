@@ -42,15 +42,16 @@ constexpr int kStagedBytes = ((kMaxStagedBatch + 1) * 4 + 15) / 16 * 16;   // on
 
 struct ItemSlot {          // one work item, as the producer decoded it
     int32_t b, kvh, h0, nh;            // h0: first query head of the KV head's group; nh columns
-    int32_t s, nkeys, ntiles, valid;   // valid = 0 marks the end of the queue
+    int32_t s, nkeys, ntiles, valid;   // valid: 0 end of the queue, 1 an item, 2 the only split of its sequence
     int64_t first_key;                 // varlen: K/V row of the split start; bhsd: position
     int32_t c0;                        // first packed (token, head) column of this item
     int32_t vis0;                      // keys of the split query token 0 may see (may be <= 0)
 };
 static_assert(sizeof(ItemSlot) == 48, "ItemSlot layout");
 
-template <int D, int NT>
+template <int D, int NT, int ST = kStages>
 struct Shape {
+    static constexpr int kStages = ST;                             // ring depth
     static constexpr int kHalves = D / 64;                         // 128-byte column slices
     static constexpr int kSliceBytes = kStageKeys * 128;           // one slice of a stage tile
     static constexpr int kTileBytes = kHalves * kSliceBytes;       // K (or V) bytes per stage
@@ -82,7 +83,7 @@ struct SplitParams {
     uint32_t* err;           // device error word
     uint32_t* work;          // work-queue head
     uint32_t* done;          // CTAs finished
-    uint16_t* out;           // [B, Hq, D] when S == 1 (o_0 is the output), else nullptr
+    uint16_t* out;           // [B, Hq, D]: rows of sequences with one split are written here (nullptr: none)
     int B, Hq, Hkv, G, S, kv_rows, layout, chunks, no_kv, n_items;
     int split_len;           // 0: every sequence has S splits; else S_b = min(S, ceil(L_b / split_len))
     int stage_cu;            // cu_seqlens_k staged in shared memory (B small enough)
@@ -378,7 +379,9 @@ __device__ __forceinline__ ItemSlot decode_item_cols(const SplitParams& p, int i
     // query token t sits at position L - tq + t and sees keys up to it
     const int64_t vis0 = L - p.tq + 1 - lo;
     it.vis0 = static_cast<int>(vis0 < -(1 << 30) ? -(1 << 30) : vis0);
-    it.valid = 1;
+    // the only split of its sequence: its weight in the combine is exactly 1, so the
+    // split step writes the output row itself
+    it.valid = Sb == 1 ? 2 : 1;
     return it;
 }
 
@@ -403,7 +406,7 @@ struct SplitLayout {
     uint8_t* smem;          // 1024-byte aligned base: the K/V ring
     ItemSlot* slots;        // [kItemSlots] item descriptors
     uint32_t ring, qbuf;    // shared addresses of the ring and the Q rows [kItemSlots][columns][D]
-    uint32_t full0, empty0; // [kStages] stage landed / stage released
+    uint32_t full0, empty0; // [stages] stage landed / stage released
     uint32_t ifull0, iempty0;   // [kItemSlots] descriptor published / slot released
     uint32_t mfull, mdone;  // an item's per-warp partials written; (two n-tiles) a merge round read
     int32_t* cus;           // cu_seqlens_k [B + 1] staged in shared memory, or nullptr
@@ -411,17 +414,17 @@ struct SplitLayout {
     uint8_t* extra;         // past the staged arrays (free for the kernel's own use)
 };
 
-template <int D, int NT>
+template <int D, int NT, int ST>
 __device__ __forceinline__ SplitLayout split_layout(uint8_t* smem_raw, const SplitParams& p) {
-    using Sh = Shape<D, NT>;
+    using Sh = Shape<D, NT, ST>;
     SplitLayout s;
     s.smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     s.slots = reinterpret_cast<ItemSlot*>(s.smem + Sh::kSlotOff);
     s.ring = smem_addr(s.smem);
     s.qbuf = s.ring + Sh::kQOff;
     s.full0 = s.ring + Sh::kBarOff;
-    s.empty0 = s.full0 + 8 * kStages;
-    s.ifull0 = s.empty0 + 8 * kStages;
+    s.empty0 = s.full0 + 8 * ST;
+    s.ifull0 = s.empty0 + 8 * ST;
     s.iempty0 = s.ifull0 + 8 * kItemSlots;
     s.mfull = s.iempty0 + 8 * kItemSlots;
     s.mdone = s.mfull + 8;
@@ -433,13 +436,13 @@ __device__ __forceinline__ SplitLayout split_layout(uint8_t* smem_raw, const Spl
 
 // Barrier set-up and tensor-map prefetch; everything before the grid-dependency
 // wait overlaps the previous kernel in the stream.
-template <int NT>
+template <int NT, int ST>
 __device__ __forceinline__ void split_setup(const SplitLayout& sl, const SplitParams& p, const CUtensorMap* tmK,
                                             const CUtensorMap* tmV, const CUtensorMap* tmK16,
                                             const CUtensorMap* tmV16) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < ST; ++i) {
             mbar_init(sl.full0 + 8 * i, 1);
             mbar_init(sl.empty0 + 8 * i, kConsumerWarps);
         }
@@ -467,11 +470,11 @@ __device__ __forceinline__ void split_setup(const SplitLayout& sl, const SplitPa
 // item's descriptor and bulk-copies its Q rows, and streams its K/V tiles into
 // the ring; after an item's tiles it hands the consumers one ring stage, empty,
 // for the item's merge.
-template <int D, int NT>
+template <int D, int NT, int ST>
 __device__ __forceinline__ void split_producer(const SplitLayout& sl, const SplitParams& p, const CUtensorMap* ptmK,
                                                const CUtensorMap* ptmV, const CUtensorMap* ptmK16,
                                                const CUtensorMap* ptmV16) {
-    using Sh = Shape<D, NT>;
+    using Sh = Shape<D, NT, ST>;
     const int lane = threadIdx.x & 31;
     const CUtensorMap& tmK = *ptmK;
     const CUtensorMap& tmV = *ptmV;
@@ -569,7 +572,7 @@ __device__ __forceinline__ void split_producer(const SplitLayout& sl, const Spli
             // last tile: the atomic's round trip then overlaps the last copies, yet a
             // CTA never holds a reserved item for long (which would hurt the balance
             // at the end of the queue).
-            const int fetch_at = max(0, item.ntiles - kStages);
+            const int fetch_at = max(0, item.ntiles - Sh::kStages);
             int next_idx = 0;
             if (item.ntiles == 0) next_idx = static_cast<int>(gridDim.x + atomicAdd(p.work, 1u));
             bool ok = true;
@@ -617,7 +620,7 @@ __device__ __forceinline__ void split_producer(const SplitLayout& sl, const Spli
                         }
                     }
                 }
-                if (++st == kStages) {
+                if (++st == Sh::kStages) {
                     st = 0;
                     ph ^= 1;
                 }
@@ -634,7 +637,7 @@ __device__ __forceinline__ void split_producer(const SplitLayout& sl, const Spli
                 break;
             }
             mbar_arrive(full0 + 8 * st);
-            if (++st == kStages) {
+            if (++st == Sh::kStages) {
                 st = 0;
                 ph ^= 1;
             }
@@ -694,8 +697,8 @@ __device__ __forceinline__ void merge_write(const SplitParams& p, const ItemSlot
             const int64_t row = qrow * p.S + item.s;
             *reinterpret_cast<float4*>(p.opart + row * D + d0) = o;
             if (d0 == 0) p.lse[row] = M == -INFINITY ? -INFINITY : (M + fast_log2(lsum)) * kLn2;
-            // one split: its weight exp(lse_0 - lse) is 1, so o_0 is the answer
-            if (p.out != nullptr)
+            // the sequence's only split: its weight exp(lse_0 - lse) is 1, so o_0 is the answer
+            if (p.out != nullptr && item.valid == 2)
                 *reinterpret_cast<uint2*>(p.out + qrow * D + d0) = make_uint2(pack2<DT>(o.x, o.y), pack2<DT>(o.z, o.w));
         }
     }
@@ -883,8 +886,9 @@ struct SplitLaunch {
     int cache_idx;   // which DeviceCache: the number of [B + 1] arrays staged in shared memory
 };
 
-// `out` is written by the split kernel itself only with one uniform split.
-template <int D, int NT>
+// `out` (nullptr for the split step alone) gets the rows of every sequence that has
+// a single split, whose o_0 is already the answer.
+template <int D, int NT, int ST = kStages>
 inline bool prepare_split(const Call& c, void* out, SplitLaunch& a) {
     std::memset(&a.mk, 0, sizeof(a.mk));
     std::memset(&a.mv, 0, sizeof(a.mv));
@@ -904,7 +908,7 @@ inline bool prepare_split(const Call& c, void* out, SplitLaunch& a) {
     p.err = reinterpret_cast<uint32_t*>(wsb);
     p.work = reinterpret_cast<uint32_t*>(wsb + kWorkCounterOff);
     p.done = reinterpret_cast<uint32_t*>(wsb + kDoneCounterOff);
-    p.out = (c.S == 1 && c.split_len == 0) ? static_cast<uint16_t*>(out) : nullptr;
+    p.out = static_cast<uint16_t*>(out);
     p.lse = reinterpret_cast<float*>(wsb + kHeaderBytes);
     p.opart = reinterpret_cast<float*>(wsb + kHeaderBytes +
                                        round_up(static_cast<size_t>(c.B) * c.tq * c.Hq * c.S * 4, 256));
@@ -924,7 +928,7 @@ inline bool prepare_split(const Call& c, void* out, SplitLaunch& a) {
     p.scale_log2 = c.scale * kLog2e;
     p.wait_limit_ns = kWaitLimitNs;
     const bool var = c.split_len != 0;
-    a.smem = Shape<D, NT>::kSmemBytes + (p.stage_cu ? kStagedBytes : 0) + (var ? kStagedBytes : 0);
+    a.smem = Shape<D, NT, ST>::kSmemBytes + (p.stage_cu ? kStagedBytes : 0) + (var ? kStagedBytes : 0);
     a.cache_idx = (p.stage_cu ? 1 : 0) + (var ? 1 : 0);
     return true;
 }
