@@ -60,7 +60,7 @@ def test_workspace_layout(lib):
     B, Hq, D, S = 3, 28, 128, 7
     lo = lib.decode_attn_splitkv_lse_offset()
     oo = lib.decode_attn_splitkv_opart_offset(B, Hq, S)
-    assert lo == 256 and oo % 256 == 0 and oo >= lo + 4 * B * Hq * S
+    assert lo == 4096 and oo % 256 == 0 and oo >= lo + 4 * B * Hq * S
     assert da.workspace_size(B, Hq, D, S) == oo + 4 * B * Hq * S * D
     assert da.workspace_size(0, Hq, D, S) == 0
     assert da.workspace_size(B, Hq, D, 0) == 0
@@ -204,9 +204,12 @@ def test_binding_refuses_without_library(tmp_path):
 def test_varsplit_plan(lib):
     n, m = da.varsplit_plan(64, 28, 4, 128, 64 * 4352, 8192, 152)
     assert n % 64 == 0 and n >= 256 and m == -(-8192 // n)
-    # about eight items per SM over the whole batch
+    # items of about 0.4 of one CTA's share (304 CTAs at head_dim 128): 2.5 per CTA
     items = 64 * 4352 * 4 / n
-    assert 8 * 152 * 0.8 <= items <= 8 * 152 * 1.2
+    assert 2.5 * 304 * 0.9 <= items <= 2.5 * 304 * 1.05
+    # one long sequence among short ones: it gets at most about half the CTAs' worth of items
+    n, m = da.varsplit_plan(16, 32, 8, 128, 131072 + 15 * 512, 131072, 152)
+    assert n % 64 == 0 and 8 * m <= 304 // 2 + 8 and n >= 2 * 131072 * 8 // 304
     n, m = da.varsplit_plan(2, 4, 1, 64, 237, 200, 152)
     assert (n, m) == (256, 1)
     with pytest.raises(ValueError):
