@@ -89,15 +89,12 @@ typedef enum {
 /*
  * Workspace layout (all offsets from the workspace base, which must be
  * 256-byte aligned):
- *   [0, 4096)           header: uint32 device error word at offset 0, the split step's
- *                       work-queue counters at offsets 64 and 128, [192, 256) reserved,
- *                       then from offset 256 one pair of uint32 counters per (sequence,
- *                       KV head, column chunk) for the single-wave merge (see
- *                       decode_attn_splitkv). Every counter is zero between calls: the
- *                       call that uses it re-arms it.
- *   [4096, 4096 + A)    lse_part, float32 [B, Hq, num_splits], natural log of the
+ *   [0, 256)            header: uint32 device error word at offset 0, the split step's
+ *                       work-queue counters at offsets 64 and 128 (zero between calls:
+ *                       the last CTA of each call re-arms them), rest reserved
+ *   [256, 256 + A)      lse_part, float32 [B, Hq, num_splits], natural log of the
  *                       scaled scores, A = round_up(B*Hq*num_splits*4, 256)
- *   [4096 + A, total)   o_part, float32 [B, Hq, num_splits, D], normalised per split
+ *   [256 + A, total)    o_part, float32 [B, Hq, num_splits, D], normalised per split
  * Returns the total size in bytes, or 0 if an argument is out of range.
  */
 size_t decode_attn_splitkv_workspace_size(int B, int Hq, int D, int num_splits);
@@ -107,10 +104,10 @@ size_t decode_attn_splitkv_lse_offset(void);
 size_t decode_attn_splitkv_opart_offset(int B, int Hq, int num_splits);
 
 /*
- * Zero the workspace header (the device error word and every counter). Call
- * once on a freshly allocated workspace before its first use, and again after a
- * DA_DEVERR_TIMEOUT. Enqueued on `stream`.
- * Errors: DA_ERR_INVALID_ARG (NULL, or smaller than the 4096-byte header),
+ * Zero the workspace header (the device error word and the work-queue
+ * counters). Call once on a freshly allocated workspace before its first use,
+ * and again after a DA_DEVERR_TIMEOUT. Enqueued on `stream`.
+ * Errors: DA_ERR_INVALID_ARG (NULL, or fewer than 256 bytes),
  * DA_ERR_ALIGNMENT (not 256-byte aligned), DA_ERR_CUDA.
  */
 da_status decode_attn_splitkv_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
@@ -144,12 +141,7 @@ void decode_attn_splitkv_split_range(int64_t L, int num_splits, int s, int64_t* 
 
 /*
  * The whole decode attention: the split step, then the combine step, both on
- * `stream`. When every work item of the split step fits one wave of resident
- * CTAs (B * Hkv * column chunks * num_splits no more than the CTAs the device
- * holds at once, num_splits > 1), the split kernel is launched cooperatively and
- * the CTAs of each (sequence, KV head, column chunk) wait for each other and
- * merge its splits themselves, each writing a slice of the output: no combine
- * kernel runs. The results, and the partials left in the workspace, are the same.
+ * `stream`.
  *   q              device, [B, Hq, D] elements of `dtype`, 16-byte aligned
  *   k, v           device, layout per `layout` (above), 16-byte aligned; may be
  *                  NULL only when kv_rows == 0

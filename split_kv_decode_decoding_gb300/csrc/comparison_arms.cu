@@ -977,7 +977,6 @@ da_status launch_split_tc(const Call& c, void* out, cudaStream_t stream) {
     p.work = reinterpret_cast<uint32_t*>(wsb + kWorkCounterOff);
     p.done = reinterpret_cast<uint32_t*>(wsb + kDoneCounterOff);
     p.out = (c.S == 1 && c.split_len == 0) ? static_cast<uint16_t*>(out) : nullptr;
-    p.wave = nullptr;
     p.lse = reinterpret_cast<float*>(wsb + decode_attn_splitkv_lse_offset());
     p.opart = reinterpret_cast<float*>(wsb + decode_attn_splitkv_opart_offset(c.B * c.tq, c.Hq, c.S));
     p.B = c.B;

@@ -510,12 +510,71 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
         }
         if (!ok) break;
     }
-    // single-wave launch: the CTAs of each unit merge its splits (no combine step)
-    if (p.wave != nullptr) ok = wave_merge<D, DT>(p, decode_item<NT * kHeadsPerCta>(p, blockIdx.x, sl.cus, sl.prefix), ok);
     split_finish(p, ok, bad_bar, bad_ph);
 }
 
 // ------------------------------------------------------------ combine step
+// Fold one split (its lse and four dims of its o) into a lane's running
+// (max, sum, weighted accumulator); the max moves up as larger lse arrive, so a
+// single pass over the splits suffices. Empty splits (lse = -inf) weigh 0.
+__device__ __forceinline__ void combine_fold(float lv, float4 ov, float& m, float& z, float4& acc) {
+    if (lv == -INFINITY) return;
+    if (lv > m) {
+        const float sc = fast_exp2((m - lv) * kLog2e);   // 0 when m is still -inf
+        acc.x *= sc;
+        acc.y *= sc;
+        acc.z *= sc;
+        acc.w *= sc;
+        z *= sc;
+        m = lv;
+    }
+    const float w = fast_exp2((lv - m) * kLog2e);
+    acc.x = fmaf(w, ov.x, acc.x);
+    acc.y = fmaf(w, ov.y, acc.y);
+    acc.z = fmaf(w, ov.z, acc.z);
+    acc.w = fmaf(w, ov.w, acc.w);
+    z += w;
+}
+
+// Merge the running states of lanes `first` apart, 2 * first apart, ... up to 16
+// apart: afterwards the lanes that hold the same dims share the merged state
+// (fixed order, deterministic).
+__device__ __forceinline__ void merge_lanes(float& m, float& z, float4& acc, int first) {
+    for (int off = first; off < 32; off <<= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+        const float z2 = __shfl_xor_sync(0xffffffffu, z, off);
+        float4 a2;
+        a2.x = __shfl_xor_sync(0xffffffffu, acc.x, off);
+        a2.y = __shfl_xor_sync(0xffffffffu, acc.y, off);
+        a2.z = __shfl_xor_sync(0xffffffffu, acc.z, off);
+        a2.w = __shfl_xor_sync(0xffffffffu, acc.w, off);
+        const float M = fmaxf(m, m2);
+        if (M != -INFINITY) {
+            const float a = m == -INFINITY ? 0.f : fast_exp2((m - M) * kLog2e);
+            const float b = m2 == -INFINITY ? 0.f : fast_exp2((m2 - M) * kLog2e);
+            acc.x = a * acc.x + b * a2.x;
+            acc.y = a * acc.y + b * a2.y;
+            acc.z = a * acc.z + b * a2.z;
+            acc.w = a * acc.w + b * a2.w;
+            z = a * z + b * z2;
+            m = M;
+        }
+    }
+}
+
+// Four merged dims of an output row: acc / z rounded to the output dtype, or 0 when
+// every split was empty.
+template <int DT>
+__device__ __forceinline__ void store_quad(uint16_t* o, float m, float z, const float4& acc) {
+    if (m == -INFINITY) {
+        *reinterpret_cast<uint2*>(o) = make_uint2(0u, 0u);
+    } else {
+        const float inv = 1.f / z;
+        *reinterpret_cast<uint2*>(o) =
+            make_uint2(pack2<DT>(acc.x * inv, acc.y * inv), pack2<DT>(acc.z * inv, acc.w * inv));
+    }
+}
+
 // One warp per (row = (b, query head), slice of DC = D / dchunks dims). Each
 // lane owns four dims of one split at a time; 32 / (DC / 4) splits are read per
 // iteration, four iterations' loads are issued together, and the lanes' partial
@@ -594,14 +653,12 @@ __global__ void selftest_timeout_kernel(uint32_t* err, unsigned long long limit_
 }
 
 // ------------------------------------------------------------ host side
-// merged: non-null for a call that produces `out`; set when the kernel merged the
-// splits itself (single-wave launch), so that no combine step follows.
 template <int D, int DT, int NT, int ST>
-da_status launch_split(const Call& c, void* out, cudaStream_t stream, bool* merged) {
+da_status launch_split(const Call& c, void* out, cudaStream_t stream) {
     SplitLaunch a;
     if (!prepare_split<D, NT, ST>(c, out, a)) return DA_ERR_CUDA;
     static DeviceCache caches[3];
-    return launch_persistent(split_kernel<D, DT, NT, ST>, a, caches[a.cache_idx], stream, merged);
+    return launch_persistent(split_kernel<D, DT, NT, ST>, a, caches[a.cache_idx], stream);
 }
 
 
@@ -645,18 +702,16 @@ da_status launch_combine(const Call& c, void* out, cudaStream_t stream) {
 }
 
 template <int D, int DT>
-da_status launch_split_cols(const Call& c, void* out, cudaStream_t st, bool* merged) {
+da_status launch_split_cols(const Call& c, void* out, cudaStream_t st) {
     const bool wide = item_cols(static_cast<int64_t>(c.Hq / c.Hkv) * c.tq) > kHeadsPerCta;
-    if (wide) return launch_split<D, DT, 2, kStages>(c, out, st, merged);
-    return launch_split<D, DT, 1, kStages>(c, out, st, merged);
+    if (wide) return launch_split<D, DT, 2, kStages>(c, out, st);
+    return launch_split<D, DT, 1, kStages>(c, out, st);
 }
 
-da_status dispatch_split(const Call& c, void* out, cudaStream_t st, bool* merged = nullptr) {
+da_status dispatch_split(const Call& c, void* out, cudaStream_t st) {
     if (c.D == 128)
-        return c.dt == DA_F16 ? launch_split_cols<128, DA_F16>(c, out, st, merged)
-                              : launch_split_cols<128, DA_BF16>(c, out, st, merged);
-    return c.dt == DA_F16 ? launch_split_cols<64, DA_F16>(c, out, st, merged)
-                          : launch_split_cols<64, DA_BF16>(c, out, st, merged);
+        return c.dt == DA_F16 ? launch_split_cols<128, DA_F16>(c, out, st) : launch_split_cols<128, DA_BF16>(c, out, st);
+    return c.dt == DA_F16 ? launch_split_cols<64, DA_F16>(c, out, st) : launch_split_cols<64, DA_BF16>(c, out, st);
 }
 
 da_status dispatch_combine(const Call& c, void* out, cudaStream_t st) {
@@ -665,13 +720,11 @@ da_status dispatch_combine(const Call& c, void* out, cudaStream_t st) {
     return c.dt == DA_F16 ? launch_combine<64, DA_F16>(c, out, st) : launch_combine<64, DA_BF16>(c, out, st);
 }
 
-// Split step, then the combine step unless the split step wrote all of `out`:
-// every sequence has a single split (S = 1, or a per-sequence cap of 1), or the
-// items fit one wave and the split kernel merged the splits itself.
+// Split step, then the combine step unless every sequence has a single split
+// (S = 1, or a per-sequence cap of 1): the split step then wrote all of `out`.
 da_status run_decode(const Call& c, void* out, cudaStream_t st) {
-    bool merged = false;
-    da_status r = dispatch_split(c, out, st, &merged);
-    if (r != DA_OK || c.S == 1 || merged) return r;
+    da_status r = dispatch_split(c, out, st);
+    if (r != DA_OK || c.S == 1) return r;
     return dispatch_combine(c, out, st);
 }
 

@@ -31,11 +31,9 @@ constexpr int kPrefetchStages = 4;  // BHSD: first stages pulled into L2 while c
 constexpr int kMinBlocksPerSm = 2;
 constexpr int kItemSlots = 2;       // item descriptors the producer may run ahead
 constexpr float kLazyRescale = 8.f; // 16-column items: headroom (log2) before the running max moves
-constexpr size_t kHeaderBytes = 4096;
+constexpr size_t kHeaderBytes = 256;
 constexpr size_t kWorkCounterOff = 64;   // header: uint32 work-queue head
 constexpr size_t kDoneCounterOff = 128;  // header: uint32 count of CTAs finished
-constexpr size_t kWaveCounterOff = 256;  // header: {arrived, left} uint32 pairs, one per unit (single-wave merge)
-constexpr int kMaxWaveUnits = static_cast<int>((kHeaderBytes - kWaveCounterOff) / 8);   // 480
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
@@ -86,7 +84,6 @@ struct SplitParams {
     uint32_t* work;          // work-queue head
     uint32_t* done;          // CTAs finished
     uint16_t* out;           // [B, Hq, D]: rows of sequences with one split are written here (nullptr: none)
-    uint32_t* wave;          // single-wave merge: per-unit {arrived, left} counters (nullptr: a combine step follows)
     int B, Hq, Hkv, G, S, kv_rows, layout, chunks, no_kv, n_items;
     int split_len;           // 0: every sequence has S splits; else S_b = min(S, ceil(L_b / split_len))
     int stage_cu;            // cu_seqlens_k staged in shared memory (B small enough)
@@ -727,172 +724,6 @@ __device__ __forceinline__ void split_finish(const SplitParams& p, bool ok, uint
     }
 }
 
-// ------------------------------------------------------------ merging splits
-// Fold one split (its lse and four dims of its o) into a lane's running
-// (max, sum, weighted accumulator); the max moves up as larger lse arrive, so a
-// single pass over the splits suffices. Empty splits (lse = -inf) weigh 0.
-__device__ __forceinline__ void combine_fold(float lv, float4 ov, float& m, float& z, float4& acc) {
-    if (lv == -INFINITY) return;
-    if (lv > m) {
-        const float sc = fast_exp2((m - lv) * kLog2e);   // 0 when m is still -inf
-        acc.x *= sc;
-        acc.y *= sc;
-        acc.z *= sc;
-        acc.w *= sc;
-        z *= sc;
-        m = lv;
-    }
-    const float w = fast_exp2((lv - m) * kLog2e);
-    acc.x = fmaf(w, ov.x, acc.x);
-    acc.y = fmaf(w, ov.y, acc.y);
-    acc.z = fmaf(w, ov.z, acc.z);
-    acc.w = fmaf(w, ov.w, acc.w);
-    z += w;
-}
-
-// Merge the running states of lanes `first` apart, 2 * first apart, ... below
-// `end`: afterwards every lane of a group of end / first such lanes holds the
-// group's merged state (fixed order, deterministic).
-__device__ __forceinline__ void merge_lanes(float& m, float& z, float4& acc, int first, int end = 32) {
-    for (int off = first; off < end; off <<= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-        const float z2 = __shfl_xor_sync(0xffffffffu, z, off);
-        float4 a2;
-        a2.x = __shfl_xor_sync(0xffffffffu, acc.x, off);
-        a2.y = __shfl_xor_sync(0xffffffffu, acc.y, off);
-        a2.z = __shfl_xor_sync(0xffffffffu, acc.z, off);
-        a2.w = __shfl_xor_sync(0xffffffffu, acc.w, off);
-        const float M = fmaxf(m, m2);
-        if (M != -INFINITY) {
-            const float a = m == -INFINITY ? 0.f : fast_exp2((m - M) * kLog2e);
-            const float b = m2 == -INFINITY ? 0.f : fast_exp2((m2 - M) * kLog2e);
-            acc.x = a * acc.x + b * a2.x;
-            acc.y = a * acc.y + b * a2.y;
-            acc.z = a * acc.z + b * a2.z;
-            acc.w = a * acc.w + b * a2.w;
-            z = a * z + b * z2;
-            m = M;
-        }
-    }
-}
-
-// Four merged dims of an output row: acc / z rounded to the output dtype, or 0 when
-// every split was empty.
-template <int DT>
-__device__ __forceinline__ void store_quad(uint16_t* o, float m, float z, const float4& acc) {
-    if (m == -INFINITY) {
-        *reinterpret_cast<uint2*>(o) = make_uint2(0u, 0u);
-    } else {
-        const float inv = 1.f / z;
-        *reinterpret_cast<uint2*>(o) =
-            make_uint2(pack2<DT>(acc.x * inv, acc.y * inv), pack2<DT>(acc.z * inv, acc.w * inv));
-    }
-}
-
-__device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory"); }
-
-// consumer_bar that also returns whether `v` holds in every consumer thread
-__device__ __forceinline__ bool consumer_bar_and(bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 q, %1, 0;\n\t"
-        "bar.red.and.pred p, 1, %2, q;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(v)), "r"(kConsumerWarps * 32)
-        : "memory");
-    return r != 0;
-}
-
-// Single-wave merge. When every work item of a uniform-split call fits one wave
-// (one item per CTA, all CTAs resident together: a cooperative launch), the S CTAs
-// of a unit (sequence, KV head, column chunk) merge its splits themselves instead
-// of a combine kernel: each publishes its partial (a release add on the unit's
-// "arrived" counter after the consumer warps' writes), waits until all S have
-// arrived (bounded), then merges its own 1/S of the unit's output columns x dims
-// from the S partials in L2 (lse = ln sum_s exp(lse_s), out = sum_s exp(lse_s -
-// lse) o_s: the combine segment of the TileLang page) and writes it. The last CTA
-// to leave re-arms the two counters for the next call. Every consumer warp calls
-// it once, with ok = its pipeline finished without a time-out (the merge runs only
-// if all did); returns false if it did not run or its wait timed out
-// (DA_DEVERR_TIMEOUT is then set).
-template <int D, int DT>
-__device__ __forceinline__ bool wave_merge(const SplitParams& p, const ItemSlot& it, bool ok) {
-    __shared__ int all_arrived;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int idx = static_cast<int>(blockIdx.x);          // this CTA's only item
-    const int unit = (idx / p.chunks) / p.S * p.chunks + idx % p.chunks;
-    uint32_t* arrived = p.wave + 2 * unit;
-    uint32_t* left = arrived + 1;
-    // every consumer thread's partial writes precede the release below
-    if (!consumer_bar_and(ok)) return false;
-    if (tid == 0) {
-        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(arrived) : "memory");
-        bool ok = false;
-        const unsigned long long t0 = global_ns();
-        while (true) {
-            uint32_t v;
-            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(arrived) : "memory");
-            if (v >= static_cast<uint32_t>(p.S)) {
-                ok = true;
-                break;
-            }
-            if (global_ns() - t0 > p.wait_limit_ns) break;
-            __nanosleep(64);
-        }
-        if (!ok) flag_error(p.err, DA_DEVERR_TIMEOUT);
-        all_arrived = ok;
-    }
-    consumer_bar();   // the acquire above orders every consumer thread's reads below
-    if (!all_arrived) return false;
-    constexpr int kQuadsPerCol = D / 4;
-    const int quads = it.nh * kQuadsPerCol;
-    const int lo = quads * it.s / p.S, hi = quads * (it.s + 1) / p.S;
-    // A group of g lanes (g = S rounded up to a power of two, at most 32) merges one
-    // quad (four dims of one column), lane j of the group reading splits j, j + g,
-    // ...; a warp takes 32 / g quads at a time, the four warps interleaved.
-    int g = 1;
-    while (g < p.S && g < 32) g <<= 1;
-    const int qpw = 32 / g;                       // quads per warp and pass
-    const int gq = lane / g, gl = lane % g;
-    for (int q0 = lo + warp * qpw; q0 < hi; q0 += kConsumerWarps * qpw) {
-        const int q = q0 + gq;
-        const bool live = q < hi;
-        const int64_t qrow = column_row(p, it, live ? q / kQuadsPerCol : 0);
-        const float* l = p.lse + qrow * p.S;
-        const float* po = p.opart + qrow * p.S * D + (live ? q % kQuadsPerCol : 0) * 4;
-        float m = -INFINITY, z = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        // four splits' loads in flight per lane before any is folded
-        for (int s0 = gl; s0 < p.S; s0 += 4 * g) {
-            float lv[4];
-            float4 ov[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int s = s0 + u * g;
-                if (live && s < p.S) {
-                    lv[u] = __ldcg(l + s);
-                    ov[u] = __ldcg(reinterpret_cast<const float4*>(po + static_cast<int64_t>(s) * D));
-                } else {
-                    lv[u] = -INFINITY;
-                    ov[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) combine_fold(lv[u], ov[u], m, z, acc);
-        }
-        merge_lanes(m, z, acc, 1, g);
-        if (live && gl == 0) store_quad<DT>(p.out + qrow * D + (q % kQuadsPerCol) * 4, m, z, acc);
-    }
-    // re-arm: every CTA of the unit has passed its wait once all S have left
-    if (tid == 0 && atomicAdd(left, 1u) == static_cast<uint32_t>(p.S) - 1) {
-        *arrived = 0u;
-        *left = 0u;
-    }
-    return true;
-}
-
 // ------------------------------------------------------------ host side
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -1078,7 +909,6 @@ inline bool prepare_split(const Call& c, void* out, SplitLaunch& a) {
     p.work = reinterpret_cast<uint32_t*>(wsb + kWorkCounterOff);
     p.done = reinterpret_cast<uint32_t*>(wsb + kDoneCounterOff);
     p.out = static_cast<uint16_t*>(out);
-    p.wave = nullptr;
     p.lse = reinterpret_cast<float*>(wsb + kHeaderBytes);
     p.opart = reinterpret_cast<float*>(wsb + kHeaderBytes +
                                        round_up(static_cast<size_t>(c.B) * c.tq * c.Hq * c.S * 4, 256));
@@ -1104,39 +934,18 @@ inline bool prepare_split(const Call& c, void* out, SplitLaunch& a) {
 }
 
 // Launch a persistent split kernel: as many CTAs as fit on the device at once,
-// at most one per work item, with programmatic dependent launch. With
-// `merged` non-null (a call that produces `out` from several uniform splits)
-// and every item fitting one wave, the kernel is launched cooperatively (all
-// its CTAs resident together) and merges the splits itself (wave_merge); then
-// *merged is set and no combine step is needed.
+// at most one per work item, with programmatic dependent launch.
 template <class K>
-inline da_status launch_persistent(K kern, const SplitLaunch& a, DeviceCache& cache, cudaStream_t stream,
-                                   bool* merged = nullptr) {
+inline da_status launch_persistent(K kern, const SplitLaunch& a, DeviceCache& cache, cudaStream_t stream) {
     int grid = 0;
     if (persistent_grid(kern, kThreads, a.smem, cache, &grid) != cudaSuccess) return DA_ERR_CUDA;
+    grid = std::min(grid, a.p.n_items);
+    cudaLaunchAttribute attrs[1] = {pdl_attr()};
     cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = a.smem;
     cfg.stream = stream;
-    const int units = a.p.n_items / a.p.S;
-    if (merged != nullptr && a.p.out != nullptr && a.p.S > 1 && a.p.split_len == 0 && a.p.n_items <= grid &&
-        units <= kMaxWaveUnits) {
-        SplitParams p = a.p;
-        p.wave = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(a.p.err) + kWaveCounterOff);
-        cudaLaunchAttribute coop;
-        coop.id = cudaLaunchAttributeCooperative;
-        coop.val.cooperative = 1;
-        cfg.gridDim = dim3(a.p.n_items);
-        cfg.attrs = &coop;
-        cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, kern, a.mk, a.mv, a.mk16, a.mv16, p) == cudaSuccess) {
-            *merged = true;
-            return DA_OK;
-        }
-        (void)cudaGetLastError();   // a refused cooperative launch falls back to the combine step
-    }
-    cudaLaunchAttribute attrs[1] = {pdl_attr()};
-    cfg.gridDim = dim3(std::min(grid, a.p.n_items));
     cfg.attrs = attrs;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, a.mk, a.mv, a.mk16, a.mv16, a.p) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
