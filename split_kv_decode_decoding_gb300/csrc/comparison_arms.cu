@@ -112,7 +112,7 @@ split_kernel_fma(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     // per consumer warp: softmax weights [16 keys][8 columns] and 8 rescale factors
     float* fma_p = reinterpret_cast<float*>(sl.extra);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    split_setup<NT, kStages>(sl, p, &tmK, &tmV, &tmK16, &tmV16);
+    split_setup<D, NT, kStages>(sl, p, &tmK, &tmV, &tmK16, &tmV16);
     if (warp == kConsumerWarps) {
         split_producer<D, NT, kStages>(sl, p, &tmK, &tmV, &tmK16, &tmV16);
         return;
@@ -994,6 +994,7 @@ da_status launch_split_tc(const Call& c, void* out, cudaStream_t stream) {
     p.n_items = c.B * c.Hkv * p.chunks * c.S;   // per-sequence mode: an upper bound (the kernel counts)
     p.split_len = c.split_len;
     p.stage_cu = c.B <= kMaxStagedBatch;
+    p.sorted = 0;   // this kernel's producer hands out items in index order
     p.scale_log2 = c.scale * kLog2e;
     p.wait_limit_ns = kWaitLimitNs;
 

@@ -74,7 +74,7 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
     const uint32_t ring = sl.ring, qbuf = sl.qbuf, full0 = sl.full0, empty0 = sl.empty0;
     const uint32_t ifull0 = sl.ifull0, iempty0 = sl.iempty0, mfull = sl.mfull, mdone = sl.mdone;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    split_setup<NT, ST>(sl, p, &tmK, &tmV, &tmK16, &tmV16);
+    split_setup<D, NT, ST>(sl, p, &tmK, &tmV, &tmK16, &tmV16);
     if (warp == kConsumerWarps) {
         split_producer<D, NT, ST>(sl, p, &tmK, &tmV, &tmK16, &tmV16);
         return;

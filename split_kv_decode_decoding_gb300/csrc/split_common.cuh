@@ -39,6 +39,16 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr int kMaxStagedBatch = 1024;                          // B up to which cu_seqlens_k is staged in smem
 constexpr int kStagedBytes = ((kMaxStagedBatch + 1) * 4 + 15) / 16 * 16;   // one [B + 1] int32 array
+// Uniform splits over a varlen batch of at most kMaxSortedBatch sequences: the work
+// queue hands out the sequences longest first, so that the last items to start are
+// the short ones. The order (perm[rank] = sequence) lives in the staged
+// cu_seqlens_k area, past the B + 1 entries it uses.
+constexpr int kMaxSortedBatch = 128;
+constexpr int kLenOff = 384;    // int32 entries into the staged cu_seqlens_k area: lengths [B]
+constexpr int kPermOff = 512;   // and the order [B] (the area holds 1025 + 3 entries)
+static_assert(kLenOff >= kMaxSortedBatch + 1 && kPermOff >= kLenOff + kMaxSortedBatch &&
+                  kPermOff + kMaxSortedBatch <= kStagedBytes / 4,
+              "the sorted order fits the staged cu_seqlens_k area past its entries");
 
 struct ItemSlot {          // one work item, as the producer decoded it
     int32_t b, kvh, h0, nh;            // h0: first query head of the KV head's group; nh columns
@@ -87,6 +97,7 @@ struct SplitParams {
     int B, Hq, Hkv, G, S, kv_rows, layout, chunks, no_kv, n_items;
     int split_len;           // 0: every sequence has S splits; else S_b = min(S, ceil(L_b / split_len))
     int stage_cu;            // cu_seqlens_k staged in shared memory (B small enough)
+    int sorted;              // the producer hands out sequences longest first (see kMaxSortedBatch)
     int tq;                  // query tokens per sequence; columns per KV head = G * tq
     float scale_log2;        // scale * log2(e)
     unsigned long long wait_limit_ns;
@@ -334,6 +345,12 @@ __device__ __forceinline__ int seq_splits(int64_t L, int split_len, int max_spli
 // With per-sequence split counts, `prefix` holds the running sum of S_b
 // (prefix[b] splits before sequence b) and the sequence is found by binary
 // search.
+// Whether the work queue hands out sequences longest first (see kMaxSortedBatch):
+// set by the host for launches whose producer builds the order.
+__device__ __forceinline__ bool longest_first(const SplitParams& p, const int32_t* cus) {
+    return p.sorted != 0 && cus != nullptr;
+}
+
 __device__ __forceinline__ ItemSlot decode_item_cols(const SplitParams& p, int idx, const int32_t* cus,
                                                      const int32_t* prefix, int kCols) {
     ItemSlot it;
@@ -347,6 +364,7 @@ __device__ __forceinline__ ItemSlot decode_item_cols(const SplitParams& p, int i
         r /= p.S;
         it.kvh = r % p.Hkv;
         it.b = r / p.Hkv;
+        if (longest_first(p, cus)) it.b = cus[kPermOff + it.b];
         Sb = p.S;
     } else {
         int lo = 0, hi = p.B - 1;   // last b with prefix[b] * hc_count <= idx
@@ -436,7 +454,7 @@ __device__ __forceinline__ SplitLayout split_layout(uint8_t* smem_raw, const Spl
 
 // Barrier set-up and tensor-map prefetch; everything before the grid-dependency
 // wait overlaps the previous kernel in the stream.
-template <int NT, int ST>
+template <int D, int NT, int ST>
 __device__ __forceinline__ void split_setup(const SplitLayout& sl, const SplitParams& p, const CUtensorMap* tmK,
                                             const CUtensorMap* tmV, const CUtensorMap* tmK16,
                                             const CUtensorMap* tmV16) {
@@ -464,6 +482,47 @@ __device__ __forceinline__ void split_setup(const SplitLayout& sl, const SplitPa
     // From here on this grid touches global memory: wait for the previous kernel.
     grid_dependency_wait();
     if (threadIdx.x == 0) grid_dependents_launch();
+    if (warp == kConsumerWarps && lane == 0 && p.layout == DA_LAYOUT_BHSD && p.no_kv == 0 && p.split_len == 0 &&
+        static_cast<int>(blockIdx.x) < p.n_items) {
+        // This CTA's first item is its own index. When that is a sequence's first
+        // split, its keys start at position 0 of its slab whatever the length:
+        // start pulling its first stages into L2 while cu_seqlens_k is read.
+        const int r = static_cast<int>(blockIdx.x) / p.chunks;   // (b * Hkv + kvh) * S + s
+        if (r % p.S == 0) {
+            const int slab = r / p.S;
+            for (int t = 0; t < kPrefetchStages; ++t)
+                for (int hf = 0; hf < D / 64; ++hf) {
+                    tma_prefetch_3d(tmK, hf * 64, t * kStageKeys, slab);
+                    tma_prefetch_3d(tmV, hf * 64, t * kStageKeys, slab);
+                }
+        }
+    }
+    if (sl.cus != nullptr) {
+        // one coalesced read of cu_seqlens_k per CTA; every item is then decoded from shared memory
+        for (int i = threadIdx.x; i <= p.B; i += kThreads) sl.cus[i] = ld_cg_s32(p.cu + i);
+        __syncthreads();
+        if (longest_first(p, sl.cus)) {
+            // the order in which the work queue hands out sequences, longest first (ties
+            // by index): thread t ranks sequence t; an even batch keeps the index order
+            const int t = threadIdx.x;
+            int32_t* len = sl.cus + kLenOff;
+            const int Lt = t < p.B ? sl.cus[t + 1] - sl.cus[t] : 0;
+            if (t < p.B) len[t] = Lt;
+            const bool uneven = __syncthreads_or(t < p.B && Lt != sl.cus[1] - sl.cus[0]);
+            if (t < p.B) {
+                int rank = t;
+                if (uneven) {
+                    rank = 0;
+                    for (int b2 = 0; b2 < p.B; ++b2) {
+                        const int l2 = len[b2];
+                        rank += (l2 > Lt) || (l2 == Lt && b2 < t);
+                    }
+                }
+                sl.cus[kPermOff + rank] = t;
+            }
+            __syncthreads();
+        }
+    }
 }
 
 // The producer warp: one lane takes items from the work queue, publishes each
@@ -487,26 +546,6 @@ __device__ __forceinline__ void split_producer(const SplitLayout& sl, const Spli
     const uint32_t ifull0 = sl.ifull0, iempty0 = sl.iempty0;
     // ---------------- producer: one lane takes items and issues every copy
     int n_items = p.n_items;
-    if (lane == 0 && p.layout == DA_LAYOUT_BHSD && p.no_kv == 0 && p.split_len == 0 &&
-        static_cast<int>(blockIdx.x) < n_items) {
-        // This CTA's first item is its own index. When that is a sequence's first
-        // split, its keys start at position 0 of its slab whatever the length:
-        // start pulling its first stages into L2 while cu_seqlens_k is read.
-        const int r = static_cast<int>(blockIdx.x) / p.chunks;   // (b * Hkv + kvh) * S + s
-        if (r % p.S == 0) {
-            const int slab = r / p.S;
-            for (int t = 0; t < kPrefetchStages; ++t)
-                for (int hf = 0; hf < Sh::kHalves; ++hf) {
-                    tma_prefetch_3d(&tmK, hf * 64, t * kStageKeys, slab);
-                    tma_prefetch_3d(&tmV, hf * 64, t * kStageKeys, slab);
-                }
-        }
-    }
-    if (cus != nullptr) {
-        // one coalesced read of cu_seqlens_k per CTA; every item is then decoded from shared memory
-        for (int i = lane; i <= p.B; i += 32) cus[i] = ld_cg_s32(p.cu + i);
-        __syncwarp();
-    }
     if (p.split_len != 0) {
         // per-sequence split counts: the whole warp builds prefix[] = running sum of S_b
         int carry = 0;
@@ -925,6 +964,7 @@ inline bool prepare_split(const Call& c, void* out, SplitLaunch& a) {
     p.n_items = c.B * c.Hkv * p.chunks * c.S;   // per-sequence mode: an upper bound (the kernel counts)
     p.split_len = c.split_len;
     p.stage_cu = c.B <= kMaxStagedBatch;
+    p.sorted = c.split_len == 0 && c.lay == DA_LAYOUT_VARLEN && c.B > 1 && c.B <= kMaxSortedBatch && p.stage_cu;
     p.scale_log2 = c.scale * kLog2e;
     p.wait_limit_ns = kWaitLimitNs;
     const bool var = c.split_len != 0;
