@@ -126,7 +126,11 @@ da_status decode_attn_splitkv_workspace_init(void* workspace, size_t workspace_b
  *     raised until the longest sequence's splits are at most twice one CTA's
  *     share of a lower bound of the total keys (max_kv + (B-1) * min_kv); with
  *     16-column items (G > 8, or G * T_q > 8 when Hq is passed as Hq * T_q for
- *     several query tokens) four items per SM and four shares.
+ *     several query tokens) four items per SM and four shares. A batch of at
+ *     most 128 sequences in which no sequence holds half of that lower bound is
+ *     handed out longest first by the split step and gets fewer, longer
+ *     splits: six items per SM and four shares (16-column items: three and
+ *     eight).
  * No split is ever empty (num_splits <= min_kv; the TileLang page's scheduling
  * constraint, split kernel docstring). sm_count 0 means: query the current
  * device. Returns a value in [1, DA_MAX_SPLITS]; 1 when min_kv <= 0 or an

@@ -785,14 +785,20 @@ int decode_attn_splitkv_num_splits(int B, int Hq, int Hkv, int D, int min_kv, in
         // (16-column items carry twice the work per key and a two-round merge:
         // half as many of them, with longer splits, measured best)
         const bool wide = item_cols(Hq / Hkv) > kHeadsPerCta;
-        const int64_t per_sm = wide ? 4 : 8;
-        const double shares = wide ? 4.0 : 2.0;
+        const double total = static_cast<double>(max_kv) + static_cast<double>(B - 1) * min_kv;
+        // A batch of up to kMaxSortedBatch sequences is handed out longest first,
+        // so its short items come last and even out the end by themselves: fewer,
+        // longer splits measure best (six items per SM, splits up to four CTA
+        // shares), unless one sequence holds most of the keys and its splits are
+        // the critical path.
+        const bool sorted = B <= kMaxSortedBatch && 2.0 * max_kv <= total;
+        const int64_t per_sm = sorted ? (wide ? 3 : 6) : (wide ? 4 : 8);
+        const double shares = sorted ? (wide ? 8.0 : 4.0) : (wide ? 4.0 : 2.0);
         S = (per_sm * static_cast<int64_t>(sm_count) + units - 1) / units;
         S = std::min<int64_t>(S, std::max<int64_t>(1, min_kv / 64));
-        // ... and the longest sequence's splits at most about twice (wide items:
-        // four times) one CTA's share of the keys (the share taken from a lower
-        // bound of the total), so that no single split outlasts the rest of the batch.
-        const double total = static_cast<double>(max_kv) + static_cast<double>(B - 1) * min_kv;
+        // ... and the longest sequence's splits at most about `shares` times one
+        // CTA's share of the keys (the share taken from a lower bound of the
+        // total), so that no single split outlasts the rest of the batch.
         const double share = total * Hkv * chunks / static_cast<double>(slots);
         S = std::max<int64_t>(S, static_cast<int64_t>(std::ceil(max_kv / (shares * share))));
     } else if (5 * units >= 4 * static_cast<int64_t>(sm_count)) {

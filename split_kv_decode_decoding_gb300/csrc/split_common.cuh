@@ -513,6 +513,7 @@ __device__ __forceinline__ void split_setup(const SplitLayout& sl, const SplitPa
                 int rank = t;
                 if (uneven) {
                     rank = 0;
+#pragma unroll 8
                     for (int b2 = 0; b2 < p.B; ++b2) {
                         const int l2 = len[b2];
                         rank += (l2 > Lt) || (l2 == Lt && b2 < t);
