@@ -14,6 +14,10 @@
 
 using namespace da_impl;
 
+namespace {
+constexpr int kMaxSortedBatchModel = 128;   // batches the split step hands out longest first
+}
+
 extern "C" {
 
 // A GB300 restatement of the lecture page's decode time model
@@ -51,25 +55,36 @@ double decode_attn_splitkv_model_us(const int32_t* kv_lens, int B, int Hq, int H
     const double t0 = m[0], t_item = m[1], bw = m[3], t_comb = m[4], bw_comb = m[5], kappa = m[6];
     // one CTA's streaming cap: 16-column items carry twice the products per key
     const bool wide = item_cols(static_cast<int64_t>(Hq / Hkv) * T_q) > kHeadsPerCta;
-    const double r_cta = wide ? m[7] : m[2];
+    const double r_cta = (wide ? m[7] : m[2]) / static_cast<double>(item_chunks(static_cast<int64_t>(Hq / Hkv) * T_q));
     if (!(r_cta > 0) || !(bw > 0) || !(bw_comb > 0) || !(t_item >= 0) || !(kappa >= 0)) return -1.0;
     const int S = num_splits;
     const int chunks = static_cast<int>(item_chunks(static_cast<int64_t>(Hq / Hkv) * T_q));
     const int slots = sm_count * (D == 128 ? 2 : 4);
     const double key_bytes = 4.0 * D;   // K and V rows of one key and KV head
     // the work items in queue order: the bytes each streams (later chunks of a
-    // split re-read its keys from L2 and are not counted in W)
+    // split re-read its keys from L2 and are not counted in W). The split step
+    // hands out the sequences of a batch of at most 128 longest first (a varlen
+    // batch, which is what the model assumes), ties in index order.
+    std::vector<int> order(static_cast<size_t>(B));
+    for (int b = 0; b < B; ++b) order[b] = b;
+    if (B > 1 && B <= kMaxSortedBatchModel)
+        std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
+            return std::max(kv_lens[x], 0) > std::max(kv_lens[y], 0);
+        });
     std::vector<double> items;
     double W = 0.0, biggest = 0.0;
-    for (int b = 0; b < B; ++b) {
+    for (int b : order) {
         const int64_t L = kv_lens[b] < 0 ? 0 : kv_lens[b];
         for (int kvh = 0; kvh < Hkv; ++kvh)
             for (int s = 0; s < S; ++s) {
                 const int64_t n = L * (s + 1) / S - L * s / S;
                 const double bytes = static_cast<double>((n + kBoxKeys - 1) / kBoxKeys * kBoxKeys) * key_bytes;
-                biggest = std::max(biggest, bytes);
+                biggest = std::max(biggest, bytes / chunks);
                 W += bytes;
-                for (int c = 0; c < chunks; ++c) items.push_back(bytes);
+                // the `chunks` items of a split run side by side and read its keys
+                // once from HBM between them (the rest from L2): each item is charged
+                // its share of the HBM bytes, at its share of one CTA's rate
+                for (int c = 0; c < chunks; ++c) items.push_back(bytes / chunks);
             }
     }
     // Processor sharing: every CTA that is streaming gets min(r_cta, bw / streaming)

@@ -76,6 +76,17 @@ def test_parity_cases(case):
     check_full(p, S)
 
 
+@pytest.mark.parametrize("B", [128, 129], ids=["sorted_128", "index_order_129"])
+def test_ragged_batch_at_the_longest_first_limit(B):
+    """Uniform splits over a ragged varlen batch: up to 128 sequences the split step hands them
+    out longest first (ties by index), from 129 in index order. Lengths from a small set, so
+    that many sequences tie, and a few empty ones; every element against the oracle."""
+    rng = np.random.default_rng(B)
+    lens = [int(x) for x in rng.choice([0, 1, 33, 64, 65, 200, 513], size=B)]
+    p = custom(f"rag{B}", B, 8, 2, 64, lens, "bf16", LAYOUT_VARLEN, 3, seed=B)
+    check_full(p, 3)
+
+
 def test_varlen_rows_past_the_last_sequence_are_ignored():
     p = custom("tailnan", 2, 8, 2, 128, [70, 45], "f16", LAYOUT_VARLEN, 3, seed=5, data=False)
     from synth.workloads import materialize
