@@ -388,12 +388,16 @@ da_status decode_attn_splitkv_noalloc_get_error(uint32_t* device_error_bits, voi
  *   T = t0 + makespan + kappa * B_max / (bw / min(n_items, R))
  *         + [S > 1] * (t_comb + W_ws / bw_comb)
  *
- * makespan: a processor-sharing run of the n_items work items, in queue order,
- * over R = (2 at D = 128, 4 at D = 64) * sm_count persistent CTAs; before each
- * item a CTA spends t_item, then streams the item's K/V bytes (its keys rounded
- * up to 16, times 4*D) at min(r_cta, bw / number of CTAs streaming). B_max: the
- * largest item's bytes (kappa charges the last item for unequal CTA rates);
- * W_ws = B*T_q*Hq*S*(D+1)*4 workspace bytes combined.
+ * makespan: a processor-sharing run of the n_items work items, in queue order
+ * (the sequences of a batch of 2 to 128 longest first, ties by index, as the
+ * split step hands out a ragged varlen batch), over R = (2 at D = 128, 4 at
+ * D = 64) * sm_count persistent CTAs; before each item a CTA spends t_item,
+ * then streams the item's K/V bytes (its keys rounded up to 16, times 4*D) at
+ * min(r_cta, bw / number of CTAs streaming). When a KV head's columns take c
+ * chunks, each chunk's item is charged 1/c of the bytes at 1/c of the rate
+ * (the chunks of a split read its keys once from HBM between them). B_max: the
+ * largest item's charged bytes (kappa charges the last item for unequal CTA
+ * rates); W_ws = B*T_q*Hq*S*(D+1)*4 workspace bytes combined.
  *   kv_lens   host, int32 [B] sequence lengths (negative counts as 0)
  *   params    host, double[8] {t0 us, t_item us, r_cta B/us, bw B/us, t_comb us,
  *             bw_comb B/us, kappa, r_cta2 B/us}, or NULL for the built-in GB300

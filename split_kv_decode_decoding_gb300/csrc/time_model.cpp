@@ -31,20 +31,22 @@ extern "C" {
 // at min(r_cta, bw / streaming CTAs), r_cta being one CTA's rate for 8-column
 // items and r_cta2 for 16-column ones; kappa charges the last item for the
 // CTAs' unequal rates, and W_ws is the workspace bytes the combine reads.
-// Fitted (least squares in log time) on one GB300 to the 310 calls, of 546
+// Fitted (least squares in log time) on one GB300 to the 305 calls, of 546
 // measured (17 single-token workloads of the CodeLlama, Llama, Qwen and MHA
 // shapes and 9 of them with 2 or 4 new tokens x split counts 1 to 256, L2
 // flushed, CUDA-event median per call), that lie within 30 % of their
-// workload's fastest split count: median error 2.9 %, 90th percentile 10.8 %.
+// workload's fastest split count: median error 2.8 %, 90th percentile 10.1 %.
+// The fit puts t_item at zero: the ring, which keeps filling across items,
+// hides the per-item work.
 static const double kModelGb300[8] = {
-    /* t0 us       */ 12.24,
-    /* t_item us   */ 0.1241,
-    /* r_cta B/us  */ 76340,
-    /* bw B/us     */ 7.592e+06,
-    /* t_comb us   */ 2.462,
-    /* bw_comb     */ 8.561e+05,
-    /* kappa       */ 0.05135,
-    /* r_cta2 B/us */ 52610};
+    /* t0 us       */ 12.12,
+    /* t_item us   */ 0.0,
+    /* r_cta B/us  */ 76030,
+    /* bw B/us     */ 7.727e+06,
+    /* t_comb us   */ 3.563,
+    /* bw_comb     */ 6.607e+05,
+    /* kappa       */ 0.05334,
+    /* r_cta2 B/us */ 46900};
 
 double decode_attn_splitkv_model_us(const int32_t* kv_lens, int B, int Hq, int Hkv, int D, int T_q, int num_splits,
                                     int sm_count, const double* params) {
@@ -61,8 +63,7 @@ double decode_attn_splitkv_model_us(const int32_t* kv_lens, int B, int Hq, int H
     const int chunks = static_cast<int>(item_chunks(static_cast<int64_t>(Hq / Hkv) * T_q));
     const int slots = sm_count * (D == 128 ? 2 : 4);
     const double key_bytes = 4.0 * D;   // K and V rows of one key and KV head
-    // the work items in queue order: the bytes each streams (later chunks of a
-    // split re-read its keys from L2 and are not counted in W). The split step
+    // the work items in queue order and the bytes each streams. The split step
     // hands out the sequences of a batch of at most 128 longest first (a varlen
     // batch, which is what the model assumes), ties in index order.
     std::vector<int> order(static_cast<size_t>(B));
@@ -72,7 +73,7 @@ double decode_attn_splitkv_model_us(const int32_t* kv_lens, int B, int Hq, int H
             return std::max(kv_lens[x], 0) > std::max(kv_lens[y], 0);
         });
     std::vector<double> items;
-    double W = 0.0, biggest = 0.0;
+    double biggest = 0.0;
     for (int b : order) {
         const int64_t L = kv_lens[b] < 0 ? 0 : kv_lens[b];
         for (int kvh = 0; kvh < Hkv; ++kvh)
@@ -80,7 +81,6 @@ double decode_attn_splitkv_model_us(const int32_t* kv_lens, int B, int Hq, int H
                 const int64_t n = L * (s + 1) / S - L * s / S;
                 const double bytes = static_cast<double>((n + kBoxKeys - 1) / kBoxKeys * kBoxKeys) * key_bytes;
                 biggest = std::max(biggest, bytes / chunks);
-                W += bytes;
                 // the `chunks` items of a split run side by side and read its keys
                 // once from HBM between them (the rest from L2): each item is charged
                 // its share of the HBM bytes, at its share of one CTA's rate
@@ -126,7 +126,6 @@ double decode_attn_splitkv_model_us(const int32_t* kv_lens, int B, int Hq, int H
     const double fair = bw / static_cast<double>(std::max<size_t>(1, std::min<size_t>(items.size(), slots)));
     double t = t0 + makespan + kappa * biggest / fair;
     if (S > 1) t += t_comb + static_cast<double>(B) * T_q * Hq * S * (D + 1) * 4.0 / bw_comb;
-    (void)W;
     return t;
 }
 
