@@ -66,6 +66,8 @@ def load_library(path: str):
     lib.oracle_attention_rows_mq.restype = ctypes.c_int
     lib.oracle_split_partials_mq.argtypes = _PROBLEM_ARGS + [_I32, _I32, _P, _P, ctypes.c_int]
     lib.oracle_split_partials_mq.restype = ctypes.c_int
+    lib.oracle_split_partials_var_mq.argtypes = _PROBLEM_ARGS + [_I32, _I32, _I32, _P, _P, _P, ctypes.c_int]
+    lib.oracle_split_partials_var_mq.restype = ctypes.c_int
     lib.oracle_merge.argtypes = [_P, _P, _I64, _I32, _I32, _P, _P]
     lib.oracle_merge.restype = ctypes.c_int
     lib.oracle_weights.argtypes = _PROBLEM_ARGS + [_I32, _I32, _P]
@@ -186,6 +188,19 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle_attention_rows_mq: inconsistent problem")
         return out, lse
+
+    def split_partials_var_mq(self, p, tq: int, split_len: int, max_splits: int, nthreads: int = 0):
+        """Per-sequence split counts with tq tokens: (o_part[B,tq,Hq,max_splits,D],
+        lse_part[B,tq,Hq,max_splits], S_b[B])."""
+        keep, args = self._args(p)
+        o = np.empty((p.B, tq, p.Hq, max_splits, p.D), dtype=np.float64)
+        lse = np.empty((p.B, tq, p.Hq, max_splits), dtype=np.float64)
+        sc = np.empty(p.B, dtype=np.int32)
+        rc = self.lib.oracle_split_partials_var_mq(*args, tq, split_len, max_splits, o.ctypes.data,
+                                                   lse.ctypes.data, sc.ctypes.data, _threads(nthreads))
+        if rc != 0:
+            raise ValueError("oracle_split_partials_var_mq: inconsistent problem")
+        return o, lse, sc
 
     def split_partials_mq(self, p, tq: int, S: int, nthreads: int = 0):
         """(o_part[B,tq,Hq,S,D], lse_part[B,tq,Hq,S])."""

@@ -293,6 +293,35 @@ int oracle_split_partials(const void* q, const void* k, const void* v, const int
 
 // Per-sequence split counts: sequence b is cut into
 //     S_b = 1 if L_b = 0, else min(max_splits, ceil(L_b / split_len))
+// Per-sequence split counts with tq query tokens per sequence (causal within
+// them, as in oracle_split_partials_mq; oracle_split_partials_var below is tq = 1): o_part[B, tq, Hq, max_splits, D], lse_part[B, tq,
+// Hq, max_splits]; a split holding no key that a token may see is empty for it.
+int oracle_split_partials_var_mq(const void* q, const void* k, const void* v, const int32_t* cu, int32_t B,
+                                 int32_t Hq, int32_t Hkv, int32_t D, int64_t kv_rows, int32_t dtype,
+                                 int32_t layout, double scale, int32_t tq, int32_t split_len,
+                                 int32_t max_splits, double* o_part, double* lse_part, int32_t* s_count,
+                                 int nthreads) {
+    Problem p = make(q, k, v, cu, B, Hq, Hkv, D, kv_rows, dtype, layout, scale);
+    if (!valid(p) || tq < 1 || split_len < 1 || max_splits < 1) return -1;
+    p.tq = tq;
+    for (int b = 0; b < B; ++b) {
+        int64_t L = seq_len(p, b);
+        int64_t sb = L == 0 ? 1 : (L + split_len - 1) / split_len;
+        s_count[b] = (int32_t)(sb < max_splits ? sb : max_splits);
+    }
+    parallel_rows((int64_t)B * tq * Hq, nthreads, [&](int64_t r) {
+        int h = (int)(r % Hq), t = (int)((r / Hq) % tq), b = (int)(r / ((int64_t)Hq * tq));
+        double* o = o_part + r * max_splits * D;
+        double* l = lse_part + r * max_splits;
+        split_row(p, b, t, h, s_count[b], o, l);
+        for (int sp = s_count[b]; sp < max_splits; ++sp) {
+            l[sp] = kNegInf;
+            for (int d = 0; d < D; ++d) o[(int64_t)sp * D + d] = 0.0;
+        }
+    });
+    return 0;
+}
+
 // proportional splits (the same floor rule as above with S = S_b), so that long
 // sequences get more splits than short ones. o_part[B, Hq, max_splits, D] and
 // lse_part[B, Hq, max_splits]; entries s >= S_b hold lse = -inf, o = 0.
@@ -301,24 +330,8 @@ int oracle_split_partials_var(const void* q, const void* k, const void* v, const
                               int32_t Hq, int32_t Hkv, int32_t D, int64_t kv_rows, int32_t dtype,
                               int32_t layout, double scale, int32_t split_len, int32_t max_splits,
                               double* o_part, double* lse_part, int32_t* s_count, int nthreads) {
-    Problem p = make(q, k, v, cu, B, Hq, Hkv, D, kv_rows, dtype, layout, scale);
-    if (!valid(p) || split_len < 1 || max_splits < 1) return -1;
-    for (int b = 0; b < B; ++b) {
-        int64_t L = seq_len(p, b);
-        int64_t sb = L == 0 ? 1 : (L + split_len - 1) / split_len;
-        s_count[b] = (int32_t)(sb < max_splits ? sb : max_splits);
-    }
-    parallel_rows((int64_t)B * Hq, nthreads, [&](int64_t r) {
-        int b = (int)(r / Hq), h = (int)(r % Hq);
-        double* o = o_part + r * max_splits * D;
-        double* l = lse_part + r * max_splits;
-        split_row(p, b, 0, h, s_count[b], o, l);
-        for (int sp = s_count[b]; sp < max_splits; ++sp) {
-            l[sp] = kNegInf;
-            for (int d = 0; d < D; ++d) o[(int64_t)sp * D + d] = 0.0;
-        }
-    });
-    return 0;
+    return oracle_split_partials_var_mq(q, k, v, cu, B, Hq, Hkv, D, kv_rows, dtype, layout, scale, 1, split_len,
+                                        max_splits, o_part, lse_part, s_count, nthreads);
 }
 
 // Several query tokens per sequence: out[B, tq, Hq, D], lse[B, tq, Hq].

@@ -509,6 +509,48 @@ def pin_mq_library_cross_check(o):
                 assert (out[b, t, h] - ref.numpy()).__abs__().max() <= 1e-12
 
 
+def pin_mq_varsplit_merge_invariance(o):
+    """Several tokens with per-sequence split counts merge back to the causal unsplit result
+    (ragged batch with an empty sequence and sequences shorter than the token count, GQA,
+    both layouts); S_b follows its closed form and the splits past S_b are empty."""
+    for layout in (LAYOUT_VARLEN, LAYOUT_BHSD):
+        lens = [300, 2, 0, 77, 1000]
+        tq = 3
+        p = custom("vsm", 5, 8, 2, 64, lens, "f16", layout=layout, seed=21, tq=tq,
+                   kv_rows=1024 if layout == LAYOUT_BHSD else 0)
+        ref, ref_lse = o.attention_mq(p, tq)
+        for n, m in ((16, 64), (100, 4), (64, 1), (7, 200)):
+            op, lp, sc = o.split_partials_var_mq(p, tq, n, m)
+            out, lse = o.merge(op.reshape(-1, m, p.D), lp.reshape(-1, m))
+            out = out.reshape(ref.shape)
+            lse = lse.reshape(ref_lse.shape)
+            assert np.abs(out - ref).max() <= 1e-12, (layout, n, m)
+            fin = np.isfinite(ref_lse)
+            assert np.array_equal(fin, np.isfinite(lse))
+            assert np.abs(lse[fin] - ref_lse[fin]).max() <= 1e-12
+            for b, L in enumerate(lens):
+                assert sc[b] == (1 if L == 0 else min(m, -(-L // n)))
+                assert np.isneginf(lp[b, :, :, sc[b]:]).all() and not op[b, :, :, sc[b]:].any()
+
+
+def pin_mq_varsplit_uniform_counts(o):
+    """When every sequence gets the same S_b = S, the per-sequence partials are the uniform
+    ones of split_partials_mq, entry for entry (the same bounds floor(L*s/S))."""
+    lens = [130, 150, 161, 145]
+    tq = 4
+    p = custom("vsu", 4, 6, 3, 64, lens, "bf16", seed=22, tq=tq)
+    op, lp, sc = o.split_partials_var_mq(p, tq, 41, 8)      # ceil(L / 41) = 4 for every L here
+    assert (sc == 4).all()
+    ou, lu = o.split_partials_mq(p, tq, 4)
+    assert np.array_equal(op[:, :, :, :4], ou) and np.array_equal(lp[:, :, :, :4], lu)
+    assert np.isneginf(lp[:, :, :, 4:]).all()
+    # tq = 1 is the single-token per-sequence function
+    p1 = custom("vs1", 3, 8, 2, 64, [9, 100, 1], "f16", seed=23)
+    a, la, sa = o.split_partials_var(p1, 16, 8)
+    b, lb, sb = o.split_partials_var_mq(p1, 1, 16, 8)
+    assert np.array_equal(a, b[:, 0]) and np.array_equal(la, lb[:, 0]) and np.array_equal(sa, sb)
+
+
 ALL_PINS = [
     pin_f16_decoder, pin_bf16_decoder, pin_split_bounds_golden, pin_split_bounds_partition,
     pin_split_invariance, pin_weights_sum_to_one, pin_single_key, pin_single_key_lse,
@@ -519,4 +561,5 @@ ALL_PINS = [
     pin_split_counts_golden, pin_varsplit_merge_invariance,
     pin_mq_causal_counts_golden, pin_mq_tq1_equals_single, pin_mq_token_equals_truncated_single,
     pin_mq_split_invariance, pin_mq_library_cross_check,
+    pin_mq_varsplit_merge_invariance, pin_mq_varsplit_uniform_counts,
 ]

@@ -46,6 +46,11 @@ MUTANTS = {
                               "attend_row(p, rows_b[i], 0, rows_h[i], out + i * D, lse + i);"),
     "rows_mq_token_head_swapped": ("attend_row(p, rows_b[i], rows_t[i], rows_h[i], out + i * D, lse + i);",
                                    "attend_row(p, rows_b[i], rows_h[i], rows_t[i], out + i * D, lse + i);"),
+    # per-sequence split counts with several tokens: the token index dropped from the split
+    # step's row, or the sequence's count taken from its neighbour
+    "var_mq_token_dropped": ("split_row(p, b, t, h, s_count[b], o, l);", "split_row(p, b, 0, h, s_count[b], o, l);"),
+    "var_mq_count_of_neighbour": ("split_row(p, b, t, h, s_count[b], o, l);",
+                                  "split_row(p, b, t, h, s_count[(b + 1) % B], o, l);"),
     "merge_skips_last_split": ("for (int s = 0; s < S; ++s) {\n            if (ls[s] == kNegInf) continue;",
                                "for (int s = 0; s + 1 < S; ++s) {\n            if (ls[s] == kNegInf) continue;"),
 }
