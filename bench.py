@@ -52,7 +52,8 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--splits", type=int, default=0, help="override the split-count picker")
     ap.add_argument("--varsplit", action="store_true",
-                    help="per-sequence split counts (decode_attn_splitkv_varsplit) with its planner")
+                    help="per-sequence split counts (decode_attn_splitkv_varsplit, or "
+                         "decode_attn_splitkv_multiquery_varsplit with --tq > 1) with its planner")
     ap.add_argument("--split-len", type=int, default=0, help="override the planner's split_len")
     ap.add_argument("--cuda-core-math", action="store_true",
                     help="time the split step with its products on CUDA-core fp32 FMAs instead of "
@@ -481,7 +482,7 @@ def main():
 
     split_len = 0
     if args.varsplit:
-        split_len, S = da.varsplit_plan(p.B, p.Hq, p.Hkv, p.D, p.total_kv, max(p.lens))
+        split_len, S = da.varsplit_plan(p.B, p.Hq * p.tq, p.Hkv, p.D, p.total_kv, max(p.lens))
         if args.split_len:
             split_len = args.split_len
             S = min(da.DA_MAX_SPLITS, -(-max(p.lens) // split_len))
@@ -512,6 +513,9 @@ def main():
                                                      layout=p.layout, stream=stream)
             if S > 1:
                 da.decode_attn_splitkv_combine(out, ws, num_splits=S, stream=stream)
+        elif split_len and p.tq > 1:
+            da.decode_attn_splitkv_multiquery_varsplit(q, k, v, cu, out, ws, split_len=split_len, max_splits=S,
+                                                       scale=p.scale, layout=p.layout, stream=stream)
         elif split_len:
             da.decode_attn_splitkv_varsplit(q, k, v, cu, out, ws, split_len=split_len, max_splits=S,
                                             scale=p.scale, layout=p.layout, stream=stream)

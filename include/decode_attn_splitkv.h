@@ -281,6 +281,30 @@ da_status decode_attn_splitkv_multiquery(const void* q, const void* k, const voi
                                          void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Several new query tokens per sequence (as decode_attn_splitkv_multiquery)
+ * with per-sequence split counts S_b = 1 if L_b = 0, else min(max_splits,
+ * ceil(L_b / split_len)) (as decode_attn_splitkv_varsplit): a ragged batch can
+ * split only its long sequences, whose single items would otherwise outlast
+ * the rest of the batch, and keep the short ones whole, written by the split
+ * step itself with no combine.
+ *   q, out         device, [B, T_q, Hq, D] elements of `dtype`, 16-byte aligned
+ *   T_q            in [1, DA_MAX_QUERY_TOKENS]
+ *   split_len      >= 1; max_splits in [1, DA_MAX_SPLITS]
+ *   B              <= DA_MAX_VARSPLIT_BATCH (else DA_ERR_UNSUPPORTED)
+ *   workspace      >= decode_attn_splitkv_workspace_size(B * T_q, Hq, D, max_splits);
+ *                  rows of lse_part/o_part are (b * T_q + t) * Hq + h, with
+ *                  max_splits as the split stride; entries s >= S_b are left untouched
+ * Pick split_len and max_splits with decode_attn_splitkv_varsplit_plan(B, Hq * T_q, ...).
+ * Other arguments, results and errors as decode_attn_splitkv.
+ */
+da_status decode_attn_splitkv_multiquery_varsplit(const void* q, const void* k, const void* v,
+                                                  const int32_t* cu_seqlens_k, int B, int T_q, int Hq,
+                                                  int Hkv, int D, int kv_rows, da_dtype dtype,
+                                                  da_layout layout, float scale, int split_len,
+                                                  int max_splits, void* out, void* workspace,
+                                                  size_t workspace_bytes, void* stream);
+
+/*
  * Comparison arm for the product choice on Blackwell: decode_attn_splitkv_multiquery
  * with the split step on the tcgen05 tensor cores and the accumulators in tensor
  * memory, for G * T_q > 8 and G <= 32 (else DA_ERR_UNSUPPORTED). Per 64-key stage

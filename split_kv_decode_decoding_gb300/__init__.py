@@ -35,7 +35,7 @@ EXPORTED = [
     "decode_attn_splitkv_varsplit_plan", "decode_attn_splitkv_multiquery",
     "decode_attn_splitkv_model_us", "decode_attn_splitkv_model_best_splits",
     "decode_attn_splitkv_partial_cuda_core", "decode_attn_splitkv_multiquery_tmem",
-    "decode_attn_splitkv_noalloc_get_error",
+    "decode_attn_splitkv_noalloc_get_error", "decode_attn_splitkv_multiquery_varsplit",
 ]
 
 _lib = None
@@ -94,6 +94,9 @@ def load(path: str = LIB):
     lib.decode_attn_splitkv_multiquery.argtypes = [P, P, P, P, I, I, I, I, I, I, I, I, F, I, P, P,
                                                    SZ, P]
     lib.decode_attn_splitkv_multiquery.restype = I
+    lib.decode_attn_splitkv_multiquery_varsplit.argtypes = [P, P, P, P, I, I, I, I, I, I, I, I, F, I, I, P,
+                                                            P, SZ, P]
+    lib.decode_attn_splitkv_multiquery_varsplit.restype = I
     lib.decode_attn_splitkv_multiquery_tmem.argtypes = [P, P, P, P, I, I, I, I, I, I, I, I, F, I, P, P,
                                                         SZ, P]
     lib.decode_attn_splitkv_multiquery_tmem.restype = I
@@ -266,6 +269,24 @@ def decode_attn_splitkv_multiquery(q, k, v, cu_seqlens_k, out, workspace, *, num
     """Several query tokens per sequence: q and out are [B, T_q, Hq, D]; see the C header."""
     return _multiquery("decode_attn_splitkv_multiquery", q, k, v, cu_seqlens_k, out, workspace, num_splits,
                        scale, layout, stream)
+
+
+def decode_attn_splitkv_multiquery_varsplit(q, k, v, cu_seqlens_k, out, workspace, *, split_len: int,
+                                            max_splits: int, scale: float | None = None,
+                                            layout: int = DA_LAYOUT_VARLEN, stream=None):
+    """Several query tokens per sequence with per-sequence split counts: q and out are
+    [B, T_q, Hq, D]; see the C header."""
+    B, T, Hq, D = q.shape
+    if layout == DA_LAYOUT_VARLEN:
+        kv_rows, Hkv = k.shape[0], k.shape[1]
+    else:
+        Hkv, kv_rows = k.shape[1], k.shape[2]
+    sc = 1.0 / math.sqrt(D) if scale is None else scale
+    st = load().decode_attn_splitkv_multiquery_varsplit(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_k), B, T, Hq, Hkv, D, kv_rows, _dtype_code(q),
+        layout, sc, split_len, max_splits, _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "decode_attn_splitkv_multiquery_varsplit")
+    return out
 
 
 def decode_attn_splitkv_multiquery_tmem(q, k, v, cu_seqlens_k, out, workspace, *, num_splits: int,

@@ -941,6 +941,31 @@ da_status decode_attn_splitkv_multiquery(const void* q, const void* k, const voi
 }
 
 
+da_status decode_attn_splitkv_multiquery_varsplit(const void* q, const void* k, const void* v,
+                                                  const int32_t* cu_seqlens_k, int B, int T_q, int Hq, int Hkv,
+                                                  int D, int kv_rows, da_dtype dtype, da_layout layout,
+                                                  float scale, int split_len, int max_splits, void* out,
+                                                  void* workspace, size_t workspace_bytes, void* stream) {
+    if (split_len < 1) return DA_ERR_INVALID_ARG;
+    if (T_q < 1 || T_q > DA_MAX_QUERY_TOKENS) return DA_ERR_INVALID_ARG;
+    if (B < 1 || static_cast<int64_t>(B) * T_q > 0x7fffffffll) return DA_ERR_INVALID_ARG;
+    if (B > kMaxVarsplitBatch) return DA_ERR_UNSUPPORTED;
+    // the workspace holds B * T_q rows of Hq heads, max_splits splits each
+    const size_t need = decode_attn_splitkv_workspace_size(B * T_q, Hq, D, max_splits);
+    da_status st = check_common(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale, max_splits,
+                                workspace, need == 0 ? workspace_bytes : std::max(workspace_bytes, need));
+    if (st != DA_OK) return st;
+    if (workspace_bytes < need) return DA_ERR_WORKSPACE_TOO_SMALL;
+    if (!out) return DA_ERR_INVALID_ARG;
+    if (!aligned(out, 16)) return DA_ERR_ALIGNMENT;
+    const int64_t chunks = item_chunks(static_cast<int64_t>(Hq / Hkv) * T_q);
+    if (static_cast<int64_t>(B) * Hkv * chunks * max_splits > 0x7fffffffll) return DA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(B) * T_q * Hq * D > 0x7fffffffll) return DA_ERR_INVALID_ARG;
+    return run_decode(make_call(q, k, v, cu_seqlens_k, B, Hq, Hkv, D, kv_rows, dtype, layout, scale, max_splits,
+                                split_len, workspace, T_q),
+                      out, static_cast<cudaStream_t>(stream));
+}
+
 da_status decode_attn_splitkv_get_error(void* workspace, uint32_t* device_error_bits, void* stream) {
     if (!workspace || !device_error_bits) return DA_ERR_INVALID_ARG;
     if (!aligned(workspace, 256)) return DA_ERR_ALIGNMENT;

@@ -98,6 +98,8 @@ struct SplitParams {
     int split_len;           // 0: every sequence has S splits; else S_b = min(S, ceil(L_b / split_len))
     int stage_cu;            // cu_seqlens_k staged in shared memory (B small enough)
     int sorted;              // the producer hands out sequences longest first (see kMaxSortedBatch)
+    int prefix_off;          // per-sequence mode: prefix[] at this int32 offset in the staged
+                             // cu_seqlens_k area, or -1: in an area of its own past it
     int tq;                  // query tokens per sequence; columns per KV head = G * tq
     float scale_log2;        // scale * log2(e)
     unsigned long long wait_limit_ns;
@@ -447,8 +449,11 @@ __device__ __forceinline__ SplitLayout split_layout(uint8_t* smem_raw, const Spl
     s.mfull = s.iempty0 + 8 * kItemSlots;
     s.mdone = s.mfull + 8;
     s.cus = p.stage_cu ? reinterpret_cast<int32_t*>(s.smem + Sh::kEnd) : nullptr;
-    s.prefix = reinterpret_cast<int32_t*>(s.smem + Sh::kEnd + (p.stage_cu ? kStagedBytes : 0));
-    s.extra = s.smem + Sh::kEnd + (p.stage_cu ? kStagedBytes : 0) + (p.split_len != 0 ? kStagedBytes : 0);
+    const bool own_prefix = p.split_len != 0 && p.prefix_off < 0;
+    s.prefix = p.prefix_off >= 0 && s.cus != nullptr
+                   ? s.cus + p.prefix_off
+                   : reinterpret_cast<int32_t*>(s.smem + Sh::kEnd + (p.stage_cu ? kStagedBytes : 0));
+    s.extra = s.smem + Sh::kEnd + (p.stage_cu ? kStagedBytes : 0) + (own_prefix ? kStagedBytes : 0);
     return s;
 }
 
@@ -822,7 +827,18 @@ cudaError_t persistent_grid(K kernel, int threads, int smem, DeviceCache& cache,
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     const uint64_t bit = 1ull << dev;
     if (!(cache.attr_done.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        // The limit is the kernel's, shared by every configuration of it (each with
+        // its own cache): raise it once to what the device allows, never to one
+        // configuration's size, which a smaller one set later would undercut.
+        int optin = 0;
+        e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e != cudaSuccess) return e;
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, kernel);
+        if (e != cudaSuccess) return e;
+        const int limit = optin - static_cast<int>(fa.sharedSizeBytes);
+        if (smem > limit) return cudaErrorInvalidValue;
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
         if (e != cudaSuccess) return e;
         int sms = 0, per_sm = 0;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -969,8 +985,14 @@ inline bool prepare_split(const Call& c, void* out, SplitLaunch& a) {
     p.scale_log2 = c.scale * kLog2e;
     p.wait_limit_ns = kWaitLimitNs;
     const bool var = c.split_len != 0;
-    a.smem = Shape<D, NT, ST>::kSmemBytes + (p.stage_cu ? kStagedBytes : 0) + (var ? kStagedBytes : 0);
-    a.cache_idx = (p.stage_cu ? 1 : 0) + (var ? 1 : 0);
+    // per-sequence mode: prefix[] shares the staged cu_seqlens_k area, past its B + 1
+    // entries, when it fits there, so that the 16-column kernel still runs two CTAs
+    // per SM
+    p.prefix_off = -1;
+    if (var && p.stage_cu && 2 * (c.B + 1) + 3 <= kStagedBytes / 4) p.prefix_off = (c.B + 1 + 3) / 4 * 4;
+    const bool own_prefix = var && p.prefix_off < 0;
+    a.smem = Shape<D, NT, ST>::kSmemBytes + (p.stage_cu ? kStagedBytes : 0) + (own_prefix ? kStagedBytes : 0);
+    a.cache_idx = (p.stage_cu ? 1 : 0) + (own_prefix ? 1 : 0);
     return true;
 }
 

@@ -31,7 +31,7 @@ def header_functions():
 
 def test_exports_every_declared_symbol(lib):
     names = header_functions()
-    assert len(names) == 21
+    assert len(names) == 22
     assert sorted(names) == sorted(da.EXPORTED)
     for n in names:
         assert hasattr(lib, n), n
@@ -247,6 +247,25 @@ def test_multiquery_host_checks(lib):
     assert call(T=0) == da.DA_ERR_INVALID_ARG
     assert call(T=da.DA_MAX_QUERY_TOKENS + 1) == da.DA_ERR_INVALID_ARG
     assert call(S=0) == da.DA_ERR_INVALID_ARG
+    assert call(q=FAKE + 4) == da.DA_ERR_ALIGNMENT
+    need = da.workspace_size(2 * 2, 4, 64, 4)
+    assert call(ws_bytes=need - 1) == da.DA_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_multiquery_varsplit_host_checks(lib):
+    v = ctypes.c_void_p
+
+    def call(T=2, n=64, m=4, B=2, ws_bytes=1 << 20, q=FAKE):
+        return lib.decode_attn_splitkv_multiquery_varsplit(v(q), v(FAKE + 0x100000), v(FAKE + 0x200000),
+                                                           v(FAKE + 0x300000), B, T, 4, 1, 64, 237, 0, 0,
+                                                           0.125, n, m, v(FAKE + 0x400000), v(FAKE + 0x500000),
+                                                           ws_bytes, None)
+    assert call(n=0) == da.DA_ERR_INVALID_ARG
+    assert call(m=0) == da.DA_ERR_INVALID_ARG
+    assert call(m=da.DA_MAX_SPLITS + 1) == da.DA_ERR_INVALID_ARG
+    assert call(T=0) == da.DA_ERR_INVALID_ARG
+    assert call(T=da.DA_MAX_QUERY_TOKENS + 1) == da.DA_ERR_INVALID_ARG
+    assert call(B=da.DA_MAX_VARSPLIT_BATCH + 1, ws_bytes=1 << 30) == da.DA_ERR_UNSUPPORTED
     assert call(q=FAKE + 4) == da.DA_ERR_ALIGNMENT
     need = da.workspace_size(2 * 2, 4, 64, 4)
     assert call(ws_bytes=need - 1) == da.DA_ERR_WORKSPACE_TOO_SMALL

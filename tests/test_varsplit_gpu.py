@@ -155,3 +155,43 @@ def test_varsplit_cuda_graph_replay():
         g.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, eager)
+
+
+_MIXED_MODES = r"""
+import sys
+import numpy as np
+import torch
+sys.path.insert(0, sys.argv[1]); sys.path.insert(0, sys.argv[1] + "/tests")
+import split_kv_decode_decoding_gb300 as da
+from gpu_util import to_device
+from synth.workloads import LAYOUT_VARLEN, custom
+da.load()
+rng = np.random.default_rng(5)
+p = custom("mixed", 600, 8, 2, 64, [int(x) for x in rng.integers(1, 40, 600)], "bf16", LAYOUT_VARLEN, None, seed=5)
+q, k, v, cu = to_device(p)
+ws = da.alloc_workspace(p.B, p.Hq, p.D, 4)
+outs = []
+for mode in ("var", "uniform", "var"):
+    out = torch.empty(p.B, p.Hq, p.D, dtype=torch.bfloat16, device="cuda")
+    if mode == "var":
+        da.decode_attn_splitkv_varsplit(q, k, v, cu, out, ws, split_len=16, max_splits=3, scale=p.scale)
+    else:
+        da.decode_attn_splitkv(q, k, v, cu, out, ws, num_splits=1, scale=p.scale)
+    outs.append(out)
+torch.cuda.synchronize()
+assert da.decode_attn_splitkv_get_error(ws) == 0
+assert torch.equal(outs[0], outs[2])
+print("ok")
+"""
+
+
+def test_launch_configurations_of_one_kernel_mix_in_one_process():
+    """One kernel launched with more shared memory (600 sequences with per-sequence splits: their
+    running split counts need an area of their own), then less (uniform splits), then more again,
+    in a fresh process: every launch succeeds and the repeated call gives the same bits."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _MIXED_MODES, root], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stderr[-2000:]
