@@ -244,7 +244,9 @@ da_status decode_attn_splitkv_varsplit(const void* q, const void* k, const void*
  * 256) of about 0.4 of one persistent CTA's share of the keys (R = sm_count *
  * (2 at head_dim 128, 4 at 64) CTAs), raised so that the longest sequence has
  * at most about R / 2 work items, and the max_splits that the longest sequence
- * needs. sm_count 0 means: query the current device.
+ * needs. With several query tokens pass Hq * T_q as Hq (the share then counts
+ * each column chunk's pass over the keys). sm_count 0 means: query the current
+ * device.
  * Returns 0, or -1 (and 1, 1) if an argument is out of range.
  */
 int decode_attn_splitkv_varsplit_plan(int B, int Hq, int Hkv, int D, int64_t total_kv, int max_kv,

@@ -789,11 +789,15 @@ int decode_attn_splitkv_num_splits(int B, int Hq, int Hkv, int D, int min_kv, in
         // A batch of up to kMaxSortedBatch sequences is handed out longest first,
         // so its short items come last and even out the end by themselves: fewer,
         // longer splits measure best (six items per SM, splits up to four CTA
-        // shares), unless one sequence holds most of the keys and its splits are
-        // the critical path.
-        const bool sorted = B <= kMaxSortedBatch && 2.0 * max_kv <= total;
+        // shares), unless one sequence holds most of the keys. Its splits are then
+        // the critical path whatever the width: at most two CTA shares each
+        // (16-column items stream slower per CTA, and four shares took 153 against
+        // 114 us on one 131072-key sequence among fifteen of 512 with four query
+        // tokens).
+        const bool dominant = 2.0 * max_kv > total;
+        const bool sorted = B <= kMaxSortedBatch && !dominant;
         const int64_t per_sm = sorted ? (wide ? 3 : 6) : (wide ? 4 : 8);
-        const double shares = sorted ? (wide ? 8.0 : 4.0) : (wide ? 4.0 : 2.0);
+        const double shares = sorted ? (wide ? 8.0 : 4.0) : (dominant || !wide ? 2.0 : 4.0);
         S = (per_sm * static_cast<int64_t>(sm_count) + units - 1) / units;
         S = std::min<int64_t>(S, std::max<int64_t>(1, min_kv / 64));
         // ... and the longest sequence's splits at most about `shares` times one
@@ -889,7 +893,9 @@ int decode_attn_splitkv_varsplit_plan(int B, int Hq, int Hkv, int D, int64_t tot
     // items than half the CTAs: its splits would otherwise multiply the combine's
     // work and the per-item costs without better balance. Measured on GB300 over
     // split lengths 512 .. 7680 on the Qwen-shaped ragged batch and on a batch of
-    // one 131072-key sequence among fifteen of 512.
+    // one 131072-key sequence among fifteen of 512. Items of a whole share leave
+    // the last ones of the queue, in sequence order, as long as any: 102.4 against
+    // 96.7 us on the Qwen-shaped batch.
     int64_t len = (2 * key_units + 5 * slots - 1) / (5 * slots);
     len = std::max<int64_t>(len, (2 * static_cast<int64_t>(max_kv) * Hkv * chunks + slots - 1) / slots);
     len = std::max<int64_t>(256, (len + kStageKeys - 1) / kStageKeys * kStageKeys);   // whole stages

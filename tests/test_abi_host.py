@@ -128,6 +128,8 @@ def test_picker_choices_on_measured_workloads(lib):
     # several query tokens: Hq passed as Hq * T_q
     assert da.num_splits(64, 28 * 2, 4, 128, 552, 8192, sm) == 2        # 14 columns: S 2..4: 99.7, 101.8, 103.4
     assert da.num_splits(64, 28 * 4, 4, 128, 552, 8192, sm) == 1        # 28 columns: S 1..3: 106.8, 114.2, 124.8
+    # one 128K sequence among 512s with four tokens (16-column items): S 9: 153.0, 16: 113.7, 19: 114.7
+    assert 16 <= da.num_splits(16, 32 * 4, 8, 128, 512, 131072, sm) <= 19
 
 
 def test_picker_degenerate(lib):
@@ -215,6 +217,9 @@ def test_varsplit_plan(lib):
     # items of about 0.4 of one CTA's share (304 CTAs at head_dim 128): 2.5 per CTA
     items = 64 * 4352 * 4 / n
     assert 2.5 * 304 * 0.9 <= items <= 2.5 * 304 * 1.05
+    # four query tokens: 28 columns per KV head take two chunks, each a pass over the keys
+    n4, m4 = da.varsplit_plan(64, 28 * 4, 4, 128, 64 * 4352, 8192, 152)
+    assert 2 * 64 * 4352 * 4 / n4 <= 2.5 * 304 * 1.05 and n4 >= 2 * n - 64 and m4 == -(-8192 // n4)
     # one long sequence among short ones: it gets at most about half the CTAs' worth of items
     n, m = da.varsplit_plan(16, 32, 8, 128, 131072 + 15 * 512, 131072, 152)
     assert n % 64 == 0 and 8 * m <= 304 // 2 + 8 and n >= 2 * 131072 * 8 // 304
