@@ -12,7 +12,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 SOURCES = [os.path.join(CSRC, n) for n in
-           ("decode_attn_splitkv.cu", "comparison_arms.cu", "time_model.cpp")]
+           ("decode_attn_splitkv.cu", "comparison_arms.cu", "picker.cpp", "time_model.cpp")]
 HEADER = os.path.join(ROOT, "include", "decode_attn_splitkv.h")
 LIB = os.path.join(PKG, "_build", "libdecode_attn_splitkv.so")
 # the read-ceiling probe the benchmark times beside the decode call (not part of the library)

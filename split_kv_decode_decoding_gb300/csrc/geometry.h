@@ -1,5 +1,5 @@
 // Work-item geometry of the split step, shared by the kernels (device and host
-// code) and by the host-only time model.
+// code), the host-side split choices and the host-only time model.
 #ifndef DECODE_ATTN_SPLITKV_GEOMETRY_H
 #define DECODE_ATTN_SPLITKV_GEOMETRY_H
 
@@ -10,6 +10,9 @@ namespace da_impl {
 constexpr int kBoxKeys = 16;        // keys per TMA box = rows of one mma m-tile
 constexpr int kStageKeys = 64;      // keys per pipeline stage
 constexpr int kHeadsPerCta = 8;     // mma N: packed (token, head) columns per n-tile
+// Uniform splits over a varlen batch of at most this many sequences: the work
+// queue hands out the sequences longest first.
+constexpr int kMaxSortedBatch = 128;
 
 // Columns (packed query token x head pairs) of one work item: one n-tile of 8,
 // or two when a KV head serves more than 8 columns, so that K and V are read

@@ -43,7 +43,6 @@ constexpr int kStagedBytes = ((kMaxStagedBatch + 1) * 4 + 15) / 16 * 16;   // on
 // queue hands out the sequences longest first, so that the last items to start are
 // the short ones. The order (perm[rank] = sequence) lives in the staged
 // cu_seqlens_k area, past the B + 1 entries it uses.
-constexpr int kMaxSortedBatch = 128;
 constexpr int kLenOff = 384;    // int32 entries into the staged cu_seqlens_k area: lengths [B]
 constexpr int kPermOff = 512;   // and the order [B] (the area holds 1025 + 3 entries)
 static_assert(kLenOff >= kMaxSortedBatch + 1 && kPermOff >= kLenOff + kMaxSortedBatch &&

@@ -14,10 +14,6 @@
 
 using namespace da_impl;
 
-namespace {
-constexpr int kMaxSortedBatchModel = 128;   // batches the split step hands out longest first
-}
-
 extern "C" {
 
 // A GB300 restatement of the lecture page's decode time model
@@ -68,7 +64,7 @@ double decode_attn_splitkv_model_us(const int32_t* kv_lens, int B, int Hq, int H
     // batch, which is what the model assumes), ties in index order.
     std::vector<int> order(static_cast<size_t>(B));
     for (int b = 0; b < B; ++b) order[b] = b;
-    if (B > 1 && B <= kMaxSortedBatchModel)
+    if (B > 1 && B <= kMaxSortedBatch)
         std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
             return std::max(kv_lens[x], 0) > std::max(kv_lens[y], 0);
         });
