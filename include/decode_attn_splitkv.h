@@ -435,6 +435,17 @@ double decode_attn_splitkv_model_us(const int32_t* kv_lens, int B, int Hq, int H
                                     int num_splits, int sm_count, const double* params);
 
 /*
+ * The same model for a decode_attn_splitkv_varsplit (or _multiquery_varsplit)
+ * call: sequence b has S_b = 1 if L_b = 0, else min(max_splits, ceil(L_b /
+ * split_len)) splits, the work items go out in sequence order, and the combine
+ * reads the rows of the sequences with S_b > 1 (T_q * Hq * S_b * (D + 1) * 4
+ * bytes each). split_len >= 1; other arguments as decode_attn_splitkv_model_us.
+ * Returns the predicted time, or a negative value if an argument is out of range.
+ */
+double decode_attn_splitkv_model_varsplit_us(const int32_t* kv_lens, int B, int Hq, int Hkv, int D, int T_q,
+                                             int split_len, int max_splits, int sm_count, const double* params);
+
+/*
  * The split count (up to min(shortest length, 256)) that the built-in time model
  * predicts fastest, and the predicted time in *predicted_us (may be NULL): the
  * model-driven counterpart of decode_attn_splitkv_num_splits (the lecture

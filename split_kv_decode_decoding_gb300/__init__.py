@@ -36,6 +36,7 @@ EXPORTED = [
     "decode_attn_splitkv_model_us", "decode_attn_splitkv_model_best_splits",
     "decode_attn_splitkv_partial_cuda_core", "decode_attn_splitkv_multiquery_tmem",
     "decode_attn_splitkv_noalloc_get_error", "decode_attn_splitkv_multiquery_varsplit",
+    "decode_attn_splitkv_model_varsplit_us",
 ]
 
 _lib = None
@@ -102,6 +103,8 @@ def load(path: str = LIB):
     lib.decode_attn_splitkv_multiquery_tmem.restype = I
     lib.decode_attn_splitkv_model_us.argtypes = [P, I, I, I, I, I, I, I, P]
     lib.decode_attn_splitkv_model_us.restype = ctypes.c_double
+    lib.decode_attn_splitkv_model_varsplit_us.argtypes = [P, I, I, I, I, I, I, I, I, P]
+    lib.decode_attn_splitkv_model_varsplit_us.restype = ctypes.c_double
     lib.decode_attn_splitkv_model_best_splits.argtypes = [P, I, I, I, I, I, I,
                                                           ctypes.POINTER(ctypes.c_double)]
     lib.decode_attn_splitkv_model_best_splits.restype = I
@@ -166,6 +169,19 @@ def model_us(lens, Hq: int, Hkv: int, D: int, num_splits: int, sm_count: int, T_
         raise ValueError("model_us takes 8 parameters")
     return load().decode_attn_splitkv_model_us(ln.ctypes.data, ln.size, Hq, Hkv, D, T_q, num_splits,
                                                sm_count, None if pa is None else pa.ctypes.data)
+
+
+def model_varsplit_us(lens, Hq: int, Hkv: int, D: int, split_len: int, max_splits: int, sm_count: int,
+                      T_q: int = 1, params=None) -> float:
+    """Predicted µs of one call with per-sequence split counts (the same model)."""
+    import numpy as np
+    ln = np.ascontiguousarray(lens, dtype=np.int32)
+    pa = None if params is None else np.ascontiguousarray(params, dtype=np.float64)
+    if pa is not None and pa.size != 8:
+        raise ValueError("model_varsplit_us takes 8 parameters")
+    return load().decode_attn_splitkv_model_varsplit_us(ln.ctypes.data, ln.size, Hq, Hkv, D, T_q, split_len,
+                                                        max_splits, sm_count,
+                                                        None if pa is None else pa.ctypes.data)
 
 
 def model_best_splits(lens, Hq: int, Hkv: int, D: int, sm_count: int, T_q: int = 1) -> tuple:

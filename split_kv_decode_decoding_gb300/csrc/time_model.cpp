@@ -20,13 +20,15 @@ extern "C" {
 // (04_flash_decoding.py: decode_attention_time / best_splits, whose A100/H100
 // constants are not on the page): the call is modelled as
 //   T = t0 + makespan + kappa * (largest item's bytes) / (bw / min(items, CTAs))
-//         + [S > 1] (t_comb + W_ws / bw_comb)
+//         + [some S_b > 1] (t_comb + W_ws / bw_comb)
 // where makespan is a processor-sharing run of the work items, in queue order,
 // over the persistent CTAs: each CTA spends t_item before an item and then
 // streams its bytes (each split's key count rounded up to the 16-key TMA box)
 // at min(r_cta, bw / streaming CTAs), r_cta being one CTA's rate for 8-column
 // items and r_cta2 for 16-column ones; kappa charges the last item for the
-// CTAs' unequal rates, and W_ws is the workspace bytes the combine reads.
+// CTAs' unequal rates, and W_ws is the workspace bytes the combine reads (the
+// rows of sequences with more than one split). S_b = S with uniform splits,
+// min(S, ceil(L_b / split_len)) with per-sequence counts.
 // Fitted (least squares in log time) on one GB300 to the 305 calls, of 546
 // measured (17 single-token workloads of the CodeLlama, Llama, Qwen and MHA
 // shapes and 9 of them with 2 or 4 new tokens x split counts 1 to 256, L2
@@ -44,10 +46,16 @@ static const double kModelGb300[8] = {
     /* kappa       */ 0.05334,
     /* r_cta2 B/us */ 46900};
 
-double decode_attn_splitkv_model_us(const int32_t* kv_lens, int B, int Hq, int Hkv, int D, int T_q, int num_splits,
-                                    int sm_count, const double* params) {
+}  // extern "C"
+
+namespace {
+
+// The model of one call: S splits per sequence (split_len = 0), or per-sequence
+// counts S_b = min(S, ceil(L_b / split_len)) (1 for an empty sequence).
+double model_call(const int32_t* kv_lens, int B, int Hq, int Hkv, int D, int T_q, int num_splits, int split_len,
+                  int sm_count, const double* params) {
     if (!kv_lens || B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || (D != 64 && D != 128) || T_q < 1 ||
-        num_splits < 1 || num_splits > DA_MAX_SPLITS || sm_count < 1)
+        num_splits < 1 || num_splits > DA_MAX_SPLITS || sm_count < 1 || split_len < 0)
         return -1.0;
     const double* m = params ? params : kModelGb300;
     const double t0 = m[0], t_item = m[1], bw = m[3], t_comb = m[4], bw_comb = m[5], kappa = m[6];
@@ -59,22 +67,26 @@ double decode_attn_splitkv_model_us(const int32_t* kv_lens, int B, int Hq, int H
     const int chunks = static_cast<int>(item_chunks(static_cast<int64_t>(Hq / Hkv) * T_q));
     const int slots = sm_count * (D == 128 ? 2 : 4);
     const double key_bytes = 4.0 * D;   // K and V rows of one key and KV head
-    // the work items in queue order and the bytes each streams. The split step
-    // hands out the sequences of a batch of at most 128 longest first (a varlen
-    // batch, which is what the model assumes), ties in index order.
+    // the work items in queue order and the bytes each streams. With uniform
+    // splits the split step hands out the sequences of a batch of at most 128
+    // longest first (a varlen batch, which is what the model assumes), ties in
+    // index order; per-sequence counts go out in index order.
     std::vector<int> order(static_cast<size_t>(B));
     for (int b = 0; b < B; ++b) order[b] = b;
-    if (B > 1 && B <= kMaxSortedBatch)
+    if (split_len == 0 && B > 1 && B <= kMaxSortedBatch)
         std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
             return std::max(kv_lens[x], 0) > std::max(kv_lens[y], 0);
         });
     std::vector<double> items;
-    double biggest = 0.0;
+    double biggest = 0.0, comb_rows = 0.0;   // rows the combine merges, times their split counts
     for (int b : order) {
         const int64_t L = kv_lens[b] < 0 ? 0 : kv_lens[b];
+        int Sb = S;
+        if (split_len > 0) Sb = L == 0 ? 1 : static_cast<int>(std::min<int64_t>(S, (L + split_len - 1) / split_len));
+        if (Sb > 1) comb_rows += static_cast<double>(T_q) * Hq * Sb;
         for (int kvh = 0; kvh < Hkv; ++kvh)
-            for (int s = 0; s < S; ++s) {
-                const int64_t n = L * (s + 1) / S - L * s / S;
+            for (int s = 0; s < Sb; ++s) {
+                const int64_t n = L * (s + 1) / Sb - L * s / Sb;
                 const double bytes = static_cast<double>((n + kBoxKeys - 1) / kBoxKeys * kBoxKeys) * key_bytes;
                 biggest = std::max(biggest, bytes / chunks);
                 // the `chunks` items of a split run side by side and read its keys
@@ -121,8 +133,23 @@ double decode_attn_splitkv_model_us(const int32_t* kv_lens, int B, int Hq, int H
     // the last item, which costs a fraction kappa of its time at the fair share
     const double fair = bw / static_cast<double>(std::max<size_t>(1, std::min<size_t>(items.size(), slots)));
     double t = t0 + makespan + kappa * biggest / fair;
-    if (S > 1) t += t_comb + static_cast<double>(B) * T_q * Hq * S * (D + 1) * 4.0 / bw_comb;
+    if (comb_rows > 0) t += t_comb + comb_rows * (D + 1) * 4.0 / bw_comb;
     return t;
+}
+
+}  // namespace
+
+extern "C" {
+
+double decode_attn_splitkv_model_us(const int32_t* kv_lens, int B, int Hq, int Hkv, int D, int T_q, int num_splits,
+                                    int sm_count, const double* params) {
+    return model_call(kv_lens, B, Hq, Hkv, D, T_q, num_splits, 0, sm_count, params);
+}
+
+double decode_attn_splitkv_model_varsplit_us(const int32_t* kv_lens, int B, int Hq, int Hkv, int D, int T_q,
+                                             int split_len, int max_splits, int sm_count, const double* params) {
+    if (split_len < 1) return -1.0;
+    return model_call(kv_lens, B, Hq, Hkv, D, T_q, max_splits, split_len, sm_count, params);
 }
 
 int decode_attn_splitkv_model_best_splits(const int32_t* kv_lens, int B, int Hq, int Hkv, int D, int T_q,

@@ -31,7 +31,7 @@ def header_functions():
 
 def test_exports_every_declared_symbol(lib):
     names = header_functions()
-    assert len(names) == 22
+    assert len(names) == 23
     assert sorted(names) == sorted(da.EXPORTED)
     for n in names:
         assert hasattr(lib, n), n
@@ -316,6 +316,23 @@ def test_time_model_formula_by_hand(lib):
     params_bw = [5.0, 1.0, 65536.0, 1e5, 2.0, 1e6, 0.5, 32768.0]
     t4 = da.model_us([1000, 1000], 1, 1, 128, 2, 152, params=params_bw)
     assert abs(t4 - (5 + 1 + 262144 / 25000 + 0.5 * 262144 / 25000 + 2 + 0.002064)) < 1e-9
+
+
+def test_time_model_per_sequence_by_hand(lib):
+    """Per-sequence counts, worked by hand: lengths [1000, 300], split_len 500, max_splits 4.
+
+    S_b = 2 and 1: two items of 500 keys (512 after rounding: 262144 B) and one of 300 (304:
+    155648 B), in sequence order, three CTAs streaming at min(65536, 1e6 / 3) = 65536 B/us
+    after t_item = 1 us: the makespan is 1 + 262144 / 65536 = 5 us. Last-item term
+    0.5 * 262144 / (1e6 / 3); the combine reads the two split rows of sequence 0 only:
+    2 * 129 * 4 = 1032 B."""
+    params = [5.0, 1.0, 65536.0, 1e6, 2.0, 1e6, 0.5, 32768.0]
+    t = da.model_varsplit_us([1000, 300], 1, 1, 128, 500, 4, 152, params=params)
+    assert abs(t - (5 + 5 + 0.5 * 262144 / (1e6 / 3) + 2 + 0.001032)) < 1e-9
+    # every sequence in one split: the uniform model with S = 1 (same order here)
+    assert abs(da.model_varsplit_us([1000, 300], 1, 1, 128, 2000, 1, 152, params=params)
+               - da.model_us([1000, 300], 1, 1, 128, 1, 152, params=params)) < 1e-12
+    assert da.model_varsplit_us([1000, 300], 1, 1, 128, 0, 4, 152) < 0       # split_len < 1
 
 
 def test_time_model_properties(lib):
