@@ -1,4 +1,4 @@
-"""Compile the CUDA library for sm_103a, in tree (no cmake): three translation units
+"""Compile the CUDA library for sm_103a, in tree (no cmake): four translation units
 compiled in parallel, then linked into one shared library."""
 from __future__ import annotations
 
