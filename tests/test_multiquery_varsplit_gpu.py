@@ -162,3 +162,26 @@ def test_multiquery_varsplit_rejects_bad_arguments():
     small = da.alloc_workspace(p.B, p.Hq, p.D, 4)   # rows for one token only
     with pytest.raises(da.DecodeAttnError):
         da.decode_attn_splitkv_multiquery_varsplit(q, k, v, cu, out, small, split_len=8, max_splits=4)
+
+
+def test_multiquery_varsplit_cuda_graph_replay():
+    """The call captured in a CUDA graph and replayed gives the eager call's bits (the work queue
+    re-arms itself, nothing is allocated or copied on the host)."""
+    p = custom("mvgraph", 3, 28, 4, 128, [3000, 100, 900], "f16", LAYOUT_VARLEN, None, seed=43, tq=4)
+    q, k, v, cu = to_device(p)
+    q = q.view(p.B, 4, p.Hq, p.D)
+    ws = da.alloc_workspace(p.B * 4, p.Hq, p.D, 8)
+    out = torch.empty(p.B, 4, p.Hq, p.D, dtype=torch.float16, device="cuda")
+    da.decode_attn_splitkv_multiquery_varsplit(q, k, v, cu, out, ws, split_len=512, max_splits=8, scale=p.scale)
+    torch.cuda.synchronize()
+    eager = out.clone()
+    g = torch.cuda.CUDAGraph()
+    out.zero_()
+    with torch.cuda.graph(g):
+        da.decode_attn_splitkv_multiquery_varsplit(q, k, v, cu, out, ws, split_len=512, max_splits=8,
+                                                   scale=p.scale)
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
+    assert da.decode_attn_splitkv_get_error(ws) == 0
