@@ -135,6 +135,23 @@ def test_varsplit_large_ragged_batch(B):
             assert max_abs(opart[b, :, :n], ref_op[b, :, :n]) <= opart_tol(p), b
 
 
+@pytest.mark.parametrize("B", [511, 512])
+def test_varsplit_running_counts_in_and_out_of_the_staged_area(B):
+    """Up to 511 sequences the per-sequence running split counts share the staged cu_seqlens_k
+    area; from 512 they take an area of their own. Both sides of that limit, every output
+    element against the oracle."""
+    rng = np.random.default_rng(B)
+    lens = [int(x) for x in rng.choice([0, 1, 17, 64, 100, 300], size=B)]
+    p = custom(f"vlim{B}", B, 4, 1, 64, lens, "f16", LAYOUT_VARLEN, None, seed=B)
+    q, k, v, cu = to_device(p)
+    ws = da.alloc_workspace(p.B, p.Hq, p.D, 8)
+    out = torch.empty(p.B, p.Hq, p.D, dtype=torch.float16, device="cuda")
+    da.decode_attn_splitkv_varsplit(q, k, v, cu, out, ws, split_len=48, max_splits=8, scale=p.scale)
+    assert da.decode_attn_splitkv_get_error(ws) == 0
+    ref, _ = oracle.default().attention(p)
+    assert out_excess(out.to(torch.float64).cpu().numpy(), ref, p.dtype) <= OUT_TOL
+
+
 def test_multiquery_varsplit_qwen_every_row():
     """The Qwen-shaped ragged batch with four query tokens, at the planner's split length (as the
     bench times it with --varsplit --tq 4): every (sequence, token, head) row against the oracle."""
