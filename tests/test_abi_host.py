@@ -335,6 +335,21 @@ def test_time_model_per_sequence_by_hand(lib):
     assert da.model_varsplit_us([1000, 300], 1, 1, 128, 0, 4, 152) < 0       # split_len < 1
 
 
+def test_time_model_queue_order(lib):
+    """With uniform splits the model hands out a batch of up to 128 sequences longest first, as
+    the split step does: the order of the lengths does not matter. Per-sequence counts go out in
+    sequence order, where a long sequence at the end of the queue costs more."""
+    lens = [512] * 30 + [65536]
+    rev = [65536] + [512] * 30
+    t_end = da.model_us(lens, 32, 8, 128, 4, 152)
+    t_start = da.model_us(rev, 32, 8, 128, 4, 152)
+    assert abs(t_end - t_start) < 1e-9
+    # 16 splits of the long sequence x 8 KV heads + 240 short items: more items than the 304 CTAs
+    v_end = da.model_varsplit_us(lens, 32, 8, 128, 4096, 16, 152)
+    v_start = da.model_varsplit_us(rev, 32, 8, 128, 4096, 16, 152)
+    assert v_end > v_start
+
+
 def test_time_model_properties(lib):
     base = da.model_us([4096] * 8, 32, 32, 128, 1, 152)
     assert base > 0
