@@ -97,6 +97,8 @@ struct SplitParams {
     int split_len;           // 0: every sequence has S splits; else S_b = min(S, ceil(L_b / split_len))
     int stage_cu;            // cu_seqlens_k staged in shared memory (B small enough)
     int sorted;              // the producer hands out sequences longest first (see kMaxSortedBatch)
+    int rearm;               // 1: the last CTA resets the work queue; 0: the combine launch that
+                             // follows does (no counter round trip at the end of this kernel)
     int prefix_off;          // per-sequence mode: prefix[] at this int32 offset in the staged
                              // cu_seqlens_k area, or -1: in an area of its own past it
     int tq;                  // query tokens per sequence; columns per KV head = G * tq
@@ -759,7 +761,7 @@ __device__ __forceinline__ void split_finish(const SplitParams& p, bool ok, uint
         if (bad_bar != 0) mbar_wait(bad_bar, bad_ph, p.wait_limit_ns);
         return;
     }
-    if (threadIdx.x == 0) {
+    if (p.rearm && threadIdx.x == 0) {
         const uint32_t prev = atomicAdd(p.done, 1u);
         if (prev == gridDim.x - 1) {
             atomicExch(p.work, 0u);
@@ -902,6 +904,7 @@ struct Call {
     int split_len;   // 0: S splits for every sequence; else per-sequence S_b
     int tq;          // query tokens per sequence
     void* ws;
+    int combine_rearms;   // a combine launch follows the split step and resets its work queue
 };
 
 
@@ -924,6 +927,7 @@ inline Call make_call(const void* q, const void* k, const void* v, const int32_t
     c.S = S;
     c.split_len = split_len;
     c.ws = ws;
+    c.combine_rearms = 0;
     return c;
 }
 
@@ -981,6 +985,7 @@ inline bool prepare_split(const Call& c, void* out, SplitLaunch& a) {
     p.split_len = c.split_len;
     p.stage_cu = c.B <= kMaxStagedBatch;
     p.sorted = c.split_len == 0 && c.lay == DA_LAYOUT_VARLEN && c.B > 1 && c.B <= kMaxSortedBatch && p.stage_cu;
+    p.rearm = c.combine_rearms ? 0 : 1;
     p.scale_log2 = c.scale * kLog2e;
     p.wait_limit_ns = kWaitLimitNs;
     const bool var = c.split_len != 0;
