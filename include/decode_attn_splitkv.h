@@ -91,7 +91,8 @@ typedef enum {
  * 256-byte aligned):
  *   [0, 256)            header: uint32 device error word at offset 0, the split step's
  *                       work-queue counters at offsets 64 and 128 (zero between calls:
- *                       the last CTA of each call re-arms them), rest reserved
+ *                       each call's last take from the queue, or the last CTA of the
+ *                       tcgen05 arm, resets them), rest reserved
  *   [256, 256 + A)      lse_part, float32 [B, Hq, num_splits], natural log of the
  *                       scaled scores, A = round_up(B*Hq*num_splits*4, 256)
  *   [256 + A, total)    o_part, float32 [B, Hq, num_splits, D], normalised per split

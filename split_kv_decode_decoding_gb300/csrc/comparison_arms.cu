@@ -905,7 +905,8 @@ split_kernel_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
         if (threadIdx.x == 0) flag_error(p.err, DA_DEVERR_TIMEOUT);
         return;
     }
-    // the last CTA to finish re-arms the work queue (as in split_kernel)
+    // the last CTA to finish re-arms the work queue (this kernel counts its CTAs out;
+    // split_kernel resets the queue at its last take instead)
     if (threadIdx.x == 0) {
         const uint32_t prev = atomicAdd(p.done, 1u);
         if (prev == gridDim.x - 1) {
@@ -996,7 +997,6 @@ da_status launch_split_tc(const Call& c, void* out, cudaStream_t stream) {
     p.stage_cu = c.B <= kMaxStagedBatch;
     p.sorted = 0;   // this kernel's producer hands out items in index order
     p.prefix_off = -1;   // and keeps prefix[] in an area of its own
-    p.rearm = 1;         // and resets its work queue itself
     p.scale_log2 = c.scale * kLog2e;
     p.wait_limit_ns = kWaitLimitNs;
 

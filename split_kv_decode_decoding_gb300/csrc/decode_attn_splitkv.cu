@@ -584,21 +584,13 @@ struct CombineParams {
     const float* opart;      // [rows, S, D]
     uint16_t* out;           // [rows, D]
     const int32_t* cu;       // per-sequence mode: row r's split count comes from sequence r / Hq
-    uint32_t* work;          // the split step's work queue: reset here when rearm is set
-    uint32_t* done;
-    int rows, S, dchunks, Hq, split_len, layout, kv_rows, no_kv, rearm;
+    int rows, S, dchunks, Hq, split_len, layout, kv_rows, no_kv;
 };
 
 template <int D, int DT>
 __global__ void __launch_bounds__(128) combine_kernel(const CombineParams cp) {
     grid_dependency_wait();
     if (threadIdx.x == 0) grid_dependents_launch();
-    // the split step that this launch follows has finished: reset its work queue for the
-    // next call on this workspace
-    if (cp.rearm && blockIdx.x == 0 && threadIdx.x == 0) {
-        *cp.work = 0u;
-        *cp.done = 0u;
-    }
     const int warp_id = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (warp_id >= cp.rows * cp.dchunks) return;
@@ -697,9 +689,6 @@ da_status launch_combine(const Call& c, void* out, cudaStream_t stream) {
     cp.layout = c.lay;
     cp.kv_rows = c.kv_rows;
     cp.no_kv = c.kv_rows == 0;
-    cp.work = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(c.ws) + kWorkCounterOff);
-    cp.done = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(c.ws) + kDoneCounterOff);
-    cp.rearm = c.combine_rearms;
     const int64_t warps = static_cast<int64_t>(cp.rows) * cp.dchunks;
     cudaLaunchAttribute attrs[1] = {pdl_attr()};
     cudaLaunchConfig_t cfg = {};
@@ -733,9 +722,7 @@ da_status dispatch_combine(const Call& c, void* out, cudaStream_t st) {
 
 // Split step, then the combine step unless every sequence has a single split
 // (S = 1, or a per-sequence cap of 1): the split step then wrote all of `out`.
-da_status run_decode(const Call& call, void* out, cudaStream_t st) {
-    Call c = call;
-    c.combine_rearms = c.S > 1;   // the combine resets the work queue, not the split step's last CTA
+da_status run_decode(const Call& c, void* out, cudaStream_t st) {
     da_status r = dispatch_split(c, out, st);
     if (r != DA_OK || c.S == 1) return r;
     return dispatch_combine(c, out, st);

@@ -91,14 +91,12 @@ struct SplitParams {
     float* opart;            // [B, Hq, S, D]
     uint32_t* err;           // device error word
     uint32_t* work;          // work-queue head
-    uint32_t* done;          // CTAs finished
+    uint32_t* done;          // CTAs finished (the tcgen05 comparison arm's queue reset)
     uint16_t* out;           // [B, Hq, D]: rows of sequences with one split are written here (nullptr: none)
     int B, Hq, Hkv, G, S, kv_rows, layout, chunks, no_kv, n_items;
     int split_len;           // 0: every sequence has S splits; else S_b = min(S, ceil(L_b / split_len))
     int stage_cu;            // cu_seqlens_k staged in shared memory (B small enough)
     int sorted;              // the producer hands out sequences longest first (see kMaxSortedBatch)
-    int rearm;               // 1: the last CTA resets the work queue; 0: the combine launch that
-                             // follows does (no counter round trip at the end of this kernel)
     int prefix_off;          // per-sequence mode: prefix[] at this int32 offset in the staged
                              // cu_seqlens_k area, or -1: in an area of its own past it
     int tq;                  // query tokens per sequence; columns per KV head = G * tq
@@ -610,6 +608,16 @@ __device__ __forceinline__ void split_producer(const SplitLayout& sl, const Spli
             }
             return 1;
         };
+        // Take the next item index from the queue. A call takes exactly n_items
+        // indices from it (one per item after each CTA's first, one past the end
+        // per CTA that had a first item), so the take that returns the last of them
+        // resets the counter for the next call on this workspace: no CTA counts
+        // itself out at the end.
+        auto take_next = [&]() -> int {
+            const uint32_t raw = atomicAdd(p.work, 1u);
+            if (raw + 1u == static_cast<uint32_t>(n_items)) atomicExch(p.work, 0u);
+            return static_cast<int>(gridDim.x + raw);
+        };
         ItemSlot item;
         // the first item of each CTA is its own index
         int state = publish(0, static_cast<int>(blockIdx.x), item);
@@ -620,10 +628,10 @@ __device__ __forceinline__ void split_producer(const SplitLayout& sl, const Spli
             // at the end of the queue).
             const int fetch_at = max(0, item.ntiles - Sh::kStages);
             int next_idx = 0;
-            if (item.ntiles == 0) next_idx = static_cast<int>(gridDim.x + atomicAdd(p.work, 1u));
+            if (item.ntiles == 0) next_idx = take_next();
             bool ok = true;
             for (int t = 0; t < item.ntiles; ++t) {
-                if (t == fetch_at) next_idx = static_cast<int>(gridDim.x + atomicAdd(p.work, 1u));
+                if (t == fetch_at) next_idx = take_next();
                 if (!mbar_wait(empty0 + 8 * st, ph ^ 1, p.wait_limit_ns)) {
                     flag_error(p.err, DA_DEVERR_TIMEOUT);
                     ok = false;
@@ -750,24 +758,12 @@ __device__ __forceinline__ void merge_write(const SplitParams& p, const ItemSlot
     }
 }
 
-// End of a consumer warp's run: after a time-out, give an in-flight copy one
-// more bounded wait; otherwise the last CTA to finish re-arms the work queue
-// for the next call. No fence: the counters order no data (the outputs are read
-// only after this grid completes), and every CTA's last queue atomic has
-// returned before its producer published the end of the queue, which precedes
-// this increment.
+// End of a consumer warp's run. The work queue needs nothing here: its last take
+// reset it (split_producer).
 __device__ __forceinline__ void split_finish(const SplitParams& p, bool ok, uint32_t bad_bar, uint32_t bad_ph) {
-    if (!ok) {
-        if (bad_bar != 0) mbar_wait(bad_bar, bad_ph, p.wait_limit_ns);
-        return;
-    }
-    if (p.rearm && threadIdx.x == 0) {
-        const uint32_t prev = atomicAdd(p.done, 1u);
-        if (prev == gridDim.x - 1) {
-            atomicExch(p.work, 0u);
-            atomicExch(p.done, 0u);
-        }
-    }
+    // after a timed-out wait, a copy still in flight into this CTA's shared memory
+    // gets one more bounded wait before the CTA exits
+    if (!ok && bad_bar != 0) mbar_wait(bad_bar, bad_ph, p.wait_limit_ns);
 }
 
 // ------------------------------------------------------------ host side
@@ -904,7 +900,6 @@ struct Call {
     int split_len;   // 0: S splits for every sequence; else per-sequence S_b
     int tq;          // query tokens per sequence
     void* ws;
-    int combine_rearms;   // a combine launch follows the split step and resets its work queue
 };
 
 
@@ -927,7 +922,6 @@ inline Call make_call(const void* q, const void* k, const void* v, const int32_t
     c.S = S;
     c.split_len = split_len;
     c.ws = ws;
-    c.combine_rearms = 0;
     return c;
 }
 
@@ -985,7 +979,6 @@ inline bool prepare_split(const Call& c, void* out, SplitLaunch& a) {
     p.split_len = c.split_len;
     p.stage_cu = c.B <= kMaxStagedBatch;
     p.sorted = c.split_len == 0 && c.lay == DA_LAYOUT_VARLEN && c.B > 1 && c.B <= kMaxSortedBatch && p.stage_cu;
-    p.rearm = c.combine_rearms ? 0 : 1;
     p.scale_log2 = c.scale * kLog2e;
     p.wait_limit_ns = kWaitLimitNs;
     const bool var = c.split_len != 0;
