@@ -168,7 +168,7 @@ def fit(paths, within: float = 1.3, workers: int = 8) -> dict:
         params = [math.exp(v) for v in x]
         return sum(pool.map(_log_err, [(params, c) for c in chunks]))
 
-    x = [math.log(v) for v in (12.24, 0.1241, 76340, 7.592e6, 2.462, 8.561e5, 0.05135, 52610)]
+    x = [math.log(v) for v in (12.12, 1e-3, 76030, 7.727e6, 3.563, 6.607e5, 0.05334, 46900)]
     best = None
     for _ in range(3):
         res = minimize(loss, x if best is None else best.x, method="Nelder-Mead",

@@ -29,22 +29,22 @@ extern "C" {
 // CTAs' unequal rates, and W_ws is the workspace bytes the combine reads (the
 // rows of sequences with more than one split). S_b = S with uniform splits,
 // min(S, ceil(L_b / split_len)) with per-sequence counts.
-// Fitted (least squares in log time) on one GB300 to the 305 calls, of 546
+// Fitted (least squares in log time) on one GB300 to the 311 calls, of 546
 // measured (17 single-token workloads of the CodeLlama, Llama, Qwen and MHA
 // shapes and 9 of them with 2 or 4 new tokens x split counts 1 to 256, L2
 // flushed, CUDA-event median per call), that lie within 30 % of their
-// workload's fastest split count: median error 2.8 %, 90th percentile 10.1 %.
+// workload's fastest split count: median error 2.6 %, 90th percentile 11.5 %.
 // The fit puts t_item at zero: the ring, which keeps filling across items,
 // hides the per-item work.
 static const double kModelGb300[8] = {
-    /* t0 us       */ 12.12,
+    /* t0 us       */ 11.98,
     /* t_item us   */ 0.0,
-    /* r_cta B/us  */ 76030,
-    /* bw B/us     */ 7.727e+06,
-    /* t_comb us   */ 3.563,
-    /* bw_comb     */ 6.607e+05,
-    /* kappa       */ 0.05334,
-    /* r_cta2 B/us */ 46900};
+    /* r_cta B/us  */ 76280,
+    /* bw B/us     */ 7.757e+06,
+    /* t_comb us   */ 3.209,
+    /* bw_comb     */ 6.478e+05,
+    /* kappa       */ 0.05065,
+    /* r_cta2 B/us */ 46550};
 
 }  // extern "C"
 
