@@ -61,6 +61,10 @@ CASES = [
     # more than 8 columns per KV head: 16-column items (two n-tiles), and a second chunk
     ("group20_two_chunks", 2, 40, 2, 128, [300, 517], "f16", LAYOUT_VARLEN, 3, 0),
     ("group9_d64_bhsd", 2, 18, 2, 64, [100, 64], "bf16", LAYOUT_BHSD, 2, 128),
+    # the shape of the MiniInfer page's self-test (flash_decode_splitk.py, __main__: fp16, batch 2,
+    # 4 heads, head_dim 64, 256 keys, 4 splits, [batch, heads, seqlen, dim]), held here to the
+    # oracle's tolerances rather than that test's 2e-2
+    ("miniinfer_self_test_shape", 2, 4, 4, 64, [256, 256], "f16", LAYOUT_BHSD, 4, 256),
 ]
 
 
