@@ -42,6 +42,17 @@ def test_tiny_workload():
     check_full(p, p.num_splits)
 
 
+@pytest.mark.parametrize("R", [1, 8], ids=["one_head", "eight_packed_heads"])
+def test_split_invariance_of_the_lecture_example(R):
+    """The lecture page's exactness demonstration (04_flash_decoding.py, demo1_exact): one
+    sequence of 10 000 keys, head_dim 128, 1 or 8 query heads packed on one KV head, split into
+    1, 7, 64 and 1000 pieces: every split count against the same unsplit oracle result, and
+    every per-split partial against the oracle's."""
+    p = custom(f"demo1_R{R}", 1, R, 1, 128, [10000], "f16", LAYOUT_VARLEN, None, seed=11 + R)
+    for S in (1, 7, 64, 1000):
+        check_full(p, S)
+
+
 CASES = [
     # name, B, Hq, Hkv, D, lens, dtype, layout, S, kv_rows
     ("short_tiles", 3, 8, 1, 128, [1, 16, 17], "f16", LAYOUT_VARLEN, 1, 0),
