@@ -67,6 +67,9 @@ def parse():
     ap.add_argument("--tq", type=int, default=1,
                     help="query tokens per sequence (decode_attn_splitkv_multiquery when > 1)")
     ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--e2e-buffers", type=int, default=2,
+                    help="device input sets the end-to-end steps alternate (2: a step's copies overlap "
+                         "the previous step's call)")
     ap.add_argument("--e2e-copy-streams", type=int, default=1,
                     help="streams the e2e leg spreads its host->device K/V copies over")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -501,13 +504,16 @@ def main():
     if args.tmem_math and (split_len or args.cuda_core_math or (p.Hq // p.Hkv) * p.tq <= 8
                            or p.Hq // p.Hkv > 32):
         raise SystemExit("--tmem-math takes uniform splits and G * T_q > 8 with G <= 32")
-    q4 = q.view(p.B, p.tq, p.Hq, p.D)
+    q_main, k_main, v_main, cu_main = q, k, v, cu
     out4 = out.view(p.B, p.tq, p.Hq, p.D)
 
-    def call():
+    def call(bufs=None):
+        # bufs: another (q, k, v, cu) set of device inputs (the end-to-end steps alternate two)
+        q, k, v, cu = bufs if bufs is not None else (q_main, k_main, v_main, cu_main)
         if args.tmem_math:
-            da.decode_attn_splitkv_multiquery_tmem(q4, k, v, cu, out4, ws, num_splits=S, scale=p.scale,
-                                                   layout=p.layout, stream=stream)
+            da.decode_attn_splitkv_multiquery_tmem(q.view(p.B, p.tq, p.Hq, p.D), k, v, cu, out4, ws,
+                                                   num_splits=S, scale=p.scale, layout=p.layout,
+                                                   stream=stream)
         elif args.cuda_core_math:
             da.decode_attn_splitkv_partial_cuda_core(q, k, v, cu, ws, num_splits=S, scale=p.scale,
                                                      layout=p.layout, stream=stream)
@@ -613,33 +619,48 @@ def main():
 
         ncs = max(1, args.e2e_copy_streams)
         copy_streams = [torch.cuda.Stream(device=dev) for _ in range(ncs)]
-        # K and V cut into ncs pieces each, one piece of each per copy stream
+        # Two sets of device inputs, used by alternate steps: a step's host-to-device
+        # copies go into the set the previous step's call is not reading, so they run
+        # while that call runs. Every step still copies all of its inputs in.
+        nbuf = max(1, min(2, args.e2e_buffers))
+        sets = [(q, k, v, cu)] + [tuple(torch.empty_like(t) for t in (q, k, v, cu)) for _ in range(nbuf - 1)]
+        # K and V of each set cut into ncs pieces each, one piece of each per copy stream
         pieces = []
-        for dst, src in ((k, pk), (v, pv)):
-            fd, fs = dst.view(-1), src.view(-1)
-            n = fd.numel()
-            for i in range(ncs):
-                a, b = n * i // ncs, n * (i + 1) // ncs
-                pieces.append((i, fd[a:b], fs[a:b]))
+        for qx, kx, vx, cux in sets:
+            ps = []
+            for dst, src in ((kx, pk), (vx, pv)):
+                fd, fs = dst.view(-1), src.view(-1)
+                n = fd.numel()
+                for i in range(ncs):
+                    a_, b_ = n * i // ncs, n * (i + 1) // ncs
+                    ps.append((i, fd[a_:b_], fs[a_:b_]))
+            pieces.append(ps)
+        read_done = [None] * nbuf   # per set: the event after the last call that read it
+        step_no = [0]
 
         def e2e_step():
-            start = torch.cuda.Event()
-            start.record(stream)   # after the previous step's call: its K/V reads are done
+            si = step_no[0] % nbuf
+            step_no[0] += 1
+            qx, kx, vx, cux = sets[si]
             joins = []
             for i, cs in enumerate(copy_streams):
-                cs.wait_event(start)
+                if read_done[si] is not None:
+                    cs.wait_event(read_done[si])   # the set's previous reader is done with it
                 with torch.cuda.stream(cs):
-                    for j, d_, s_ in pieces:
+                    for j, d_, s_ in pieces[si]:
                         if j == i:
                             d_.copy_(s_, non_blocking=True)
                 ev = torch.cuda.Event()
                 ev.record(cs)
                 joins.append(ev)
-            q.copy_(pq, non_blocking=True)
-            cu.copy_(pcu, non_blocking=True)
+            qx.copy_(pq, non_blocking=True)
+            cux.copy_(pcu, non_blocking=True)
             for ev in joins:
                 stream.wait_event(ev)
-            call()
+            call((qx, kx, vx, cux))
+            done = torch.cuda.Event()
+            done.record(stream)
+            read_done[si] = done
             hout.copy_(out, non_blocking=True)
 
         with torch.cuda.stream(stream):
@@ -649,6 +670,8 @@ def main():
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
+            for cs in copy_streams:
+                cs.wait_event(e0)   # no copy of the timed steps starts before the clock
             for _ in range(args.e2e_steps):
                 e2e_step()
             e1.record(stream)
@@ -659,7 +682,7 @@ def main():
                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": hout.numel() * hout.element_size(),
                "api": "decode_attn_splitkv (C ABI), pinned host buffers",
-               "copy_streams": ncs}
+               "copy_streams": ncs, "input_sets": nbuf}
 
     if rank != 0:
         return
