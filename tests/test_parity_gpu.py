@@ -355,3 +355,36 @@ def test_empty_cache_without_kv_buffers():
     da.decode_attn_splitkv(q, k, v, cu2, out, ws, num_splits=S)
     assert da.decode_attn_splitkv_get_error(ws) & da.DA_DEVERR_SEQLENS
     assert not out.any()
+
+
+def test_one_workspace_across_calls_of_every_kind():
+    """One workspace, sized for the largest call, reused by calls of every kind in a row: uniform
+    splits (ragged and even batches, so both queue orders), per-sequence counts, several query
+    tokens, one split. The work queue must come back to zero after each call whatever its item
+    count (the last take resets it); every output against the oracle."""
+    orc = oracle.default()
+    ragged = custom("reuse_r", 5, 28, 4, 128, [700, 3000, 65, 1, 1500], "f16", LAYOUT_VARLEN, None, seed=51)
+    even = custom("reuse_e", 3, 16, 4, 128, [640, 640, 640], "f16", LAYOUT_VARLEN, None, seed=52)
+    multi = custom("reuse_m", 2, 28, 4, 128, [900, 300], "f16", LAYOUT_VARLEN, None, seed=53, tq=4)
+    ws = da.alloc_workspace(8 * 4, 28, 128, 16)
+    for rep in range(2):
+        for p, kind, arg in ((ragged, "uniform", 7), (even, "uniform", 3), (ragged, "var", 256),
+                             (multi, "mq", 2), (even, "uniform", 1), (multi, "mqvar", 200), (ragged, "uniform", 16)):
+            q, k, v, cu = to_device(p)
+            tq = p.tq
+            out = torch.empty(p.B, tq, p.Hq, p.D, dtype=torch.float16, device="cuda")
+            if kind == "uniform":
+                da.decode_attn_splitkv(q, k, v, cu, out.view(p.B, p.Hq, p.D), ws, num_splits=arg, scale=p.scale)
+            elif kind == "var":
+                da.decode_attn_splitkv_varsplit(q, k, v, cu, out.view(p.B, p.Hq, p.D), ws, split_len=arg,
+                                                max_splits=16, scale=p.scale)
+            elif kind == "mq":
+                da.decode_attn_splitkv_multiquery(q.view(p.B, tq, p.Hq, p.D), k, v, cu, out, ws, num_splits=arg,
+                                                  scale=p.scale)
+            else:
+                da.decode_attn_splitkv_multiquery_varsplit(q.view(p.B, tq, p.Hq, p.D), k, v, cu, out, ws,
+                                                           split_len=arg, max_splits=16, scale=p.scale)
+            assert da.decode_attn_splitkv_get_error(ws) == 0, (rep, kind)
+            ref = orc.attention_mq(p, tq)[0] if tq > 1 else orc.attention(p)[0][:, None]
+            got = out.to(torch.float64).cpu().numpy()
+            assert out_excess(got, ref, p.dtype) <= OUT_TOL, (rep, kind, arg)
