@@ -997,6 +997,7 @@ da_status launch_split_tc(const Call& c, void* out, cudaStream_t stream) {
     p.stage_cu = c.B <= kMaxStagedBatch;
     p.sorted = 0;   // this kernel's producer hands out items in index order
     p.prefix_off = -1;   // and keeps prefix[] in an area of its own
+    p.keep_partials = 0;
     p.scale_log2 = c.scale * kLog2e;
     p.wait_limit_ns = kWaitLimitNs;
 

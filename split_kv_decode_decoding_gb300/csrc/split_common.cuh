@@ -97,6 +97,8 @@ struct SplitParams {
     int split_len;           // 0: every sequence has S splits; else S_b = min(S, ceil(L_b / split_len))
     int stage_cu;            // cu_seqlens_k staged in shared memory (B small enough)
     int sorted;              // the producer hands out sequences longest first (see kMaxSortedBatch)
+    int keep_partials;       // store the partials that the combine reads back with an L2 evict-last
+                             // hint (the K/V stream is larger than the L2 and would evict them)
     int prefix_off;          // per-sequence mode: prefix[] at this int32 offset in the staged
                              // cu_seqlens_k area, or -1: in an area of its own past it
     int tq;                  // query tokens per sequence; columns per KV head = G * tq
@@ -749,8 +751,22 @@ __device__ __forceinline__ void merge_write(const SplitParams& p, const ItemSlot
         if (live) {
             const int64_t qrow = column_row(p, item, kHeadsPerCta * n + hh);
             const int64_t row = qrow * p.S + item.s;
-            *reinterpret_cast<float4*>(p.opart + row * D + d0) = o;
-            if (d0 == 0) p.lse[row] = M == -INFINITY ? -INFINITY : (M + fast_log2(lsum)) * kLn2;
+            const float lse = M == -INFINITY ? -INFINITY : (M + fast_log2(lsum)) * kLn2;
+            if (item.valid == 1 && p.keep_partials) {
+                // the combine reads these back after the whole K/V stream: ask the L2 to
+                // keep them ahead of the streamed lines
+                uint64_t keep;
+                asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
+                asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p.opart + row * D + d0),
+                             "f"(o.x), "f"(o.y), "f"(o.z), "f"(o.w), "l"(keep)
+                             : "memory");
+                if (d0 == 0)
+                    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p.lse + row), "f"(lse), "l"(keep)
+                                 : "memory");
+            } else {
+                *reinterpret_cast<float4*>(p.opart + row * D + d0) = o;
+                if (d0 == 0) p.lse[row] = lse;
+            }
             // the sequence's only split: its weight exp(lse_0 - lse) is 1, so o_0 is the answer
             if (p.out != nullptr && item.valid == 2)
                 *reinterpret_cast<uint2*>(p.out + qrow * D + d0) = make_uint2(pack2<DT>(o.x, o.y), pack2<DT>(o.z, o.w));
@@ -811,6 +827,14 @@ inline bool make_kv_map(CUtensorMap* map, const void* base, da_dtype dt, da_layo
 
 // Per-kernel, per-device launch facts: the dynamic shared-memory limit is
 // raised once per device and the persistent grid size is cached.
+// L2 size of the current device (bytes; 0 if it cannot be queried).
+inline int device_l2_bytes() {
+    int dev = 0, l2 = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
+        return 0;
+    return l2;
+}
+
 struct DeviceCache {
     std::atomic<uint64_t> attr_done{0};
     std::atomic<int> grid[64] = {};
@@ -978,6 +1002,11 @@ inline bool prepare_split(const Call& c, void* out, SplitLaunch& a) {
     p.n_items = c.B * c.Hkv * p.chunks * c.S;   // per-sequence mode: an upper bound (the kernel counts)
     p.split_len = c.split_len;
     p.stage_cu = c.B <= kMaxStagedBatch;
+    {
+        // K/V bytes the call may stream (BHSD: the slabs' capacity) against the L2
+        const double kv = 4.0 * c.D * c.Hkv * (c.lay == DA_LAYOUT_VARLEN ? 1.0 : static_cast<double>(c.B)) * c.kv_rows;
+        p.keep_partials = kv > static_cast<double>(device_l2_bytes());
+    }
     p.sorted = c.split_len == 0 && c.lay == DA_LAYOUT_VARLEN && c.B > 1 && c.B <= kMaxSortedBatch && p.stage_cu;
     p.scale_log2 = c.scale * kLog2e;
     p.wait_limit_ns = kWaitLimitNs;
