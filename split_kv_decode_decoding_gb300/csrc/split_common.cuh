@@ -752,9 +752,12 @@ __device__ __forceinline__ void merge_write(const SplitParams& p, const ItemSlot
             const int64_t qrow = column_row(p, item, kHeadsPerCta * n + hh);
             const int64_t row = qrow * p.S + item.s;
             const float lse = M == -INFINITY ? -INFINITY : (M + fast_log2(lsum)) * kLn2;
-            if (item.valid == 1 && p.keep_partials) {
-                // the combine reads these back after the whole K/V stream: ask the L2 to
-                // keep them ahead of the streamed lines
+            // the sequence's only split: its weight exp(lse_0 - lse) is 1, so o_0 is the answer
+            const bool direct = p.out != nullptr && item.valid == 2;
+            if (p.keep_partials) {
+                // A K/V stream larger than the L2: the item's writes go to the L2 with an
+                // evict-last policy, so that they are not written back to DRAM in the middle
+                // of the stream (and the combine finds the partials it reads back there)
                 uint64_t keep;
                 asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
                 asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p.opart + row * D + d0),
@@ -763,13 +766,17 @@ __device__ __forceinline__ void merge_write(const SplitParams& p, const ItemSlot
                 if (d0 == 0)
                     asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p.lse + row), "f"(lse), "l"(keep)
                                  : "memory");
+                if (direct)
+                    asm volatile("st.global.L2::cache_hint.v2.u32 [%0], {%1, %2}, %3;" ::"l"(p.out + qrow * D + d0),
+                                 "r"(pack2<DT>(o.x, o.y)), "r"(pack2<DT>(o.z, o.w)), "l"(keep)
+                                 : "memory");
             } else {
                 *reinterpret_cast<float4*>(p.opart + row * D + d0) = o;
                 if (d0 == 0) p.lse[row] = lse;
+                if (direct)
+                    *reinterpret_cast<uint2*>(p.out + qrow * D + d0) =
+                        make_uint2(pack2<DT>(o.x, o.y), pack2<DT>(o.z, o.w));
             }
-            // the sequence's only split: its weight exp(lse_0 - lse) is 1, so o_0 is the answer
-            if (p.out != nullptr && item.valid == 2)
-                *reinterpret_cast<uint2*>(p.out + qrow * D + d0) = make_uint2(pack2<DT>(o.x, o.y), pack2<DT>(o.z, o.w));
         }
     }
 }
