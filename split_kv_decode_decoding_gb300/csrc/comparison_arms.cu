@@ -287,7 +287,7 @@ split_kernel_fma(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
                 if (zeroed) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty0 + 8 * st);
-                if (++st == p.ring) {
+                if (++st == kStages) {
                     st = 0;
                     ph ^= 1;
                 }
@@ -329,7 +329,7 @@ split_kernel_fma(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * st);
-        if (++st == p.ring) {
+        if (++st == kStages) {
             st = 0;
             ph ^= 1;
         }
@@ -998,7 +998,6 @@ da_status launch_split_tc(const Call& c, void* out, cudaStream_t stream) {
     p.sorted = 0;   // this kernel's producer hands out items in index order
     p.prefix_off = -1;   // and keeps prefix[] in an area of its own
     p.keep_partials = 0;
-    p.ring = TcShape<D>::kStages;   // its own ring (the shared producer is not used)
     p.scale_log2 = c.scale * kLog2e;
     p.wait_limit_ns = kWaitLimitNs;
 

@@ -230,7 +230,7 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty0 + 8 * st);
-                if (++st == p.ring) {
+                if (++st == Sh::kStages) {
                     st = 0;
                     ph ^= 1;
                 }
@@ -436,7 +436,7 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty0 + 8 * st);
-                if (++st == p.ring) {
+                if (++st == Sh::kStages) {
                     st = 0;
                     ph ^= 1;
                 }
@@ -504,7 +504,7 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * st);
-        if (++st == p.ring) {
+        if (++st == Sh::kStages) {
             st = 0;
             ph ^= 1;
         }

@@ -102,8 +102,6 @@ struct SplitParams {
     int prefix_off;          // per-sequence mode: prefix[] at this int32 offset in the staged
                              // cu_seqlens_k area, or -1: in an area of its own past it
     int tq;                  // query tokens per sequence; columns per KV head = G * tq
-    int ring;                // ring stages in use (at most the kernel's): the producer and the
-                             // consumers wrap at it
     float scale_log2;        // scale * log2(e)
     unsigned long long wait_limit_ns;
 };
@@ -630,7 +628,7 @@ __device__ __forceinline__ void split_producer(const SplitLayout& sl, const Spli
             // last tile: the atomic's round trip then overlaps the last copies, yet a
             // CTA never holds a reserved item for long (which would hurt the balance
             // at the end of the queue).
-            const int fetch_at = max(0, item.ntiles - p.ring);
+            const int fetch_at = max(0, item.ntiles - Sh::kStages);
             int next_idx = 0;
             if (item.ntiles == 0) next_idx = take_next();
             bool ok = true;
@@ -678,7 +676,7 @@ __device__ __forceinline__ void split_producer(const SplitLayout& sl, const Spli
                         }
                     }
                 }
-                if (++st == p.ring) {
+                if (++st == Sh::kStages) {
                     st = 0;
                     ph ^= 1;
                 }
@@ -695,7 +693,7 @@ __device__ __forceinline__ void split_producer(const SplitLayout& sl, const Spli
                 break;
             }
             mbar_arrive(full0 + 8 * st);
-            if (++st == p.ring) {
+            if (++st == Sh::kStages) {
                 st = 0;
                 ph ^= 1;
             }
@@ -847,11 +845,10 @@ inline int device_l2_bytes() {
 struct DeviceCache {
     std::atomic<uint64_t> attr_done{0};
     std::atomic<int> grid[64] = {};
-    std::atomic<int> per_sm[64] = {};
 };
 
 template <class K>
-cudaError_t persistent_grid(K kernel, int threads, int smem, DeviceCache& cache, int* grid, int* per_sm_out = nullptr) {
+cudaError_t persistent_grid(K kernel, int threads, int smem, DeviceCache& cache, int* grid) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -878,11 +875,9 @@ cudaError_t persistent_grid(K kernel, int threads, int smem, DeviceCache& cache,
         if (e != cudaSuccess) return e;
         if (per_sm < 1) return cudaErrorInvalidConfiguration;
         cache.grid[dev].store(sms * per_sm, std::memory_order_relaxed);
-        cache.per_sm[dev].store(per_sm, std::memory_order_relaxed);
         cache.attr_done.fetch_or(bit, std::memory_order_acq_rel);
     }
     *grid = cache.grid[dev].load(std::memory_order_relaxed);
-    if (per_sm_out != nullptr) *per_sm_out = cache.per_sm[dev].load(std::memory_order_relaxed);
     return cudaSuccess;
 }
 
@@ -973,7 +968,6 @@ struct SplitLaunch {
     SplitParams p;
     int smem;        // dynamic shared memory, bytes
     int cache_idx;   // which DeviceCache: the number of [B + 1] arrays staged in shared memory
-    int lean_ring;   // ring stages to use when every CTA of a grid of two or more per SM has an item
 };
 
 // `out` (nullptr for the split step alone) gets the rows of every sequence that has
@@ -1023,14 +1017,6 @@ inline bool prepare_split(const Call& c, void* out, SplitLaunch& a) {
     p.sorted = c.split_len == 0 && c.lay == DA_LAYOUT_VARLEN && c.B > 1 && c.B <= kMaxSortedBatch && p.stage_cu;
     p.scale_log2 = c.scale * kLog2e;
     p.wait_limit_ns = kWaitLimitNs;
-    // The whole ring by default. One-column-block items at head_dim 128 stream with
-    // two stages when two or more CTAs per SM all have work (launch_persistent):
-    // fewer bytes in flight per SM there measured faster, while a lone CTA on an SM,
-    // or the 16-column consumers, keep all three. Per-sequence mode keeps them too:
-    // its item count is known only on the device (n_items is a bound), and a batch
-    // with fewer items than CTAs leaves CTAs alone on their SMs.
-    p.ring = ST;
-    a.lean_ring = NT == 1 && D == 128 && c.split_len == 0 ? std::min(2, ST) : ST;
     const bool var = c.split_len != 0;
     // per-sequence mode: prefix[] shares the staged cu_seqlens_k area, past its B + 1
     // entries, when it fits there, so that the 16-column kernel still runs two CTAs
@@ -1047,11 +1033,9 @@ inline bool prepare_split(const Call& c, void* out, SplitLaunch& a) {
 // at most one per work item, with programmatic dependent launch.
 template <class K>
 inline da_status launch_persistent(K kern, const SplitLaunch& a, DeviceCache& cache, cudaStream_t stream) {
-    int grid = 0, per_sm = 0;
-    if (persistent_grid(kern, kThreads, a.smem, cache, &grid, &per_sm) != cudaSuccess) return DA_ERR_CUDA;
-    SplitParams p = a.p;
-    if (per_sm >= 2 && p.n_items >= grid) p.ring = a.lean_ring;
-    grid = std::min(grid, p.n_items);
+    int grid = 0;
+    if (persistent_grid(kern, kThreads, a.smem, cache, &grid) != cudaSuccess) return DA_ERR_CUDA;
+    grid = std::min(grid, a.p.n_items);
     cudaLaunchAttribute attrs[1] = {pdl_attr()};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
@@ -1060,7 +1044,7 @@ inline da_status launch_persistent(K kern, const SplitLaunch& a, DeviceCache& ca
     cfg.stream = stream;
     cfg.attrs = attrs;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a.mk, a.mv, a.mk16, a.mv16, p) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
+    return cudaLaunchKernelEx(&cfg, kern, a.mk, a.mv, a.mk16, a.mv16, a.p) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
 }
 
 // The combine step over a call's workspace (decode_attn_splitkv.cu).
