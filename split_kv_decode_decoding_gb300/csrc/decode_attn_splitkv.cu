@@ -371,27 +371,35 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
                     }
                     const int key_lo = t * kStageKeys + warp * kBoxKeys + g;   // relative to split start
                     uint32_t pb0[NT], pb1[NT];
+                    // scores -> exp2 domain, mask keys past the split end
+                    float x[NT][4], mx0[NT], mx1[NT];
+                    bool move = false;
     #pragma unroll
                     for (int n = 0; n < NT; ++n) {
-                        // scores -> exp2 domain, mask keys past the split end
-                        const float x0 = key_lo < visA[n] ? (sc[n][0] + sd[n][0]) * p.scale_log2 : -INFINITY;
-                        const float x1 = key_lo < visB[n] ? (sc[n][1] + sd[n][1]) * p.scale_log2 : -INFINITY;
-                        const float x2 = key_lo + 8 < visA[n] ? (sc[n][2] + sd[n][2]) * p.scale_log2 : -INFINITY;
-                        const float x3 = key_lo + 8 < visB[n] ? (sc[n][3] + sd[n][3]) * p.scale_log2 : -INFINITY;
-                        // Lazy reference: a column's running max m_run moves only when some score
-                        // of the warp's box exceeds it by more than kLazyRescale (log2 units), so
-                        // the shuffle reduction and the accumulator rescale run on a few boxes
-                        // per item; the weights stay below 2^kLazyRescale, well inside the fp16
-                        // and bf16 range, and every sum below shares the same reference.
-                        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
-                        if (__any_sync(0xffffffffu, mx0 > m_run[n][0] + kLazyRescale ||
-                                                        mx1 > m_run[n][1] + kLazyRescale)) {
+                        x[n][0] = key_lo < visA[n] ? (sc[n][0] + sd[n][0]) * p.scale_log2 : -INFINITY;
+                        x[n][1] = key_lo < visB[n] ? (sc[n][1] + sd[n][1]) * p.scale_log2 : -INFINITY;
+                        x[n][2] = key_lo + 8 < visA[n] ? (sc[n][2] + sd[n][2]) * p.scale_log2 : -INFINITY;
+                        x[n][3] = key_lo + 8 < visB[n] ? (sc[n][3] + sd[n][3]) * p.scale_log2 : -INFINITY;
+                        mx0[n] = fmaxf(x[n][0], x[n][2]);
+                        mx1[n] = fmaxf(x[n][1], x[n][3]);
+                        move = move || mx0[n] > m_run[n][0] + kLazyRescale || mx1[n] > m_run[n][1] + kLazyRescale;
+                    }
+                    // Lazy reference: a column's running max m_run moves only when some score
+                    // of the warp's box exceeds it by more than kLazyRescale (log2 units), so
+                    // the shuffle reduction and the accumulator rescale run on a few boxes per
+                    // item; one vote covers every n-tile, and all of them move together (a
+                    // column whose max did not rise keeps its reference: al = 1). The weights
+                    // stay below 2^kLazyRescale, well inside the fp16 and bf16 range, and every
+                    // sum below shares the same reference.
+                    if (__any_sync(0xffffffffu, move)) {
+    #pragma unroll
+                        for (int n = 0; n < NT; ++n) {
     #pragma unroll
                             for (int off = 4; off < 32; off <<= 1) {
-                                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                                mx0[n] = fmaxf(mx0[n], __shfl_xor_sync(0xffffffffu, mx0[n], off));
+                                mx1[n] = fmaxf(mx1[n], __shfl_xor_sync(0xffffffffu, mx1[n], off));
                             }
-                            const float mn0 = fmaxf(m_run[n][0], mx0), mn1 = fmaxf(m_run[n][1], mx1);
+                            const float mn0 = fmaxf(m_run[n][0], mx0[n]), mn1 = fmaxf(m_run[n][1], mx1[n]);
                             // a column that has seen no key yet (several query tokens) keeps -inf:
                             // 0 stands in as its reference so that no weight below is NaN
                             const float ms0 = mn0 == -INFINITY ? 0.f : mn0, ms1 = mn1 == -INFINITY ? 0.f : mn1;
@@ -408,10 +416,13 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
                             m_run[n][0] = mn0;
                             m_run[n][1] = mn1;
                         }
+                    }
+    #pragma unroll
+                    for (int n = 0; n < NT; ++n) {
                         const float ms0 = m_run[n][0] == -INFINITY ? 0.f : m_run[n][0];
                         const float ms1 = m_run[n][1] == -INFINITY ? 0.f : m_run[n][1];
-                        const float p0 = fast_exp2(x0 - ms0), p1 = fast_exp2(x1 - ms1);
-                        const float p2 = fast_exp2(x2 - ms0), p3 = fast_exp2(x3 - ms1);
+                        const float p0 = fast_exp2(x[n][0] - ms0), p1 = fast_exp2(x[n][1] - ms1);
+                        const float p2 = fast_exp2(x[n][2] - ms0), p3 = fast_exp2(x[n][3] - ms1);
                         l_run[n][0] += p0 + p2;
                         l_run[n][1] += p1 + p3;
                         // P^T operand (k16 keys x n8 columns) via 8x8 transposes of the score fragment
