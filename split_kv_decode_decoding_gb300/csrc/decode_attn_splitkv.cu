@@ -314,10 +314,15 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
             for (int i = 0; i < D / 16; ++i)
     #pragma unroll
                 for (int n = 0; n < NT; ++n) acc[i][n][0] = acc[i][n][1] = acc[i][n][2] = acc[i][n][3] = 0.f;
-            float m_run[NT][2], l_run[NT][2];   // columns 8n + 2*t4 (+1): running max (log2 domain), sum share
+            // columns 8n + 2*t4 (+1): running max (log2 domain), sum share. A column that has
+            // seen no key holds kNoKey, a finite stand-in for -inf: it is the reference of its
+            // weights as it is (exp2(-inf - kNoKey) = 0, and the first key's rescale weighs
+            // the empty state exp2(kNoKey - m) = 0), and it becomes -inf again at the merge.
+            constexpr float kNoKey = -1e30f;
+            float m_run[NT][2], l_run[NT][2];
     #pragma unroll
             for (int n = 0; n < NT; ++n) {
-                m_run[n][0] = m_run[n][1] = -INFINITY;
+                m_run[n][0] = m_run[n][1] = kNoKey;
                 l_run[n][0] = l_run[n][1] = 0.f;
             }
 
@@ -399,11 +404,9 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
                                 mx0[n] = fmaxf(mx0[n], __shfl_xor_sync(0xffffffffu, mx0[n], off));
                                 mx1[n] = fmaxf(mx1[n], __shfl_xor_sync(0xffffffffu, mx1[n], off));
                             }
+                            // a column that has still seen no key keeps kNoKey (al = 1 on zeros)
                             const float mn0 = fmaxf(m_run[n][0], mx0[n]), mn1 = fmaxf(m_run[n][1], mx1[n]);
-                            // a column that has seen no key yet (several query tokens) keeps -inf:
-                            // 0 stands in as its reference so that no weight below is NaN
-                            const float ms0 = mn0 == -INFINITY ? 0.f : mn0, ms1 = mn1 == -INFINITY ? 0.f : mn1;
-                            const float al0 = fast_exp2(m_run[n][0] - ms0), al1 = fast_exp2(m_run[n][1] - ms1);
+                            const float al0 = fast_exp2(m_run[n][0] - mn0), al1 = fast_exp2(m_run[n][1] - mn1);
                             l_run[n][0] *= al0;
                             l_run[n][1] *= al1;
     #pragma unroll
@@ -419,10 +422,8 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
                     }
     #pragma unroll
                     for (int n = 0; n < NT; ++n) {
-                        const float ms0 = m_run[n][0] == -INFINITY ? 0.f : m_run[n][0];
-                        const float ms1 = m_run[n][1] == -INFINITY ? 0.f : m_run[n][1];
-                        const float p0 = fast_exp2(x[n][0] - ms0), p1 = fast_exp2(x[n][1] - ms1);
-                        const float p2 = fast_exp2(x[n][2] - ms0), p3 = fast_exp2(x[n][3] - ms1);
+                        const float p0 = fast_exp2(x[n][0] - m_run[n][0]), p1 = fast_exp2(x[n][1] - m_run[n][1]);
+                        const float p2 = fast_exp2(x[n][2] - m_run[n][0]), p3 = fast_exp2(x[n][3] - m_run[n][1]);
                         l_run[n][0] += p0 + p2;
                         l_run[n][1] += p1 + p3;
                         // P^T operand (k16 keys x n8 columns) via 8x8 transposes of the score fragment
@@ -485,8 +486,8 @@ split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CU
                     ++md;
                 }
                 if (g == 0) {
-                    red_m[warp * 8 + 2 * t4] = m_run[n][0];
-                    red_m[warp * 8 + 2 * t4 + 1] = m_run[n][1];
+                    red_m[warp * 8 + 2 * t4] = m_run[n][0] == kNoKey ? -INFINITY : m_run[n][0];
+                    red_m[warp * 8 + 2 * t4 + 1] = m_run[n][1] == kNoKey ? -INFINITY : m_run[n][1];
                     red_l[warp * 8 + 2 * t4] = l_run[n][0];
                     red_l[warp * 8 + 2 * t4 + 1] = l_run[n][1];
                 }
