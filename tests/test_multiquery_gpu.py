@@ -47,6 +47,11 @@ CASES = [
     ("one_split_direct", 3, 2, 8, 2, 64, [1, 2, 3], "bf16", LAYOUT_VARLEN, 1, 0),
     # 20 columns per KV head: a 16-column item and a 4-column one, over NaN-padded slabs
     ("bhsd_g4_tq5", 2, 5, 16, 4, 128, [500, 37], "bf16", LAYOUT_BHSD, 3, 512),
+    # 16-column items at head_dim 128 whose columns see no key of a split: with 7 keys in 6
+    # splits ([5, 7) the last), token 0 sees keys [0, 5) only, so its last split is empty
+    # (lse -inf) while the item's other columns have keys
+    ("d128_g4_tq3_unseen_split", 2, 3, 16, 4, 128, [7, 40], "bf16", LAYOUT_VARLEN, 6, 0),
+    ("d128_g4_tq3_unseen_split_bhsd", 2, 3, 16, 4, 128, [7, 40], "f16", LAYOUT_BHSD, 6, 64),
 ]
 
 
